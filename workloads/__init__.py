@@ -1,0 +1,307 @@
+"""Seeded synthetic inputs for paged decode attention.
+
+This module builds INPUTS only: query rows, per-token K/V rows, context lengths,
+block tables and the slot of every token a caller would append. It holds none of
+the attention, softmax or quantisation arithmetic: both the CUDA library and the
+CPU oracle receive what this module produces and do their own work on it.
+
+Shapes follow the layer geometries the source pages use:
+  * "LLM 推理底层：KV Cache 显存几何、GQA/MLA 压缩与 PagedAttention 调度"
+    (blog.faulkner.fun), section "KV Cache 容量公式": Llama-3-70B with
+    n_h=64, n_kv=8, d_h=128, B=16, S=8192.
+  * "【infra之路】10-PagedAttention 与 KV Cache 管理" (qwbw.cn), §2.1 and §5:
+    LLaMA-7B with 32 KV heads, head_dim 128 and block_size 16.
+  * "kv-cache-guide" (guijiagi.com), §2.3 table: LLaMA-2/3 layer shapes.
+
+Block tables are a seeded random permutation of the physical pool dealt out in
+sequence order, so consecutive logical blocks land on scattered physical blocks,
+as the block-table figure of qwbw.cn §3.3 shows.
+
+Token rows are generated per "stream" with a generator seeded from
+(workload seed, stream id), so any one sequence's K/V history can be rebuilt on
+its own without generating the whole pool. A stream is either one sequence's
+private tokens or one group's shared prefix.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Iterator, Optional
+
+import numpy as np
+import torch
+
+BLOCK_SIZE = 16
+
+
+@dataclass(frozen=True)
+class Geometry:
+    """Per-layer attention geometry: query heads, KV heads, head dim, KV dtype."""
+
+    n_h: int
+    n_kv: int
+    d_h: int
+    block_size: int = BLOCK_SIZE
+    kv_dtype: str = "bf16"  # "bf16" or "int8"
+
+    @property
+    def g(self) -> int:
+        return self.n_h // self.n_kv
+
+
+@dataclass
+class Workload:
+    """One decode step's worth of paged-attention inputs.
+
+    context_lens[b] counts every token of sequence b INCLUDING the new token,
+    which sits at position context_lens[b]-1 and is appended by the step itself.
+    Positions 0..context_lens[b]-2 are history that is written into the pool
+    before the step (``history_chunks``).
+    """
+
+    name: str
+    geom: Geometry
+    seed: int
+    context_lens: np.ndarray          # int32 [B]
+    block_tables: np.ndarray          # int32 [B, max_blocks]; unused entries = -1
+    num_blocks: int
+    scale: float
+    prefix_len: np.ndarray            # int32 [B]: shared-prefix tokens of each seq (0 = none)
+    group: np.ndarray                 # int32 [B]: shared-prefix group id (-1 = none)
+    description: str = ""
+    # streams are generated lazily; cache of (stream id) -> (k, v) on a device
+    _cache: dict = field(default_factory=dict, repr=False)
+
+    # ------------------------------------------------------------------ sizes
+    @property
+    def B(self) -> int:
+        return int(self.context_lens.shape[0])
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.B else 0
+
+    def num_seq_blocks(self, b: int) -> int:
+        return -(-int(self.context_lens[b]) // self.geom.block_size)
+
+    # ---------------------------------------------------------------- streams
+    def _stream_seed(self, stream: int) -> int:
+        return (self.seed * 1_000_003 + 7919 * (stream + 1)) & 0x7FFF_FFFF_FFFF
+
+    def _gen_rows(self, stream: int, n: int, device) -> tuple[torch.Tensor, torch.Tensor]:
+        gen = torch.Generator(device=device)
+        gen.manual_seed(self._stream_seed(stream))
+        shape = (n, self.geom.n_kv, self.geom.d_h)
+        k = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+        v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+        return k, v
+
+    def _prefix_stream(self, grp: int) -> int:
+        return 1_000_000 + grp
+
+    def seq_kv(self, b: int, device="cpu") -> tuple[torch.Tensor, torch.Tensor]:
+        """K and V rows of every position of sequence b: bf16 [ctx_b, n_kv, d_h]."""
+        ctx = int(self.context_lens[b])
+        p = int(self.prefix_len[b])
+        ks, vs = [], []
+        if p > 0:
+            kp, vp = self._gen_rows(self._prefix_stream(int(self.group[b])), p, device)
+            ks.append(kp)
+            vs.append(vp)
+        ko, vo = self._gen_rows(b, ctx - p, device)
+        ks.append(ko)
+        vs.append(vo)
+        return torch.cat(ks, 0), torch.cat(vs, 0)
+
+    def q(self, device="cpu") -> torch.Tensor:
+        """Query rows of the step: bf16 [B, n_h, d_h]."""
+        gen = torch.Generator(device=device)
+        gen.manual_seed(self._stream_seed(2_000_000))
+        x = torch.randn((self.B, self.geom.n_h, self.geom.d_h), generator=gen, device=device)
+        return x.to(torch.bfloat16)
+
+    # ------------------------------------------------------------------ slots
+    def slot_of(self, b: int, pos: np.ndarray) -> np.ndarray:
+        """Slot a block manager hands out for position(s) pos of sequence b.
+
+        This is the caller-side input of the cache append (the block manager
+        owns the table; it tells the kernel where each new row goes).
+        """
+        bs = self.geom.block_size
+        pos = np.asarray(pos, dtype=np.int64)
+        return self.block_tables[b, pos // bs].astype(np.int64) * bs + pos % bs
+
+    def new_token_slots(self) -> np.ndarray:
+        """int64 [B]: slot of each sequence's new token (position ctx-1)."""
+        return np.array([self.slot_of(b, np.array([self.context_lens[b] - 1]))[0]
+                         for b in range(self.B)], dtype=np.int64)
+
+    def new_kv(self, device="cpu") -> tuple[torch.Tensor, torch.Tensor]:
+        """K/V rows of the new token of every sequence: bf16 [B, n_kv, d_h]."""
+        ks, vs = [], []
+        for b in range(self.B):
+            ctx = int(self.context_lens[b])
+            p = int(self.prefix_len[b])
+            assert ctx - 1 >= p, "new token must be private to its sequence"
+            ko, vo = self._gen_rows(b, ctx - p, device)
+            ks.append(ko[-1])
+            vs.append(vo[-1])
+        return torch.stack(ks), torch.stack(vs)
+
+    def history_chunks(self, device="cpu", max_rows: int = 1 << 20,
+                       seqs: Optional[list[int]] = None
+                       ) -> Iterator[tuple[torch.Tensor, torch.Tensor, np.ndarray]]:
+        """Yield (k, v, slots) covering every history position exactly once.
+
+        History = positions 0..ctx-2 of each sequence. A shared prefix is
+        yielded once, by the first sequence of its group. ``seqs`` restricts the
+        output to those sequences (their shared prefix included).
+        """
+        done_groups = set()
+        order = range(self.B) if seqs is None else seqs
+        for b in order:
+            ctx = int(self.context_lens[b])
+            p = int(self.prefix_len[b])
+            grp = int(self.group[b])
+            if p > 0 and grp not in done_groups:
+                done_groups.add(grp)
+                k, v = self._gen_rows(self._prefix_stream(grp), p, device)
+                yield from self._chunk(k, v, self.slot_of(b, np.arange(p)), max_rows)
+            n_priv = ctx - 1 - p
+            if n_priv > 0:
+                k, v = self._gen_rows(b, ctx - p, device)
+                yield from self._chunk(k[:n_priv], v[:n_priv],
+                                       self.slot_of(b, np.arange(p, ctx - 1)), max_rows)
+
+    @staticmethod
+    def _chunk(k, v, slots, max_rows):
+        for s in range(0, k.shape[0], max_rows):
+            yield k[s:s + max_rows], v[s:s + max_rows], slots[s:s + max_rows]
+
+    # ------------------------------------------------------------- accounting
+    def unique_blocks(self) -> int:
+        """Distinct physical blocks referenced by the block tables."""
+        ids = set()
+        for b in range(self.B):
+            ids.update(self.block_tables[b, :self.num_seq_blocks(b)].tolist())
+        return len(ids)
+
+    def logical_blocks(self) -> int:
+        return sum(self.num_seq_blocks(b) for b in range(self.B))
+
+
+# ---------------------------------------------------------------------------
+# builders
+# ---------------------------------------------------------------------------
+
+def _deal_tables(rng_perm: np.ndarray, context_lens: np.ndarray, block_size: int,
+                 prefix_len: np.ndarray, group: np.ndarray, max_blocks: int) -> np.ndarray:
+    """Hand out physical IDs from a shuffled pool in sequence order.
+
+    Sequences of one prefix group reuse the group's prefix block IDs.
+    """
+    B = context_lens.shape[0]
+    tables = np.full((B, max_blocks), -1, dtype=np.int32)
+    nxt = 0
+    group_prefix: dict[int, np.ndarray] = {}
+    for b in range(B):
+        nblk = -(-int(context_lens[b]) // block_size)
+        pblk = int(prefix_len[b]) // block_size
+        col = 0
+        if pblk > 0:
+            grp = int(group[b])
+            if grp not in group_prefix:
+                group_prefix[grp] = rng_perm[nxt:nxt + pblk].copy()
+                nxt += pblk
+            tables[b, :pblk] = group_prefix[grp]
+            col = pblk
+        n = nblk - col
+        tables[b, col:nblk] = rng_perm[nxt:nxt + n]
+        nxt += n
+    assert nxt <= rng_perm.shape[0], "pool too small"
+    return tables
+
+
+def make_workload(name: str, geom: Geometry, context_lens, seed: int,
+                  pool_factor: float = 1.1, num_blocks: Optional[int] = None,
+                  prefix_len=None, group=None, scale: Optional[float] = None,
+                  extra_table_cols: int = 0, description: str = "") -> Workload:
+    """Build a workload from explicit context lengths.
+
+    pool_factor: the physical pool holds ceil(pool_factor * blocks needed) blocks
+    (unless num_blocks is given), so some blocks stay unused.
+    """
+    ctx = np.asarray(context_lens, dtype=np.int32)
+    B = ctx.shape[0]
+    bs = geom.block_size
+    pl = np.zeros(B, np.int32) if prefix_len is None else np.asarray(prefix_len, np.int32)
+    gr = np.full(B, -1, np.int32) if group is None else np.asarray(group, np.int32)
+    nblk = [-(-int(c) // bs) for c in ctx]
+    # blocks actually handed out (a shared prefix counts once per group)
+    needed = 0
+    seen = set()
+    for b in range(B):
+        pblk = int(pl[b]) // bs
+        if pblk and int(gr[b]) not in seen:
+            seen.add(int(gr[b]))
+            needed += pblk
+        needed += nblk[b] - pblk
+    if num_blocks is None:
+        num_blocks = max(1, math.ceil(pool_factor * needed))
+    assert num_blocks >= needed
+    gen = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(num_blocks, generator=gen).numpy().astype(np.int32)
+    max_blocks = max(nblk) + extra_table_cols if B else 1
+    tables = _deal_tables(perm, ctx, bs, pl, gr, max(max_blocks, 1))
+    if scale is None:
+        scale = 1.0 / math.sqrt(geom.d_h)
+    return Workload(name=name, geom=geom, seed=seed, context_lens=ctx, block_tables=tables,
+                    num_blocks=int(num_blocks), scale=float(scale), prefix_len=pl, group=gr,
+                    description=description)
+
+
+# ---------------------------------------------------------------------------
+# the five named workloads
+# ---------------------------------------------------------------------------
+
+CONFIG_NAMES = ["tiny", "llama3_8b", "llama3_70b", "llama2_7b_int8_prefix", "long_context"]
+
+
+def named_workload(name: str) -> Workload:
+    """The five layer-decode workloads, seeded with 94 + their index."""
+    idx = CONFIG_NAMES.index(name)
+    seed = 94 + idx
+    if name == "tiny":
+        return make_workload(
+            name, Geometry(n_h=4, n_kv=2, d_h=64), [5, 37], seed, num_blocks=8,
+            description="B=2, ctx {5,37}, n_h=4, n_kv=2, d_h=64, pool of 8 blocks")
+    if name == "llama3_8b":
+        rng = np.random.default_rng(seed)
+        ctx = rng.integers(512, 4096, size=64, endpoint=True)
+        return make_workload(
+            name, Geometry(n_h=32, n_kv=8, d_h=128), ctx, seed,
+            description="Llama-3-8B layer: B=64, ctx U[512,4096], n_h=32, n_kv=8, d_h=128, bf16")
+    if name == "llama3_70b":
+        return make_workload(
+            name, Geometry(n_h=64, n_kv=8, d_h=128), [8192] * 16, seed,
+            description="Llama-3-70B layer: B=16, ctx 8192, n_h=64, n_kv=8, d_h=128, bf16")
+    if name == "llama2_7b_int8_prefix":
+        rng = np.random.default_rng(seed)
+        suffix = np.clip(np.round(rng.lognormal(mean=6.0, sigma=1.0, size=32)), 16, 4096).astype(np.int64)
+        prefix = 2048
+        ctx = prefix + suffix
+        grp = np.repeat(np.arange(4), 8)
+        return make_workload(
+            name, Geometry(n_h=32, n_kv=32, d_h=128, kv_dtype="int8"), ctx, seed,
+            prefix_len=np.full(32, prefix), group=grp,
+            description="LLaMA-2-7B MHA layer, INT8 KV: B=32 in 4 groups of 8 sharing a "
+                        "2048-token prefix, suffix lognormal(6,1) clipped to [16,4096]")
+    if name == "long_context":
+        return make_workload(
+            name, Geometry(n_h=32, n_kv=8, d_h=128), [131072, 98304, 65536, 32768], seed,
+            description="long context: B=4, ctx {131072,98304,65536,32768}, n_h=32, n_kv=8, d_h=128")
+    raise KeyError(name)
