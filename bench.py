@@ -1,0 +1,422 @@
+#!/usr/bin/env python
+"""Benchmark of one paged decode step on GB300.
+
+A step is the whole hot path for one batch: pa_cache_write of every
+sequence's new token (slot-mapped append; INT8 quantise for an INT8 pool),
+then pa_decode (block-table gather, g-wide q.K, online softmax, P.V, split
+merge). Inputs are seeded synthetic tensors resident in HBM before timing.
+
+Metric: KV-read HBM GB/s of the step (algorithmic bytes / time), with the
+decode kernel's fraction of the measured HBM peak and sequences/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+With N > 1 (torchrun) every rank runs an independent replica of the same
+workload on its own GPU (the path has no cross-GPU exchange): weak scaling,
+value = bytes of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import CONFIG_NAMES, named_workload  # noqa: E402
+
+METRIC = "paged GQA decode attention: KV-read HBM GB/s, % of peak, seqs/s"
+DEFAULT_WORKLOAD = "llama3_8b"
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB of L2
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", choices=CONFIG_NAMES, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--num-ctas", type=int, default=0, help="force the decode split (tuning)")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------- bytes
+def kv_bytes_per_elem(w) -> int:
+    return 1 if w.geom.kv_dtype == "int8" else 2
+
+
+def decode_bytes(w, unique_blocks: bool = True) -> dict:
+    """Algorithmic bytes of one pa_decode launch.
+
+    Per sequence: ctx*2*n_kv*d_h*b_kv of K and V (+ ctx*2*n_kv*4 of fp32
+    scales for INT8), 4*ceil(ctx/16) of block table, 4 of context length, and
+    2*2*n_h*d_h of q and out. Shared prefix blocks count once (unique bytes).
+    """
+    g = w.geom
+    bkv = kv_bytes_per_elem(w)
+    per_token = 2 * g.n_kv * g.d_h * bkv + (2 * g.n_kv * 4 if g.kv_dtype == "int8" else 0)
+    tok_logical = int(w.context_lens.sum())
+    if unique_blocks:
+        # tokens in unique physical blocks (shared prefixes once)
+        seen = set()
+        tok = 0
+        for b in range(w.B):
+            ctx = int(w.context_lens[b])
+            for i in range(w.num_seq_blocks(b)):
+                blk = int(w.block_tables[b, i])
+                if blk in seen:
+                    continue
+                seen.add(blk)
+                tok += min(16, ctx - 16 * i)
+    else:
+        tok = tok_logical
+    blocks = sum(w.num_seq_blocks(b) for b in range(w.B))
+    other = 4 * blocks + 4 * w.B + 2 * 2 * w.B * g.n_h * g.d_h
+    return {"bytes": tok * per_token + other, "logical_bytes": tok_logical * per_token + other,
+            "flops": 4 * g.n_h * g.d_h * tok_logical}
+
+
+def cache_write_bytes(w) -> int:
+    """Bytes of one pa_cache_write of B new tokens: read k, v and slots, write rows."""
+    g = w.geom
+    rows = w.B * g.n_kv
+    read = 2 * rows * g.d_h * 2 + 8 * w.B
+    write = 2 * rows * g.d_h * kv_bytes_per_elem(w) + (2 * rows * 4 if g.kv_dtype == "int8" else 0)
+    return read + write
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_94_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """ncu DRAM bytes per decode launch, if recorded for the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(workload)
+    if not d or d.get("kernel_hash") != kernel_source_hash():
+        return None
+    return d.get("bytes_per_launch")
+
+
+# -------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# -------------------------------------------------------------------- oracle
+def oracle_sample(w, gen_device, seconds: float):
+    """Time the CPU oracle on a bounded sample of the workload's sequences.
+
+    Returns (bytes of the sample, seconds, description). The sample grows one
+    sequence at a time until about `seconds` of oracle time is spent.
+    """
+    import oracle
+    from oracle import Pool
+
+    g = w.geom
+    done_bytes, spent, seqs = 0, 0.0, []
+    order = list(range(w.B))
+    q_all = oracle.bf16_bits(w.q(gen_device))
+    per_token = 2 * g.n_kv * g.d_h * kv_bytes_per_elem(w) + (2 * g.n_kv * 4 if g.kv_dtype == "int8" else 0)
+    for b in order:
+        k, v = w.seq_kv(b, gen_device)
+        ctx = int(w.context_lens[b])
+        nblk = -(-ctx // 16)
+        pool = Pool(nblk, g.n_kv, g.d_h, 16, g.kv_dtype)
+        pool.write(oracle.bf16_bits(k), oracle.bf16_bits(v), np.arange(ctx))
+        table = np.arange(nblk, dtype=np.int32)[None]
+        t0 = time.perf_counter()
+        oracle.decode(q_all[b:b + 1], pool, table, np.array([ctx], np.int32), g.n_h, w.scale)
+        spent += time.perf_counter() - t0
+        done_bytes += ctx * per_token + 4 * nblk + 4 + 4 * g.n_h * g.d_h
+        seqs.append(b)
+        if spent >= seconds:
+            break
+    desc = (f"{len(seqs)} of {w.B} sequences ({int(sum(w.context_lens[s] for s in seqs))} tokens), "
+            f"single-threaded C fp64 oracle")
+    return done_bytes, spent, desc
+
+
+# ------------------------------------------------------------------- native
+def run_native(args, rank, world, local_rank):
+    import paged_kv_cache_94_gb300 as pa
+    from paged_kv_cache_94_gb300 import build as pa_build
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    pa_build.build()
+    w = named_workload(args.workload)
+    g = w.geom
+
+    # ---- resident inputs: pool with the history, the step's tensors
+    kc, vc, ks, vs = pa.allocate_pool(w.num_blocks, g.n_kv, g.d_h, g.kv_dtype, dev)
+    for k, v, slots in w.history_chunks(device=dev):
+        pa.pa_cache_write(k, v, torch.from_numpy(slots).to(dev), kc, vc, ks, vs)
+    q = w.q(dev)
+    kn, vn = w.new_kv(dev)
+    slots_new = torch.from_numpy(w.new_token_slots()).to(dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = pa.decode_workspace(pa.geometry(kc, g.n_h), w.B, dev, args.num_ctas)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize(dev)
+
+    def step():
+        pa.pa_cache_write(kn, vn, slots_new, kc, vc, ks, vs, dev_status=status)
+        pa.pa_decode(q, kc, vc, bt, cl, w.scale, out=out, k_scale=ks, v_scale=vs, workspace=ws,
+                     dev_status=status, num_ctas=args.num_ctas)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+        ev[i][0].record(stream)
+        pa.pa_cache_write(kn, vn, slots_new, kc, vc, ks, vs, dev_status=status)
+        ev[i][1].record(stream)
+        pa.pa_decode(q, kc, vc, bt, cl, w.scale, out=out, k_scale=ks, v_scale=vs, workspace=ws,
+                     dev_status=status, num_ctas=args.num_ctas)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    write_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {pa.pa_status_from_device(st)}")
+
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+
+    db = decode_bytes(w)
+    wb = cache_write_bytes(w)
+    step_bytes = db["bytes"] + wb
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    dec_avg = statistics.mean(dec_ms)
+    pk = peaks()
+    achieved = db["bytes"] / (dec_avg * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8" if g.kv_dtype == "int8" else "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.description}", "num_seqs": w.B,
+                   "context_tokens": int(w.context_lens.sum()),
+                   "l2": "flushed between timed steps (512 MiB write); KV working set "
+                         f"{db['bytes'] / 1e6:.0f} MB > 129 MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "seqs_per_s": round(world * w.B / (ms_per_step * 1e-3), 1),
+        "decode_ms": round(dec_avg, 5), "cache_write_ms": round(statistics.mean(write_ms), 5),
+        "bytes_per_step": step_bytes, "logical_kv_bytes": db["logical_bytes"],
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                     "traffic": recorded_traffic(args.workload),
+                     "kernel": "pa::decode_kernel", "peak_source": pk["source"],
+                     "algorithmic_bytes_per_launch": db["bytes"]},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+
+    # ---- end to end through the public API with host buffers
+    if not args.no_e2e:
+        hq = q.cpu().pin_memory()
+        hk, hv = kn.cpu().pin_memory(), vn.cpu().pin_memory()
+        hs = slots_new.cpu().pin_memory()
+        hbt, hcl = bt.cpu().pin_memory(), cl.cpu().pin_memory()
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+        ds, dbt, dcl = torch.empty_like(slots_new), torch.empty_like(bt), torch.empty_like(cl)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hbt, hcl))
+        d2h = hout.numel() * hout.element_size()
+
+        def e2e_step():
+            for d, h in ((dq, hq), (dk, hk), (dv, hv), (ds, hs), (dbt, hbt), (dcl, hcl)):
+                d.copy_(h, non_blocking=True)
+            pa.pa_cache_write(dk, dv, ds, kc, vc, ks, vs, dev_status=status)
+            pa.pa_decode(dq, kc, vc, dbt, dcl, w.scale, out=out, k_scale=ks, v_scale=vs,
+                         workspace=ws, dev_status=status)
+            hout.copy_(out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            flush.zero_()
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            e2e_ev[i][0].record(stream)
+            e2e_step()
+            e2e_ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e_ms /= args.steps
+        result["e2e"] = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2),
+                         "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        result["gpu_launches"] += 2 * args.steps
+
+    # ---- the oracle on the host cores (rank 0 only, N=1 only)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nbytes, secs, desc = oracle_sample(w, dev, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s",
+                                  "cores": 1, "kind": "oracle", "sample": desc,
+                                  "seconds": round(secs, 2)}
+    return result
+
+
+# ---------------------------------------------------------------- reference
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is the oracle on a
+    bounded sample of the workload, on the host cores."""
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = named_workload(args.workload)
+    per_step = max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, dev, per_step)
+    tot_b, tot_s, desc = 0, 0.0, ""
+    for _ in range(args.steps):
+        nb, s, desc = oracle_sample(w, dev, per_step)
+        tot_b += nb
+        tot_s += s
+    value = tot_b / tot_s / 1e9
+    g = w.geom
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_s / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.description}", "num_seqs": w.B},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc + " per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group(
+            backend="nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    try:
+        res = run_native(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

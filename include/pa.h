@@ -1,0 +1,232 @@
+/*
+ * pa.h -- C ABI of the GB300 paged KV-cache decode-attention library (libpa.so).
+ *
+ * Two operations on a paged KV cache, both asynchronous on a caller stream:
+ *
+ *   pa_cache_write  append the new token's K/V rows at the slots a block
+ *                   manager handed out (optionally quantising them to INT8);
+ *   pa_decode       single-token decode attention of every sequence's query
+ *                   heads over that sequence's paged K/V history.
+ *
+ * Sources (web pages; cited by title and section):
+ *  [F] "LLM 推理底层：KV Cache 显存几何、GQA/MLA 压缩与 PagedAttention 调度"
+ *      (blog.faulkner.fun)
+ *  [Q] "【infra之路】10-PagedAttention 与 KV Cache 管理" (qwbw.cn)
+ *  [G] "kv-cache-guide" (guijiagi.com)
+ *  [T] "KV Cache 显存管理全景：内存碎片拟合推导、vLLM PagedAttention 虚拟内存与
+ *      Prefix Caching" (talentme.airsota.com)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer (memory the GPU can read or
+ *    write), except where a comment says otherwise. Tensors are dense and
+ *    row-major in the shapes given. The caller owns every buffer; the library
+ *    allocates no device memory and keeps no pointer after a call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Calls only enqueue work: none of them synchronises the device or
+ *    reads device memory from the host.
+ *  - Alignment: tensors of bf16 or int8 rows (k, v, q, out, the pools) must
+ *    start on a 16-byte boundary, fp32 scales on 16 bytes for pa_decode and
+ *    4 bytes for pa_cache_write, slot_mapping on 8 bytes and the decode
+ *    workspace on 256 bytes; otherwise PA_ERR_ALIGNMENT.
+ *  - Errors the host can see (null pointers, unsupported shapes, a workspace
+ *    that is too small, a failed launch) are returned before or at launch and
+ *    nothing is enqueued when the return value is not PA_OK.
+ *  - Errors only the GPU can see (a block id outside the pool, a slot outside
+ *    the pool, a context length the block table cannot hold) never trap or
+ *    fault: the kernel skips the offending unit of work and ORs a PA_DEV_* bit
+ *    into *dev_status when dev_status is not NULL. Read dev_status after the
+ *    stream has finished and turn it into a status with
+ *    pa_status_from_device(). What was skipped: a bad slot is not written; a
+ *    bad block contributes nothing to its sequence's attention; a bad context
+ *    length gives that sequence an all-zero output.
+ *
+ * Pool layout (the block layout [num_blocks, H, block_size, D] that [G] §7.1
+ * gives for PagedAttention):
+ *   k_cache, v_cache : [num_blocks][n_kv][block_size][d_h]  bf16 or int8 codes
+ *   k_scale, v_scale : [num_blocks][n_kv][block_size]       fp32 (INT8 only)
+ * so the 16 rows of one (block, kv head) pair are one contiguous tile.
+ * Token j of a sequence lives in physical block block_table[j / block_size] at
+ * offset j % block_size ([F] "逻辑块与物理块映射"); its slot is
+ * phys * block_size + offset.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. PA_OK is zero; every error is negative. */
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_NULL = -1,        /* a required pointer is NULL */
+    PA_ERR_SHAPE = -2,       /* a size is out of range (n_h % n_kv != 0, count <= 0, ...) */
+    PA_ERR_DTYPE = -3,       /* kv_dtype is not a pa_kv_dtype value */
+    PA_ERR_UNSUPPORTED = -4, /* a valid but unsupported geometry (d_h, block_size, group size) */
+    PA_ERR_BAD_BLOCK = -5,   /* device: a block table entry outside [0, num_blocks) */
+    PA_ERR_BAD_SLOT = -6,    /* device: a slot >= num_blocks * block_size */
+    PA_ERR_WORKSPACE = -7,   /* workspace NULL or smaller than pa_decode_workspace_size() */
+    PA_ERR_CUDA = -8,        /* a CUDA runtime or driver call failed */
+    PA_ERR_BAD_CONTEXT = -9, /* device: a context length < 0 or > max_blocks_per_seq * block_size */
+    PA_ERR_TIMEOUT = -10,    /* device: a pipeline wait gave up after about one second */
+    PA_ERR_ALIGNMENT = -11   /* a pointer lacks the alignment its entry point documents */
+} pa_status;
+
+/* Bits the kernels OR into *dev_status. */
+#define PA_DEV_BAD_BLOCK 0x1
+#define PA_DEV_BAD_SLOT 0x2
+#define PA_DEV_BAD_CONTEXT 0x4
+#define PA_DEV_TIMEOUT 0x8
+
+/* Element type of the cached K/V. */
+typedef enum pa_kv_dtype {
+    PA_KV_BF16 = 0, /* bf16 rows, stored as given */
+    PA_KV_INT8 = 1  /* int8 codes + one fp32 scale per (token, kv head), [G] §4.2 */
+} pa_kv_dtype;
+
+/* Attention and pool geometry of one layer.
+ *   n_h        query heads per token
+ *   n_kv       KV heads per token; n_h % n_kv == 0, and g = n_h / n_kv query
+ *              heads share one KV head ([F] table "注意力头架构演进", GQA row);
+ *              query head h reads KV head h / g. g = 1 is MHA.
+ *   d_h        head dimension: 64 or 128
+ *   block_size tokens per physical block: 16 (the vLLM default, [Q] §5)
+ *   num_blocks physical blocks in the pool
+ *   kv_dtype   a pa_kv_dtype value
+ * Supported group sizes g: 1, 2, 4, 8, 16. */
+typedef struct pa_geom {
+    int64_t num_blocks;
+    int32_t n_h;
+    int32_t n_kv;
+    int32_t d_h;
+    int32_t block_size;
+    int32_t kv_dtype;
+    int32_t reserved; /* must be 0 */
+} pa_geom;
+
+/*
+ * pa_cache_write -- slot-mapped append of new K/V rows.
+ *
+ * [T] 第三章 `write_kv` and [F] "逻辑块与物理块映射": the row of token t goes to
+ * physical block slot/block_size at offset slot%block_size, for every KV head:
+ *     k_cache[s / bs][h][s % bs][:] = k[t][h][:]     (same for v)
+ * Only the new rows are written; history stays untouched (the cached K/V of
+ * earlier tokens never change, [F] "自回归解码与 KV Cache 的物理来源").
+ *
+ * INT8 (geom.kv_dtype == PA_KV_INT8), [G] §4.2 `quantize_kv_cache`, per
+ * (token, head) row of d_h values, in IEEE fp32:
+ *     scale = max_d |x_d| / 127
+ *     code  = clamp(round_half_even(x / scale), -128, 127)
+ * and scale is stored in k_scale/v_scale[s / bs][h][s % bs]. A row of zeros
+ * stores scale 0 and zero codes.
+ *
+ *   k, v          bf16 [num_tokens][n_kv][d_h]      new rows (read)
+ *   slot_mapping  int64 [num_tokens]                 slot of each row; < 0 = skip
+ *   num_tokens    >= 0 (0 enqueues nothing)
+ *   k_cache, v_cache  pool (written), layout above
+ *   k_scale, v_scale  fp32 scales (written); must be NULL for PA_KV_BF16
+ *   dev_status    optional int32 device word for PA_DEV_BAD_SLOT
+ * Duplicate non-negative slots in one call leave the slot's content undefined.
+ */
+pa_status pa_cache_write(const void *k, const void *v, const int64_t *slot_mapping,
+                         int64_t num_tokens, void *k_cache, void *v_cache, float *k_scale,
+                         float *v_scale, pa_geom geom, int32_t *dev_status, void *stream);
+
+/*
+ * Bytes of device workspace pa_decode needs for num_seqs sequences on the
+ * CURRENT device (it depends on the SM count). num_ctas = 0 asks for the
+ * library's default grid; a positive value sizes the workspace for
+ * pa_decode_ex with that many CTAs. Returns 0 for an invalid geometry.
+ */
+size_t pa_decode_workspace_size(pa_geom geom, int32_t num_seqs, int32_t num_ctas);
+
+/*
+ * Zero a workspace (cudaMemsetAsync on `stream`).
+ *
+ * Workspace layout: the first round_up(4 * num_seqs * n_kv, 256) bytes are
+ * one int32 counter per (sequence, kv head); they must be zero when pa_decode
+ * starts, and every pa_decode leaves them zero again when its kernel ends. The
+ * rest is scratch for split partial results. So zero a workspace once before
+ * its first use, and again before a call whose num_seqs * n_kv is larger than
+ * any earlier call's on it.
+ */
+pa_status pa_decode_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * pa_decode -- decode attention over the paged KV cache.
+ *
+ * For every sequence b < num_seqs and query head h < n_h ([F] eq. for o_t in
+ * "自回归解码与 KV Cache 的物理来源"; [Q] §3.4 `paged_attention`):
+ *     kv   = h / g
+ *     s_j  = scale * < q[b][h][:], K_b[j][kv][:] >          for j < ctx_b
+ *     out[b][h][:] = sum_j softmax(s)_j * V_b[j][kv][:]
+ * where K_b[j] is read through the block table (token j in block
+ * block_tables[b][j / bs] at offset j % bs) and ctx_b = context_lens[b]
+ * counts the whole history INCLUDING the new token, which the caller appends
+ * with pa_cache_write first. INT8 rows are read as code * scale (fp32),
+ * [G] §4.2 `dequantize_kv`. The pages use scale = 1 / sqrt(d_h).
+ * Accumulation is fp32; the output is rounded to bf16. ctx_b == 0 gives a
+ * zero row. Long contexts are split across CTAs and merged with a
+ * log-sum-exp reduction, so results do not depend on how the work was split
+ * beyond fp32 rounding.
+ *
+ *   q                bf16 [num_seqs][n_h][d_h]
+ *   k_cache, v_cache pool, layout above (read)
+ *   k_scale, v_scale fp32 scales for PA_KV_INT8, else NULL
+ *   block_tables     int32 [num_seqs][max_blocks_per_seq]; entries past a
+ *                    sequence's ceil(ctx/bs) blocks are never read
+ *   context_lens     int32 [num_seqs] (device memory; not read by the host)
+ *   num_seqs         0..8192 (0 enqueues nothing)
+ *   scale            softmax scale applied to q.k
+ *   out              bf16 [num_seqs][n_h][d_h] (written)
+ *   workspace        >= pa_decode_workspace_size(geom, num_seqs, 0) bytes,
+ *                    256-byte aligned, counter area zero on entry (see
+ *                    pa_decode_workspace_init). Calls that share a workspace
+ *                    must be ordered on one stream.
+ *   dev_status       optional int32 device word (PA_DEV_* bits)
+ */
+pa_status pa_decode(const void *q, const void *k_cache, const void *v_cache,
+                    const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                    int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                    float scale, void *out, void *workspace, size_t workspace_bytes, pa_geom geom,
+                    int32_t *dev_status, void *stream);
+
+/* pa_decode with an explicit CTA count (num_ctas > 0) instead of the
+ * library's default of one wave of resident CTAs. Results agree with
+ * pa_decode within fp32 rounding; this exists to test split invariance and
+ * to tune the split. The workspace must be sized for the same num_ctas. */
+pa_status pa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
+                       const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                       int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                       float scale, void *out, void *workspace, size_t workspace_bytes,
+                       pa_geom geom, int32_t *dev_status, void *stream, int32_t num_ctas);
+
+/* Default CTA count pa_decode uses for this geometry on the current device
+ * (>= 1), or a negative pa_status. */
+int32_t pa_decode_default_ctas(pa_geom geom, int32_t num_seqs);
+
+/* Host-only: how pa_decode splits work. The W = n_kv * sum_b ceil(ctx_b / bs)
+ * (sequence, kv head, block) items are laid out sequence-major, kv-head next;
+ * CTA c takes items [floor(c*W/G), floor((c+1)*W/G)). For item x this returns
+ * the CTA that owns it. Exposed so the split can be checked on a CPU. */
+int32_t pa_plan_owner(int64_t item, int64_t total_items, int32_t num_ctas);
+
+/* Human-readable name of a status. Never NULL. */
+const char *pa_status_string(pa_status status);
+
+/* The status a device word stands for (first bit set wins: BAD_BLOCK,
+ * BAD_SLOT, BAD_CONTEXT, TIMEOUT), PA_OK for 0. */
+pa_status pa_status_from_device(int32_t dev_word);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int32_t pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

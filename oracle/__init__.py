@@ -27,13 +27,24 @@ BAD_SLOT = 2
 BAD_CTX = 4
 
 
+def _stamp() -> str:
+    import hashlib
+    import platform
+    return hashlib.sha256(platform.machine().encode() + open(_SRC, "rb").read()).hexdigest()
+
+
 def build(force: bool = False) -> str:
-    """Compile pa_oracle.c with gcc into oracle/liboracle.so."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    """Compile pa_oracle.c with gcc into oracle/liboracle.so (if stale)."""
+    stamp_path = _LIB + ".stamp"
+    stamp = _stamp()
+    if force or not os.path.exists(_LIB) or not os.path.exists(stamp_path) or \
+            open(stamp_path).read() != stamp:
         tmp = _LIB + f".{os.getpid()}.tmp"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
                                "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
+        with open(stamp_path, "w") as f:
+            f.write(stamp)
     return _LIB
 
 

@@ -1,0 +1,299 @@
+"""Python binding of libpa.so: paged KV-cache decode attention on GB300.
+
+Argument marshalling only. Every step of the computation runs in the CUDA
+kernels of libpa.so (see include/pa.h for the C ABI); this module checks the
+torch tensors it is given, passes their device pointers and the current CUDA
+stream, and raises PAError on a non-OK status. There is no CPU fallback: if
+the library has not been built, or no CUDA device is present, the calls raise.
+
+    pa_cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None)
+    out = pa_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
+                    k_scale=None, v_scale=None)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libpa.so")
+
+PA_KV_BF16 = 0
+PA_KV_INT8 = 1
+
+PA_DEV_BAD_BLOCK = 0x1
+PA_DEV_BAD_SLOT = 0x2
+PA_DEV_BAD_CONTEXT = 0x4
+PA_DEV_TIMEOUT = 0x8
+
+STATUS = {
+    0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_DTYPE",
+    -4: "PA_ERR_UNSUPPORTED", -5: "PA_ERR_BAD_BLOCK", -6: "PA_ERR_BAD_SLOT",
+    -7: "PA_ERR_WORKSPACE", -8: "PA_ERR_CUDA", -9: "PA_ERR_BAD_CONTEXT",
+    -10: "PA_ERR_TIMEOUT", -11: "PA_ERR_ALIGNMENT",
+}
+EXPORTED = ["pa_cache_write", "pa_decode_workspace_size", "pa_decode_workspace_init",
+            "pa_decode", "pa_decode_ex", "pa_decode_default_ctas", "pa_plan_owner",
+            "pa_status_string", "pa_status_from_device", "pa_version"]
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        msg = _lib().pa_status_string(status).decode() if _LIB is not None else STATUS.get(status)
+        super().__init__(f"{where}: {msg} ({status})" if where else f"{msg} ({status})")
+
+
+class pa_geom(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int64), ("n_h", ctypes.c_int32),
+                ("n_kv", ctypes.c_int32), ("d_h", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_LIB = None
+_LIB_LOCK = threading.Lock()
+
+
+def _lib():
+    """Load libpa.so (raises if it was not built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    with _LIB_LOCK:
+        if _LIB is not None:
+            return _LIB
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                f"g.build()'` (nvcc, sm_103a). There is no CPU fallback.")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                ctypes.c_size_t)
+        lib.pa_cache_write.restype = ctypes.c_int
+        lib.pa_cache_write.argtypes = [P, P, P, i64, P, P, P, P, pa_geom, P, P]
+        lib.pa_decode_workspace_size.restype = sz
+        lib.pa_decode_workspace_size.argtypes = [pa_geom, i32, i32]
+        lib.pa_decode_workspace_init.restype = ctypes.c_int
+        lib.pa_decode_workspace_init.argtypes = [P, sz, P]
+        dec = [P, P, P, P, P, P, i32, P, i32, f32, P, P, sz, pa_geom, P, P]
+        lib.pa_decode.restype = ctypes.c_int
+        lib.pa_decode.argtypes = dec
+        lib.pa_decode_ex.restype = ctypes.c_int
+        lib.pa_decode_ex.argtypes = dec + [i32]
+        lib.pa_decode_default_ctas.restype = i32
+        lib.pa_decode_default_ctas.argtypes = [pa_geom, i32]
+        lib.pa_plan_owner.restype = i32
+        lib.pa_plan_owner.argtypes = [i64, i64, i32]
+        lib.pa_status_string.restype = ctypes.c_char_p
+        lib.pa_status_string.argtypes = [ctypes.c_int]
+        lib.pa_status_from_device.restype = ctypes.c_int
+        lib.pa_status_from_device.argtypes = [i32]
+        lib.pa_version.restype = i32
+        lib.pa_version.argtypes = []
+        _LIB = lib
+        return lib
+
+
+def library():
+    """The loaded ctypes library (for direct C-ABI calls)."""
+    return _lib()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise PAError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(name: str, t: torch.Tensor, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def geometry(k_cache: torch.Tensor, n_h: int) -> pa_geom:
+    """pa_geom of a pool [num_blocks, n_kv, 16, d_h] (bf16 or int8) for n_h query heads."""
+    if k_cache.dim() != 4:
+        raise ValueError("k_cache must be [num_blocks, n_kv, block_size, d_h]")
+    nb, n_kv, bs, d = k_cache.shape
+    if k_cache.dtype == torch.bfloat16:
+        dt = PA_KV_BF16
+    elif k_cache.dtype == torch.int8:
+        dt = PA_KV_INT8
+    else:
+        raise TypeError("k_cache must be bfloat16 or int8")
+    return pa_geom(num_blocks=nb, n_h=n_h, n_kv=n_kv, d_h=d, block_size=bs, kv_dtype=dt, reserved=0)
+
+
+def pa_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor,
+                   k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                   dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Append rows k, v [T, n_kv, d_h] (bf16) at slot_mapping [T] (int64) into the pool."""
+    _need_cuda("k", k, torch.bfloat16)
+    _need_cuda("v", v, torch.bfloat16)
+    _need_cuda("slot_mapping", slot_mapping, torch.int64)
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
+    g = geometry(k_cache, n_h=k_cache.shape[1])
+    if k.shape != (slot_mapping.shape[0], g.n_kv, g.d_h) or v.shape != k.shape:
+        raise ValueError("k, v must be [num_tokens, n_kv, d_h] matching the pool and slot_mapping")
+    if g.kv_dtype == PA_KV_INT8:
+        for nm, s in (("k_scale", k_scale), ("v_scale", v_scale)):
+            if s is None:
+                raise ValueError(f"{nm} is required for an int8 pool")
+            _need_cuda(nm, s, torch.float32)
+            if tuple(s.shape) != tuple(k_cache.shape[:3]):
+                raise ValueError(f"{nm} must be [num_blocks, n_kv, block_size]")
+    if dev_status is not None:
+        _need_cuda("dev_status", dev_status, torch.int32)
+    st = _lib().pa_cache_write(_ptr(k), _ptr(v), _ptr(slot_mapping), slot_mapping.shape[0],
+                               _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), g,
+                               _ptr(dev_status), _stream_ptr(stream))
+    _check(st, "pa_cache_write")
+
+
+_WS: dict = {}
+_WS_LOCK = threading.Lock()
+
+
+def _counter_bytes(g: pa_geom, num_seqs: int) -> int:
+    return (4 * num_seqs * g.n_kv + 255) // 256 * 256
+
+
+def decode_workspace(g: pa_geom, num_seqs: int, device: torch.device, num_ctas: int = 0,
+                     stream=None) -> torch.Tensor:
+    """A workspace for pa_decode, cached per device.
+
+    Its leading counter area must be zero on entry; pa_decode leaves it zero,
+    so the cache only re-zeroes it when a call needs a larger counter area
+    than the buffer has had zeroed so far.
+    """
+    nbytes = _lib().pa_decode_workspace_size(g, num_seqs, num_ctas)
+    if nbytes == 0:
+        raise PAError(-2, "pa_decode_workspace_size")
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    need_zero = _counter_bytes(g, num_seqs)
+    with _WS_LOCK:
+        ent = _WS.get(key)
+        if ent is None or ent[0].numel() < nbytes:
+            ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+            ent = [ws, ws.numel()]
+            _WS[key] = ent
+        elif ent[1] < need_zero:
+            s = torch.cuda.current_stream(device) if stream is None else stream
+            _check(_lib().pa_decode_workspace_init(_ptr(ent[0]), ent[0].numel(),
+                                                   ctypes.c_void_p(s.cuda_stream)),
+                   "pa_decode_workspace_init")
+            ent[1] = ent[0].numel()
+        # after this call only the counter area is known to be zero: the rest
+        # is scratch, where a later call with more units puts its counters
+        ent[1] = need_zero
+        return ent[0]
+
+
+def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+              block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+              out: Optional[torch.Tensor] = None, k_scale: Optional[torch.Tensor] = None,
+              v_scale: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+              dev_status: Optional[torch.Tensor] = None, stream=None, num_ctas: int = 0
+              ) -> torch.Tensor:
+    """Decode attention: q [B, n_h, d_h] bf16 over the paged pool -> out [B, n_h, d_h] bf16.
+
+    block_tables [B, max_blocks] int32 and context_lens [B] int32 live on the device.
+    num_ctas > 0 forces the number of CTAs the work is split over (pa_decode_ex).
+    """
+    _need_cuda("q", q, torch.bfloat16)
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    if q.dim() != 3:
+        raise ValueError("q must be [num_seqs, n_h, d_h]")
+    B, n_h, d = q.shape
+    g = geometry(k_cache, n_h)
+    if d != g.d_h or block_tables.dim() != 2 or block_tables.shape[0] != B or \
+            context_lens.shape != (B,):
+        raise ValueError("q, block_tables, context_lens disagree on num_seqs or d_h")
+    if g.kv_dtype == PA_KV_INT8:
+        for nm, s in (("k_scale", k_scale), ("v_scale", v_scale)):
+            if s is None:
+                raise ValueError(f"{nm} is required for an int8 pool")
+            _need_cuda(nm, s, torch.float32)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, torch.bfloat16)
+        if out.shape != q.shape:
+            raise ValueError("out must have the shape of q")
+    if workspace is None:
+        workspace = decode_workspace(g, B, q.device, num_ctas, stream)
+    else:
+        _need_cuda("workspace", workspace)
+    if dev_status is not None:
+        _need_cuda("dev_status", dev_status, torch.int32)
+    lib = _lib()
+    args = [_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+            _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, float(scale),
+            _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), g,
+            _ptr(dev_status), _stream_ptr(stream)]
+    if num_ctas > 0:
+        st = lib.pa_decode_ex(*args, int(num_ctas))
+    else:
+        st = lib.pa_decode(*args)
+    _check(st, "pa_decode")
+    return out
+
+
+def pa_decode_default_ctas(k_cache: torch.Tensor, n_h: int, num_seqs: int) -> int:
+    r = _lib().pa_decode_default_ctas(geometry(k_cache, n_h), num_seqs)
+    if r < 0:
+        raise PAError(r, "pa_decode_default_ctas")
+    return r
+
+
+def pa_status_from_device(word: int) -> int:
+    return _lib().pa_status_from_device(int(word))
+
+
+def pa_plan_owner(item: int, total_items: int, num_ctas: int) -> int:
+    return _lib().pa_plan_owner(int(item), int(total_items), int(num_ctas))
+
+
+def pa_version() -> int:
+    return _lib().pa_version()
+
+
+def allocate_pool(num_blocks: int, n_kv: int, d_h: int, kv_dtype: str = "bf16",
+                  device="cuda", block_size: int = 16):
+    """Zeroed device pool tensors: (k_cache, v_cache, k_scale, v_scale)."""
+    shape = (num_blocks, n_kv, block_size, d_h)
+    if kv_dtype == "bf16":
+        kc = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        vc = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        return kc, vc, None, None
+    if kv_dtype == "int8":
+        kc = torch.zeros(shape, dtype=torch.int8, device=device)
+        vc = torch.zeros(shape, dtype=torch.int8, device=device)
+        ks = torch.zeros(shape[:3], dtype=torch.float32, device=device)
+        vs = torch.zeros(shape[:3], dtype=torch.float32, device=device)
+        return kc, vc, ks, vs
+    raise ValueError(kv_dtype)

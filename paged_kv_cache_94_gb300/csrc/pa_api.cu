@@ -1,0 +1,372 @@
+// C ABI of libpa.so: argument checks, tensor maps, grid sizing and launches.
+// Every function here runs on the host and only enqueues work.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/pa.h"
+#include "pa_decode.cuh"
+#include "pa_internal.h"
+
+namespace {
+
+using pa::DecodeKernel;
+using pa::DecodeParams;
+
+constexpr int kMaxSeqs = 8192;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int group_of(const pa_geom &g) { return g.n_h / g.n_kv; }
+
+pa_status check_geom(const pa_geom &g)
+{
+    if (g.reserved != 0)
+        return PA_ERR_SHAPE;
+    if (g.kv_dtype != PA_KV_BF16 && g.kv_dtype != PA_KV_INT8)
+        return PA_ERR_DTYPE;
+    if (g.n_h <= 0 || g.n_kv <= 0 || g.n_h % g.n_kv != 0 || g.num_blocks <= 0)
+        return PA_ERR_SHAPE;
+    if (g.block_size != 16 || (g.d_h != 64 && g.d_h != 128))
+        return PA_ERR_UNSUPPORTED;
+    const int gq = group_of(g);
+    if (gq != 1 && gq != 2 && gq != 4 && gq != 8 && gq != 16)
+        return PA_ERR_UNSUPPORTED;
+    // TMA row coordinates (block * n_kv + head) * 16 must fit in int32
+    if (g.num_blocks * (int64_t)g.n_kv * 16 >= (int64_t(1) << 31))
+        return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+const DecodeKernel *kernel_for(const pa_geom &g)
+{
+    const int gq = group_of(g);
+    return g.kv_dtype == PA_KV_INT8 ? pa::find_decode_kernel_int8(g.d_h, gq)
+                                    : pa::find_decode_kernel_bf16(g.d_h, gq);
+}
+
+// --------------------------------------------------------------- device info
+struct DeviceInfo {
+    int sms = 0;
+};
+
+DeviceInfo g_dev[64];
+std::mutex g_mu;
+
+pa_status current_device(int &dev, int &sms)
+{
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_dev[dev].sms == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return PA_ERR_CUDA;
+        g_dev[dev].sms = n;
+    }
+    sms = g_dev[dev].sms;
+    return PA_OK;
+}
+
+// Resident CTAs per SM of a kernel at a given shared-memory size. Sets the
+// kernel's dynamic shared-memory limit on the current device first.
+pa_status ctas_per_sm(const DecodeKernel *kd, size_t smem, int &n)
+{
+    if (cudaFuncSetAttribute(kd->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kd->fn, kd->threads, smem) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (n <= 0)
+        return PA_ERR_UNSUPPORTED; // does not fit on an SM
+    return PA_OK;
+}
+
+pa_status default_ctas(const pa_geom &g, int num_seqs, int &grid)
+{
+    const DecodeKernel *kd = kernel_for(g);
+    if (!kd)
+        return PA_ERR_UNSUPPORTED;
+    int dev, sms, per;
+    pa_status st = current_device(dev, sms);
+    if (st != PA_OK)
+        return st;
+    st = ctas_per_sm(kd, kd->smem_bytes(num_seqs), per);
+    if (st != PA_OK)
+        return st;
+    grid = sms * per;
+    return PA_OK;
+}
+
+size_t counters_bytes(int64_t units) { return (size_t)((units * 4 + 255) / 256 * 256); }
+
+size_t workspace_bytes_for(const pa_geom &g, int num_seqs, int grid)
+{
+    const int64_t units = (int64_t)num_seqs * g.n_kv;
+    const int64_t rec = (int64_t)group_of(g) * (g.d_h + 2) * 4;
+    return counters_bytes(units) + (size_t)((grid + units) * rec);
+}
+
+// ---------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D view of a pool: rows of d_h elements, one row per (block, head, offset);
+// a box is one 16-row tile of at most 128 bytes per row, swizzled so that
+// ldmatrix/ld.shared of 8 consecutive rows hit distinct banks.
+pa_status encode_pool(CUtensorMap &m, const void *base, const pa_geom &g)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return PA_ERR_CUDA;
+    const bool i8 = g.kv_dtype == PA_KV_INT8;
+    const int esz = i8 ? 1 : 2;
+    const cuuint64_t dims[2] = {(cuuint64_t)g.d_h, (cuuint64_t)(g.num_blocks * g.n_kv * 16)};
+    const cuuint64_t strides[1] = {(cuuint64_t)g.d_h * esz};
+    const cuuint32_t box_x = (cuuint32_t)((g.d_h * esz > 128) ? 128 / esz : g.d_h);
+    const cuuint32_t box[2] = {box_x, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw =
+        (box_x * esz == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUresult r =
+        fn(&m, i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+           const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                      const float *v_scale, const int32_t *block_tables, int32_t max_blocks,
+                      const int32_t *context_lens, int32_t num_seqs, float scale, void *out,
+                      void *workspace, size_t workspace_bytes, pa_geom g, int32_t *dev_status,
+                      void *stream, int32_t num_ctas)
+{
+    pa_status st = check_geom(g);
+    if (st != PA_OK)
+        return st;
+    if (num_seqs < 0 || num_seqs > kMaxSeqs || max_blocks <= 0 || num_ctas < 0)
+        return PA_ERR_SHAPE;
+    if ((int64_t)num_seqs * max_blocks >= (int64_t(1) << 31))
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
+        return !workspace ? PA_ERR_WORKSPACE : PA_ERR_NULL;
+    const bool i8 = g.kv_dtype == PA_KV_INT8;
+    if (i8 && (!k_scale || !v_scale))
+        return PA_ERR_NULL;
+    if (!i8 && (k_scale || v_scale))
+        return PA_ERR_SHAPE;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(workspace, 256) || (i8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16))))
+        return PA_ERR_ALIGNMENT;
+
+    const DecodeKernel *kd = kernel_for(g);
+    if (!kd)
+        return PA_ERR_UNSUPPORTED;
+    int dev, sms, per;
+    if ((st = current_device(dev, sms)) != PA_OK)
+        return st;
+    const size_t smem = kd->smem_bytes(num_seqs);
+    if ((st = ctas_per_sm(kd, smem, per)) != PA_OK)
+        return st;
+    const int grid = num_ctas > 0 ? num_ctas : sms * per;
+    if (workspace_bytes < workspace_bytes_for(g, num_seqs, grid))
+        return PA_ERR_WORKSPACE;
+
+    CUtensorMap tk, tv;
+    if ((st = encode_pool(tk, k_cache, g)) != PA_OK || (st = encode_pool(tv, v_cache, g)) != PA_OK)
+        return st;
+
+    DecodeParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    const int64_t units = (int64_t)num_seqs * g.n_kv;
+    p.counters = static_cast<int32_t *>(workspace);
+    p.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + counters_bytes(units));
+    p.dev_status = dev_status;
+    p.num_blocks = g.num_blocks;
+    p.num_seqs = num_seqs;
+    p.n_kv = g.n_kv;
+    p.max_blocks = max_blocks;
+    p.num_ctas = grid;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    const cudaError_t e =
+        kd->launch(tk, tv, p, grid, smem, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+} // namespace
+
+namespace pa {
+const DecodeKernel *find_decode_kernel_bf16_d64(int group);
+const DecodeKernel *find_decode_kernel_bf16_d128(int group);
+const DecodeKernel *find_decode_kernel_int8_d64(int group);
+const DecodeKernel *find_decode_kernel_int8_d128(int group);
+
+const DecodeKernel *find_decode_kernel_bf16(int d_h, int group)
+{
+    return d_h == 128 ? find_decode_kernel_bf16_d128(group)
+                      : d_h == 64 ? find_decode_kernel_bf16_d64(group) : nullptr;
+}
+
+const DecodeKernel *find_decode_kernel_int8(int d_h, int group)
+{
+    return d_h == 128 ? find_decode_kernel_int8_d128(group)
+                      : d_h == 64 ? find_decode_kernel_int8_d64(group) : nullptr;
+}
+} // namespace pa
+
+extern "C" {
+
+pa_status pa_cache_write(const void *k, const void *v, const int64_t *slot_mapping,
+                         int64_t num_tokens, void *k_cache, void *v_cache, float *k_scale,
+                         float *v_scale, pa_geom geom, int32_t *dev_status, void *stream)
+{
+    pa_status st = check_geom(geom);
+    if (st != PA_OK)
+        return st;
+    if (num_tokens < 0)
+        return PA_ERR_SHAPE;
+    if (num_tokens == 0)
+        return PA_OK;
+    if (num_tokens * geom.n_kv > (int64_t(1) << 33))
+        return PA_ERR_UNSUPPORTED;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+        return PA_ERR_NULL;
+    const bool i8 = geom.kv_dtype == PA_KV_INT8;
+    if (i8 && (!k_scale || !v_scale))
+        return PA_ERR_NULL;
+    if (!i8 && (k_scale || v_scale))
+        return PA_ERR_SHAPE;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8) || (i8 && (!aligned(k_scale, 4) || !aligned(v_scale, 4))))
+        return PA_ERR_ALIGNMENT;
+    const cudaError_t e = pa::launch_cache_write(
+        k, v, slot_mapping, num_tokens, geom.n_kv, geom.d_h, i8, geom.num_blocks * 16, k_cache,
+        v_cache, k_scale, v_scale, dev_status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_decode_workspace_size(pa_geom geom, int32_t num_seqs, int32_t num_ctas)
+{
+    if (check_geom(geom) != PA_OK || num_seqs < 0 || num_seqs > kMaxSeqs || num_ctas < 0)
+        return 0;
+    int grid = num_ctas;
+    if (grid == 0 && default_ctas(geom, num_seqs, grid) != PA_OK)
+        return 0;
+    return workspace_bytes_for(geom, num_seqs, grid);
+}
+
+pa_status pa_decode_workspace_init(void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!workspace)
+        return PA_ERR_WORKSPACE;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+pa_status pa_decode(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
+                    const float *v_scale, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                    const int32_t *context_lens, int32_t num_seqs, float scale, void *out,
+                    void *workspace, size_t workspace_bytes, pa_geom geom, int32_t *dev_status,
+                    void *stream)
+{
+    return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, scale, out, workspace, workspace_bytes, geom,
+                       dev_status, stream, 0);
+}
+
+pa_status pa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
+                       const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                       int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                       float scale, void *out, void *workspace, size_t workspace_bytes,
+                       pa_geom geom, int32_t *dev_status, void *stream, int32_t num_ctas)
+{
+    if (num_ctas <= 0)
+        return PA_ERR_SHAPE;
+    return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, scale, out, workspace, workspace_bytes, geom,
+                       dev_status, stream, num_ctas);
+}
+
+int32_t pa_decode_default_ctas(pa_geom geom, int32_t num_seqs)
+{
+    pa_status st = check_geom(geom);
+    if (st != PA_OK)
+        return st;
+    if (num_seqs < 0 || num_seqs > kMaxSeqs)
+        return PA_ERR_SHAPE;
+    int grid = 0;
+    st = default_ctas(geom, num_seqs, grid);
+    return st != PA_OK ? st : grid;
+}
+
+int32_t pa_plan_owner(int64_t item, int64_t total_items, int32_t num_ctas)
+{
+    if (total_items <= 0 || num_ctas <= 0 || item < 0 || item >= total_items)
+        return -1;
+    return (int32_t)pa::plan_owner(item, total_items, num_ctas);
+}
+
+const char *pa_status_string(pa_status s)
+{
+    switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_NULL: return "PA_ERR_NULL: a required pointer is NULL";
+    case PA_ERR_SHAPE: return "PA_ERR_SHAPE: a size or argument combination is invalid";
+    case PA_ERR_DTYPE: return "PA_ERR_DTYPE: unknown kv_dtype";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: geometry not supported";
+    case PA_ERR_BAD_BLOCK: return "PA_ERR_BAD_BLOCK: block table entry outside the pool";
+    case PA_ERR_BAD_SLOT: return "PA_ERR_BAD_SLOT: slot outside the pool";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: a CUDA call failed";
+    case PA_ERR_BAD_CONTEXT: return "PA_ERR_BAD_CONTEXT: context length outside the block table";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a pipeline wait gave up";
+    case PA_ERR_ALIGNMENT: return "PA_ERR_ALIGNMENT: a pointer is not aligned as required";
+    }
+    return "unknown pa_status";
+}
+
+pa_status pa_status_from_device(int32_t w)
+{
+    if (w & PA_DEV_BAD_BLOCK)
+        return PA_ERR_BAD_BLOCK;
+    if (w & PA_DEV_BAD_SLOT)
+        return PA_ERR_BAD_SLOT;
+    if (w & PA_DEV_BAD_CONTEXT)
+        return PA_ERR_BAD_CONTEXT;
+    if (w & PA_DEV_TIMEOUT)
+        return PA_ERR_TIMEOUT;
+    return PA_OK;
+}
+
+int32_t pa_version(void) { return 100; }
+
+} // extern "C"

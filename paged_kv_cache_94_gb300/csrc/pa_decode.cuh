@@ -1,0 +1,305 @@
+// Paged decode-attention kernels for sm_103a.
+//
+// What is computed (per sequence b, query head h; "LLM 推理底层：KV Cache 显存几何、
+// GQA/MLA 压缩与 PagedAttention 调度", eq. for o_t):
+//     out[b][h] = softmax(scale * q[b][h] K_b^T) V_b
+// over the ctx_b cached tokens of sequence b, read through its block table
+// (same page, "逻辑块与物理块映射"), with g = n_h / n_kv query heads sharing a
+// KV head (same page, GQA row of the "注意力头架构演进" table).
+//
+// How the work is split.
+//   An "item" is one (sequence, kv head, 16-token block). Items are laid out
+//   sequence-major, then kv head, then block, so the W items of the whole
+//   batch form one line. CTA c of G takes items [c*W/G, (c+1)*W/G): every CTA
+//   gets the same number of K/V bytes whatever the mix of context lengths, and
+//   long contexts are split across CTAs ("split-context" decode). A CTA's
+//   range is cut at (sequence, kv head) boundaries into segments.
+//   The g query heads of one KV head are processed together, so each K/V tile
+//   is read from HBM once for all g heads.
+// Inside a CTA.
+//   Each warp owns every NW-th item of the range and a private ring of S
+//   shared-memory stages. Lane 0 issues TMA tile loads (cp.async.bulk.tensor,
+//   128-byte swizzle) S items ahead; completion is tracked by one mbarrier per
+//   stage. Block-table entries are fetched 32 items ahead, one per lane.
+//   A warp keeps an online-softmax state (running max m, sum l, accumulator)
+//   per query head, in the log2 domain.
+// Merging.
+//   At a segment end the warps' states are merged through shared memory. A
+//   segment that is a whole (sequence, kv head) writes the output directly.
+//   Otherwise it writes (m, l, acc) to a workspace slot; the last CTA to finish
+//   that (sequence, kv head) -- found with one atomic counter, no waiting --
+//   merges all slots with the log-sum-exp rule
+//       M = max_p m_p,  out = sum_p 2^(m_p-M) acc_p / sum_p 2^(m_p-M) l_p
+//   and resets the counter to zero for the next call.
+#pragma once
+
+#include "pa_internal.h"
+#include "pa_plan.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+constexpr int kBlockTokens = 16;
+
+struct DecodeParams {
+    const __nv_bfloat16 *q;      // [B][n_h][D]
+    const float *k_scale;        // INT8: [NB][n_kv][16]
+    const float *v_scale;
+    const int32_t *block_tables; // [B][max_blocks]
+    const int32_t *context_lens; // [B]
+    __nv_bfloat16 *out;          // [B][n_h][D]
+    float *partials;             // [(G + B*n_kv)][g][D + 2]
+    int32_t *counters;           // [B*n_kv], zero between calls
+    int32_t *dev_status;         // optional
+    int64_t num_blocks;
+    int32_t num_seqs;
+    int32_t n_kv;
+    int32_t max_blocks;
+    int32_t num_ctas;
+    float scale_log2;            // softmax scale * log2(e)
+};
+
+__device__ __forceinline__ void flag_error(int32_t *dev_status, int32_t bit)
+{
+    if (dev_status)
+        atomicOr(dev_status, bit);
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory carve-up common to both kernels.
+// ---------------------------------------------------------------------------
+template <int D, int GQ, int NW, int S, int STAGE_BYTES, int EXTRA_PER_STAGE, int Q_PER_WARP>
+struct SmemLayout {
+    static constexpr int kRing = NW * S * STAGE_BYTES;                  // 1024-aligned tiles
+    static constexpr int kExtra = NW * S * EXTRA_PER_STAGE;             // per-stage side data
+    static constexpr int kQ = NW * Q_PER_WARP;                          // per-warp query copy
+    static constexpr int kBars = NW * S * 8;
+    static constexpr int kMeta = NW * S * 4;
+    static constexpr int kMerge = NW * GQ * (D + 2) * 4;
+    static constexpr int kMisc = 64;
+    static constexpr int kOffExtra = kRing;
+    static constexpr int kOffQ = kOffExtra + kExtra;
+    static constexpr int kOffBars = (kOffQ + kQ + 15) / 16 * 16;
+    static constexpr int kOffMeta = kOffBars + kBars;
+    static constexpr int kOffMerge = (kOffMeta + kMeta + 15) / 16 * 16;
+    static constexpr int kOffMisc = kOffMerge + kMerge;
+    static constexpr int kOffPrefix = kOffMisc + kMisc;
+    static size_t bytes(int num_seqs) { return 1024 + kOffPrefix + 4 * (size_t)(num_seqs + 1); }
+};
+
+// ---------------------------------------------------------------------------
+// Prefix over sequences: P[b] = sum_{b' < b} ceil(ctx_b' / 16). A context
+// length outside [0, max_blocks*16] counts as 0 blocks (and is reported).
+// ---------------------------------------------------------------------------
+template <int NT>
+__device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P, int32_t *wsum)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NWARP = NT / 32;
+    int32_t carry = 0;
+    if (tid == 0)
+        P[0] = 0;
+    for (int base = 0; base < p.num_seqs; base += NT) {
+        const int b = base + tid;
+        int32_t v = 0;
+        if (b < p.num_seqs) {
+            const int32_t ctx = p.context_lens[b];
+            if (ctx < 0 || (int64_t)ctx > (int64_t)p.max_blocks * kBlockTokens) {
+                if (blockIdx.x == 0)
+                    flag_error(p.dev_status, PA_DEV_BAD_CONTEXT_BIT);
+            } else {
+                v = (ctx + kBlockTokens - 1) / kBlockTokens;
+            }
+        }
+        int32_t x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o)
+                x += y;
+        }
+        if (lane == 31)
+            wsum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t t = lane < NWARP ? wsum[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int32_t y = __shfl_up_sync(0xffffffffu, t, o);
+                if (lane >= o)
+                    t += y;
+            }
+            if (lane < NWARP)
+                wsum[lane] = t; // inclusive
+        }
+        __syncthreads();
+        const int32_t before = warp ? wsum[warp - 1] : 0;
+        if (b < p.num_seqs)
+            P[b + 1] = carry + before + x;
+        carry += wsum[NWARP - 1];
+        __syncthreads();
+    }
+}
+
+// Item x -> (sequence b, kv head, block index i within the sequence, blocks
+// of the sequence). Largest b with n_kv*P[b] <= x; such a b has blocks.
+__device__ __forceinline__ void locate_item(int64_t x, const int32_t *P, int num_seqs, int n_kv,
+                                            int &b, int &kvh, int &i, int &nb)
+{
+    int lo = 0, hi = num_seqs;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)n_kv * P[mid] <= x)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    b = lo;
+    nb = P[b + 1] - P[b];
+    const int64_t r = x - (int64_t)n_kv * P[b];
+    kvh = (int)(r / nb);
+    i = (int)(r - (int64_t)kvh * nb);
+}
+
+// Zero the output rows of sequences with no blocks (ctx == 0 or invalid).
+template <int D>
+__device__ __forceinline__ void zero_empty_sequences(const DecodeParams &p, const int32_t *P,
+                                                     int n_h)
+{
+    const int rows16 = n_h * D * 2 / 16; // 16-byte chunks per sequence
+    for (int b = blockIdx.x; b < p.num_seqs; b += p.num_ctas) {
+        if (P[b + 1] != P[b])
+            continue;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (size_t)b * n_h * D);
+        for (int i = threadIdx.x; i < rows16; i += blockDim.x)
+            dst[i] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// End of a segment: merge the NW warp states in `merge` ([NW][GQ][D+2]:
+// m, l, acc[D]) and write the output or a partial; the last CTA of a split
+// (sequence, kv head) merges the partials. Called by all threads.
+// ---------------------------------------------------------------------------
+template <int D, int GQ, int NW>
+__device__ __forceinline__ void finish_segment(const DecodeParams &p, const float *merge,
+                                               int32_t *misc, int b, int kvh, int64_t unit_start,
+                                               int nb, int64_t W, bool whole)
+{
+    constexpr int NT = NW * 32;
+    constexpr int REC = D + 2;
+    const int n_h = p.n_kv * GQ;
+    const int u = b * p.n_kv + kvh;
+    __nv_bfloat16 *out = p.out + ((size_t)b * n_h + (size_t)kvh * GQ) * D;
+    float *rec = p.partials + ((size_t)blockIdx.x + u) * (GQ * REC);
+
+    for (int idx = threadIdx.x; idx < GQ * D; idx += NT) {
+        const int h = idx / D, d = idx - h * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+            M = fmaxf(M, merge[(w * GQ + h) * REC]);
+        float O = 0.f, L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float mw = merge[(w * GQ + h) * REC];
+                const float sc = fast_exp2(mw - M);
+                L += sc * merge[(w * GQ + h) * REC + 1];
+                O += sc * merge[(w * GQ + h) * REC + 2 + d];
+            }
+        }
+        if (whole) {
+            out[h * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+        } else {
+            if (d == 0) {
+                rec[h * REC] = M;
+                rec[h * REC + 1] = L;
+            }
+            rec[h * REC + 2 + d] = O;
+        }
+    }
+    if (whole) {
+        __syncthreads();
+        return;
+    }
+    // Publish the partial; the last of the nseg CTAs of this unit merges.
+    __threadfence();
+    __syncthreads();
+    const int64_t c_first = plan_owner(unit_start, W, p.num_ctas);
+    const int64_t c_last = plan_owner(unit_start + nb - 1, W, p.num_ctas);
+    if (threadIdx.x == 0) {
+        const int nseg = (int)(c_last - c_first + 1);
+        const int old = atomicAdd(&p.counters[u], 1);
+        const int last = (old == nseg - 1);
+        if (last)
+            p.counters[u] = 0; // every arrival of this launch is in: reset for the next call
+        misc[0] = last;
+        __threadfence();
+    }
+    __syncthreads();
+    if (misc[0]) {
+        const float *base = p.partials + ((size_t)c_first + u) * (GQ * REC);
+        const int nseg = (int)(c_last - c_first + 1);
+        for (int idx = threadIdx.x; idx < GQ * D; idx += NT) {
+            const int h = idx / D, d = idx - h * D;
+            float M = -INFINITY;
+            for (int s = 0; s < nseg; ++s)
+                M = fmaxf(M, __ldcg(base + (size_t)s * GQ * REC + h * REC));
+            float O = 0.f, L = 0.f;
+            if (M != -INFINITY) {
+                for (int s = 0; s < nseg; ++s) {
+                    const float *r = base + (size_t)s * GQ * REC + h * REC;
+                    const float sc = fast_exp2(__ldcg(r) - M);
+                    L += sc * __ldcg(r + 1);
+                    O += sc * __ldcg(r + 2 + d);
+                }
+            }
+            out[h * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+        }
+    }
+    __syncthreads();
+}
+
+// Byte offset of 16-byte chunk `c` of row `r` in a TMA-swizzled tile whose
+// rows are ROWB bytes (128: SWIZZLE_128B, 64: SWIZZLE_64B).
+template <int ROWB>
+__device__ __forceinline__ uint32_t swz(int r, int c)
+{
+    if constexpr (ROWB == 128)
+        return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+    else
+        return (uint32_t)(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
+
+// ---------------------------------------------------------------------------
+// Per-warp producer: the TMA ring and the block-table prefetch.
+// ---------------------------------------------------------------------------
+struct WarpRing {
+    int64_t lo;        // CTA range start
+    int64_t n_items;   // items this warp owns
+    int warp;
+    int64_t issued;    // items whose loads were issued
+    int64_t batch;     // index of the 32-item batch held in meta_cur
+    int32_t meta_cur;  // lane l: tile row (phys*n_kv + kvh) of item 32*batch + l, or -1
+    int32_t meta_next; // the same for batch + 1
+};
+
+template <int NW>
+__device__ __forceinline__ int32_t load_item_row(const DecodeParams &p, const int32_t *P,
+                                                 const WarpRing &r, int64_t k)
+{
+    if (k >= r.n_items)
+        return -1;
+    const int64_t x = r.lo + r.warp + k * NW;
+    int b, kvh, i, nb;
+    locate_item(x, P, p.num_seqs, p.n_kv, b, kvh, i, nb);
+    const int32_t phys = __ldg(p.block_tables + (size_t)b * p.max_blocks + i);
+    if (phys < 0 || (int64_t)phys >= p.num_blocks) {
+        flag_error(p.dev_status, PA_DEV_BAD_BLOCK_BIT);
+        return -1;
+    }
+    return phys * p.n_kv + kvh;
+}
+
+} // namespace pa

@@ -1,0 +1,565 @@
+// The decode kernel template and its two compute policies.
+//
+//  Bf16Policy: K/V tiles in bf16; the g-wide contractions run on the tensor
+//              cores with mma.sync m16n8k16 (bf16 in, fp32 accumulate):
+//                S^T[16 tok][8 heads] = K[16 tok][D] . Q^T[D][8 heads]
+//                O^T[D][8 heads]     += V^T[D][16 tok] . P^T[16 tok][8 heads]
+//              Tokens sit on the M side, so the query group only pads N to 8;
+//              P^T is moved from the accumulator layout to the B-operand
+//              layout with movmatrix.
+//  Int8Policy: K/V tiles as int8 codes plus an fp32 scale per row
+//              ("kv-cache-guide" (guijiagi.com) §4.2, dequantize_kv:
+//              x = code * scale); codes become exact fp32 values and the
+//              dot products run as fp32 FMA. The K scale multiplies the score,
+//              the V scale multiplies the softmax weight.
+#pragma once
+
+#include "pa_decode.cuh"
+
+namespace pa {
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p)
+{
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Exact fp32 value of signed byte k of `w` (k = 0..3). Adding 2^23 + 128 to an
+// unsigned byte u gives a float whose low mantissa bits are u; subtracting
+// 2^23 + 128 again recovers u - 128 = the signed value exactly.
+__device__ __forceinline__ void s8x4_to_f32(uint32_t w, float (&f)[4])
+{
+    const uint32_t u = w ^ 0x80808080u;
+    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.f;
+    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - 8388736.f;
+    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - 8388736.f;
+    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.f;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 K/V, tensor-core contractions.
+// ---------------------------------------------------------------------------
+template <int D_, int GQ_, int NW_, int S_>
+struct Bf16Policy {
+    static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_;
+    static constexpr bool kInt8 = false;
+    static constexpr int NT = (GQ + 7) / 8;           // 8-head n-tiles
+    static constexpr int KS = D / 16;                 // k-steps / m-tiles over D
+    static constexpr int HALVES = D / 64;             // 64-column TMA boxes per tile
+    static constexpr int TILE = kBlockTokens * D * 2; // bytes of a K (or V) tile
+    static constexpr int STAGE = 2 * TILE;
+    static constexpr int EXTRA = 0;
+    static constexpr int QBYTES = 0;
+    static constexpr uint32_t TX = STAGE;
+    using Layout = SmemLayout<D, GQ, NW, S, STAGE, EXTRA, QBYTES>;
+
+    struct State {
+        uint32_t qf[NT][KS][2]; // Q^T B-fragments
+        float m[NT][2], l[NT][2];
+        float acc[NT][KS][4];   // O^T accumulators: rows d, cols heads
+    };
+
+    __device__ static void issue(uint32_t dst, uint32_t /*extra*/, int32_t row, uint32_t bar,
+                                 const CUtensorMap *tk, const CUtensorMap *tv,
+                                 const DecodeParams & /*p*/, uint64_t pol)
+    {
+        const int32_t y = row * kBlockTokens;
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h)
+            tma_load_2d(dst + h * (TILE / HALVES), tk, h * 64, y, bar, pol);
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h)
+            tma_load_2d(dst + TILE + h * (TILE / HALVES), tv, h * 64, y, bar, pol);
+    }
+
+    __device__ static void load_q(State &st, const DecodeParams &p, int b, int kvh,
+                                  float * /*qsm*/)
+    {
+        const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
+        const int n_h = p.n_kv * GQ;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int hl = nt * 8 + gid;
+            const bool ok = hl < GQ;
+            const uint32_t *row = reinterpret_cast<const uint32_t *>(
+                p.q + ((size_t)b * n_h + (size_t)kvh * GQ + (ok ? hl : 0)) * D);
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                st.qf[nt][kk][0] = ok ? __ldg(row + kk * 8 + t4) : 0u;
+                st.qf[nt][kk][1] = ok ? __ldg(row + kk * 8 + 4 + t4) : 0u;
+            }
+        }
+    }
+
+    __device__ static void reset(State &st)
+    {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                st.m[nt][e] = -INFINITY;
+                st.l[nt][e] = 0.f;
+            }
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    st.acc[nt][mt][e] = 0.f;
+        }
+    }
+
+    // One 16-token block: K tile at kt, V tile at kt + TILE (shared addresses).
+    __device__ static void compute(State &st, uint32_t kt, uint32_t /*extra*/, int valid,
+                                   float scale_log2)
+    {
+        const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
+        const int mi = lane >> 3, rr = lane & 7;
+        const uint32_t vt = kt + TILE;
+
+        // ---- scores S^T = K Q^T (two accumulator chains for ILP)
+        float s0[NT][4], s1[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                s0[nt][e] = s1[nt][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            const int tok = rr + ((mi & 1) << 3);
+            const int chunk = 2 * kk + (mi >> 1);
+            const uint32_t addr = kt + (chunk >> 3) * (TILE / HALVES) + (uint32_t)(tok * 128) +
+                                  (uint32_t)(((chunk & 7) ^ rr) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4(addr, a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (kk & 1)
+                    mma_bf16_16816(s1[nt], a0, a1, a2, a3, st.qf[nt][kk][0], st.qf[nt][kk][1]);
+                else
+                    mma_bf16_16816(s0[nt], a0, a1, a2, a3, st.qf[nt][kk][0], st.qf[nt][kk][1]);
+            }
+        }
+
+        // ---- online softmax (columns = heads; rows = tokens gid, gid+8)
+        const bool lo_ok = gid < valid, hi_ok = gid + 8 < valid;
+        uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float sc[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sc[e] = (s0[nt][e] + s1[nt][e]) * scale_log2;
+            if (!lo_ok) {
+                sc[0] = -INFINITY;
+                sc[1] = -INFINITY;
+            }
+            if (!hi_ok) {
+                sc[2] = -INFINITY;
+                sc[3] = -INFINITY;
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float mx = fmaxf(sc[e], sc[e + 2]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float mnew = fmaxf(st.m[nt][e], mx);
+                const float base = (mnew == -INFINITY) ? 0.f : mnew;
+                const float alpha = fast_exp2(st.m[nt][e] - base);
+                st.m[nt][e] = mnew;
+                sc[e] = fast_exp2(sc[e] - base);
+                sc[e + 2] = fast_exp2(sc[e + 2] - base);
+                st.l[nt][e] = st.l[nt][e] * alpha + sc[e] + sc[e + 2];
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    st.acc[nt][mt][e] *= alpha;
+                    st.acc[nt][mt][e + 2] *= alpha;
+                }
+            }
+            pb0[nt] = movmatrix_trans(pack_bf16x2(sc[0], sc[1]));
+            pb1[nt] = movmatrix_trans(pack_bf16x2(sc[2], sc[3]));
+        }
+
+        // ---- O^T += V^T P^T
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        if (valid < kBlockTokens) {
+            const int t0 = 2 * t4;
+            mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+            mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            const int tok = rr + ((mi >> 1) << 3);
+            const int chunk = 2 * mt + (mi & 1);
+            const uint32_t addr = vt + (chunk >> 3) * (TILE / HALVES) + (uint32_t)(tok * 128) +
+                                  (uint32_t)(((chunk & 7) ^ rr) << 4);
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+            a0 &= mlo;
+            a1 &= mlo;
+            a2 &= mhi;
+            a3 &= mhi;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma_bf16_16816(st.acc[nt][mt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+        }
+    }
+
+    __device__ static void to_merge(State &st, float *merge)
+    {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float l = st.l[nt][e];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                const int h = nt * 8 + 2 * t4 + e;
+                if (h < GQ) {
+                    float *mb = merge + (warp * GQ + h) * (D + 2);
+                    if (gid == 0) {
+                        mb[0] = st.m[nt][e];
+                        mb[1] = l;
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        mb[2 + 16 * mt + gid] = st.acc[nt][mt][e];
+                        mb[2 + 16 * mt + gid + 8] = st.acc[nt][mt][e + 2];
+                    }
+                }
+            }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// INT8 K/V (codes + fp32 per-row scales), fp32 FMA contractions.
+// ---------------------------------------------------------------------------
+template <int D_, int GQ_, int NW_, int S_>
+struct Int8Policy {
+    static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_;
+    static constexpr bool kInt8 = true;
+    static constexpr int ROWB = D;                 // bytes per tile row: 128 or 64
+    static constexpr int TILE = kBlockTokens * D;  // bytes of a K (or V) code tile
+    static constexpr int STAGE = 2 * TILE;
+    static constexpr int EXTRA = 128;              // 16 K scales + 16 V scales
+    static constexpr int QBYTES = GQ > 1 ? GQ * D * 4 : 0;
+    static constexpr uint32_t TX = STAGE + EXTRA;
+    static constexpr int HALF = D / 2;             // d values per lane in the score loop
+    static constexpr int CH = HALF / 16;           // 16-byte chunks per half row
+    static constexpr int CPL = D / 32;             // d values per lane in the P.V loop
+    using Layout = SmemLayout<D, GQ, NW, S, STAGE, EXTRA, QBYTES>;
+
+    struct State {
+        float qr[GQ == 1 ? HALF : 1]; // query half-row in registers (g == 1)
+        const float *qs;              // per-warp fp32 query copy [GQ][D] (g > 1)
+        float m[GQ], l[GQ];
+        float acc[GQ][CPL];
+    };
+
+    __device__ static void issue(uint32_t dst, uint32_t extra, int32_t row, uint32_t bar,
+                                 const CUtensorMap *tk, const CUtensorMap *tv,
+                                 const DecodeParams &p, uint64_t pol)
+    {
+        const int32_t y = row * kBlockTokens;
+        tma_load_2d(dst, tk, 0, y, bar, pol);
+        tma_load_2d(dst + TILE, tv, 0, y, bar, pol);
+        bulk_load_1d(extra, p.k_scale + (size_t)row * kBlockTokens, 64, bar, pol);
+        bulk_load_1d(extra + 64, p.v_scale + (size_t)row * kBlockTokens, 64, bar, pol);
+    }
+
+    __device__ static void load_q(State &st, const DecodeParams &p, int b, int kvh, float *qsm)
+    {
+        const int lane = threadIdx.x & 31;
+        const int n_h = p.n_kv * GQ;
+        const __nv_bfloat16 *qb = p.q + ((size_t)b * n_h + (size_t)kvh * GQ) * D;
+        if constexpr (GQ == 1) {
+            const int half = lane & 1;
+#pragma unroll
+            for (int i = 0; i < HALF; i += 2) {
+                const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(qb + half * HALF + i));
+                st.qr[i] = __uint_as_float(w << 16);
+                st.qr[i + 1] = __uint_as_float(w & 0xffff0000u);
+            }
+            st.qs = nullptr;
+        } else {
+            __syncwarp();
+            for (int i = lane; i < GQ * D; i += 32)
+                qsm[i] = __bfloat162float(qb[i]);
+            __syncwarp();
+            st.qs = qsm;
+        }
+    }
+
+    __device__ static void reset(State &st)
+    {
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            st.m[h] = -INFINITY;
+            st.l[h] = 0.f;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i)
+                st.acc[h][i] = 0.f;
+        }
+    }
+
+    __device__ static void compute(State &st, uint32_t kt, uint32_t extra, int valid,
+                                   float scale_log2)
+    {
+        const int lane = threadIdx.x & 31;
+        const int j = lane >> 1, half = lane & 1;
+        const uint32_t vt = kt + TILE;
+
+        // ---- scores: lane pair (2j, 2j+1) covers token j, one half-row each
+        float dot[GQ];
+#pragma unroll
+        for (int h = 0; h < GQ; ++h)
+            dot[h] = 0.f;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+            const int chunk = half * CH + c;
+            uint32_t w0, w1, w2, w3;
+            const uint32_t addr = kt + (ROWB == 128 ? (uint32_t)(j * 128 + ((chunk ^ (j & 7)) << 4))
+                                                    : (uint32_t)(j * 64 + ((chunk ^ ((j >> 1) & 3)) << 4)));
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                         : "r"(addr));
+            const uint32_t ws[4] = {w0, w1, w2, w3};
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float f[4];
+                s8x4_to_f32(ws[q4], f);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int dl = c * 16 + q4 * 4 + e; // d within this lane's half
+                    if constexpr (GQ == 1) {
+                        dot[0] = fmaf(st.qr[dl], f[e], dot[0]);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < GQ; ++h)
+                            dot[h] = fmaf(st.qs[h * D + half * HALF + dl], f[e], dot[h]);
+                    }
+                }
+            }
+        }
+        float ksc, vsc;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(ksc) : "r"(extra + 4 * j));
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(vsc) : "r"(extra + 64 + 4 * j));
+        const bool ok = j < valid;
+
+        // ---- online softmax over the 16 tokens (lane pairs hold equal values)
+        float pv[GQ];
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            float d = dot[h] + __shfl_xor_sync(0xffffffffu, dot[h], 1);
+            float s = ok ? d * ksc * scale_log2 : -INFINITY;
+            float mx = s;
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mnew = fmaxf(st.m[h], mx);
+            const float base = (mnew == -INFINITY) ? 0.f : mnew;
+            const float alpha = fast_exp2(st.m[h] - base);
+            st.m[h] = mnew;
+            const float pj = fast_exp2(s - base);
+            st.l[h] = st.l[h] * alpha + (half == 0 ? pj : 0.f);
+            pv[h] = ok ? pj * vsc : 0.f;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i)
+                st.acc[h][i] *= alpha;
+        }
+
+        // ---- P.V: lane owns d = lane*CPL .. +CPL-1
+#pragma unroll
+        for (int jj = 0; jj < kBlockTokens; ++jj) {
+            float f[4];
+            if constexpr (CPL == 4) {
+                uint32_t w;
+                const uint32_t addr = vt + (uint32_t)(jj * 128 + (((lane >> 2) ^ (jj & 7)) << 4) +
+                                                      (lane & 3) * 4);
+                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(addr));
+                s8x4_to_f32(w, f);
+            } else {
+                uint16_t w;
+                const uint32_t addr = vt + (uint32_t)(jj * 64 + (((lane >> 3) ^ ((jj >> 1) & 3)) << 4) +
+                                                      (lane & 7) * 2);
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(w) : "r"(addr));
+                s8x4_to_f32((uint32_t)w, f);
+            }
+#pragma unroll
+            for (int h = 0; h < GQ; ++h) {
+                const float wgt = __shfl_sync(0xffffffffu, pv[h], 2 * jj);
+#pragma unroll
+                for (int i = 0; i < CPL; ++i)
+                    st.acc[h][i] = fmaf(wgt, f[i], st.acc[h][i]);
+            }
+        }
+    }
+
+    __device__ static void to_merge(State &st, float *merge)
+    {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            float l = st.l[h];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1)
+                l += __shfl_xor_sync(0xffffffffu, l, o);
+            float *mb = merge + (warp * GQ + h) * (D + 2);
+            if (lane == 0) {
+                mb[0] = st.m[h];
+                mb[1] = l;
+            }
+#pragma unroll
+            for (int i = 0; i < CPL; ++i)
+                mb[2 + lane * CPL + i] = st.acc[h][i];
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// The kernel: split, ring, segments, merge.
+// ---------------------------------------------------------------------------
+template <class Pol>
+__global__ void __launch_bounds__(Pol::NW * 32)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const DecodeParams p)
+{
+    constexpr int NW = Pol::NW, S = Pol::S, D = Pol::D, GQ = Pol::GQ;
+    using L = typename Pol::Layout;
+    static_assert(NW <= 8, "misc scratch holds 8 warp sums");
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBars);
+    int32_t *meta = reinterpret_cast<int32_t *>(smem + L::kOffMeta);
+    float *merge = reinterpret_cast<float *>(smem + L::kOffMerge);
+    int32_t *misc = reinterpret_cast<int32_t *>(smem + L::kOffMisc);
+    int32_t *P = reinterpret_cast<int32_t *>(smem + L::kOffPrefix);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n_h = p.n_kv * GQ;
+
+    if (tid == 0) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+    prefix_blocks<NW * 32>(p, P, misc + 8);
+    __syncthreads();
+    zero_empty_sequences<D>(p, P, n_h);
+    const int64_t W = (int64_t)p.n_kv * P[p.num_seqs];
+    if (W == 0)
+        return;
+    const int64_t lo = plan_lo(blockIdx.x, W, p.num_ctas);
+    const int64_t hi = plan_lo(blockIdx.x + 1, W, p.num_ctas);
+    if (lo >= hi)
+        return;
+
+    if (lane == 0)
+        for (int s = 0; s < S; ++s)
+            mbar_init(smem_u32(&bars[warp * S + s]), 1);
+    fence_barrier_init();
+    __syncthreads();
+
+    // ---- per-warp producer state
+    WarpRing r;
+    r.lo = lo;
+    r.warp = warp;
+    r.n_items = (hi - lo > warp) ? (hi - lo - warp + NW - 1) / NW : 0;
+    r.issued = 0;
+    r.batch = 0;
+    r.meta_cur = load_item_row<NW>(p, P, r, lane);
+    r.meta_next = load_item_row<NW>(p, P, r, 32 + lane);
+    const uint64_t pol = l2_policy_evict_first();
+    const uint32_t ring_base = smem_u32(smem) + (uint32_t)(warp * S * Pol::STAGE);
+    const uint32_t extra_base = smem_u32(smem + L::kOffExtra) + (uint32_t)(warp * S * Pol::EXTRA);
+    const uint32_t bar_base = smem_u32(&bars[warp * S]);
+    float *qsm = reinterpret_cast<float *>(smem + L::kOffQ) + warp * (Pol::QBYTES / 4);
+    bool dead = false;      // a wait timed out: stop issuing, skip work
+    int64_t fail_k = -1;    // first item whose wait timed out
+
+    auto issue_next = [&]() {
+        const int64_t k = r.issued;
+        const int64_t bt = k >> 5;
+        if (bt != r.batch) {
+            r.meta_cur = r.meta_next;
+            r.batch = bt;
+            r.meta_next = load_item_row<NW>(p, P, r, (bt + 1) * 32 + lane);
+        }
+        const int32_t row = __shfl_sync(0xffffffffu, r.meta_cur, (int)(k & 31));
+        if (lane == 0) {
+            const int st = (int)(k % S);
+            const uint32_t bar = bar_base + 8u * st;
+            meta[warp * S + st] = row;
+            if (row < 0) {
+                mbar_arrive(bar);
+            } else {
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(bar, Pol::TX);
+                Pol::issue(ring_base + (uint32_t)(st * Pol::STAGE),
+                           extra_base + (uint32_t)(st * Pol::EXTRA), row, bar, &tmK, &tmV, p, pol);
+            }
+        }
+        __syncwarp();
+        r.issued = k + 1;
+    };
+
+    for (int s = 0; s < S; ++s)
+        if (r.issued < r.n_items)
+            issue_next();
+
+    typename Pol::State st;
+    int64_t k = 0; // items of this warp consumed so far
+    int64_t seg_lo = lo;
+    while (seg_lo < hi) {
+        int b, kvh, i0, nb;
+        locate_item(seg_lo, P, p.num_seqs, p.n_kv, b, kvh, i0, nb);
+        const int64_t unit_start = seg_lo - i0;
+        const int64_t unit_end = unit_start + nb;
+        const int64_t seg_hi = unit_end < hi ? unit_end : hi;
+        const bool whole = (i0 == 0) && (unit_end <= hi);
+        const int last_valid = __ldg(p.context_lens + b) - (nb - 1) * kBlockTokens;
+
+        Pol::load_q(st, p, b, kvh, qsm);
+        Pol::reset(st);
+        while (k < r.n_items) {
+            const int64_t x = lo + warp + k * NW;
+            if (x >= seg_hi)
+                break;
+            const int sidx = (int)(k % S);
+            const uint32_t parity = (uint32_t)((k / S) & 1);
+            bool ok = !dead;
+            // every lane waits (acquire); the warp agrees on the outcome
+            if (ok && !__all_sync(0xffffffffu, mbar_wait(bar_base + 8u * sidx, parity))) {
+                ok = false;
+                dead = true;
+                fail_k = k;
+                if (lane == 0)
+                    flag_error(p.dev_status, PA_DEV_TIMEOUT_BIT);
+            }
+            if (ok && meta[warp * S + sidx] >= 0) {
+                const int bi = (int)(x - unit_start);
+                const int valid = (bi == nb - 1) ? last_valid : kBlockTokens;
+                Pol::compute(st, ring_base + (uint32_t)(sidx * Pol::STAGE),
+                             extra_base + (uint32_t)(sidx * Pol::EXTRA), valid, p.scale_log2);
+            }
+            __syncwarp();
+            if (!dead && r.issued < r.n_items)
+                issue_next();
+            ++k;
+        }
+        Pol::to_merge(st, merge);
+        __syncthreads();
+        finish_segment<D, GQ, NW>(p, merge, misc, b, kvh, unit_start, nb, W, whole);
+        seg_lo = seg_hi;
+    }
+
+    // After a timeout, give the copies still in flight a bounded chance to
+    // land before the CTA's shared memory is released.
+    if (dead && lane == 0)
+        for (int64_t kk = fail_k; kk < r.issued; ++kk)
+            mbar_wait(bar_base + 8u * (uint32_t)(kk % S), (uint32_t)((kk / S) & 1));
+}
+
+} // namespace pa

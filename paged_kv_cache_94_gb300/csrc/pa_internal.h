@@ -1,0 +1,36 @@
+// Declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#define PA_DEV_BAD_BLOCK_BIT 0x1
+#define PA_DEV_BAD_SLOT_BIT 0x2
+#define PA_DEV_BAD_CONTEXT_BIT 0x4
+#define PA_DEV_TIMEOUT_BIT 0x8
+
+namespace pa {
+
+struct DecodeParams;
+
+// One compiled decode kernel (a dtype, head dim and group size).
+struct DecodeKernel {
+    const void *fn;                    // __global__ entry (attributes, occupancy)
+    int threads;                       // block size
+    size_t (*smem_bytes)(int num_seqs); // dynamic shared memory for a batch size
+    cudaError_t (*launch)(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
+                          int grid, size_t smem, cudaStream_t stream);
+};
+
+// NULL when the combination is not compiled.
+const DecodeKernel *find_decode_kernel_bf16(int d_h, int group);
+const DecodeKernel *find_decode_kernel_int8(int d_h, int group);
+
+cudaError_t launch_cache_write(const void *k, const void *v, const int64_t *slots, int64_t T,
+                               int n_kv, int d_h, bool int8, int64_t num_slots, void *k_cache,
+                               void *v_cache, float *k_scale, float *v_scale, int32_t *dev_status,
+                               cudaStream_t stream);
+
+} // namespace pa

@@ -1,0 +1,24 @@
+// Work split of the decode kernels, shared by host and device code.
+//
+// W items (sequence, kv head, block) on one line; CTA c of G owns
+// [floor(c*W/G), floor((c+1)*W/G)).
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define PA_HD __host__ __device__ __forceinline__
+#else
+#define PA_HD inline
+#endif
+
+namespace pa {
+
+// First item of CTA c.
+PA_HD int64_t plan_lo(int64_t c, int64_t W, int64_t G) { return c * W / G; }
+
+// The CTA that owns item x (0 <= x < W): the largest c with plan_lo(c) <= x,
+// i.e. ceil((x+1)*G/W) - 1.
+PA_HD int64_t plan_owner(int64_t x, int64_t W, int64_t G) { return ((x + 1) * G - 1) / W; }
+
+} // namespace pa

@@ -1,0 +1,132 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute calls).
+
+The library must load and export every entry point include/pa.h declares;
+argument checks that return before any CUDA call are exercised; the work
+split (pa_plan_owner) is compared with a brute-force assignment.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_94_gb300 as pa
+from paged_kv_cache_94_gb300 import build as pa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pa_build.build()
+    return pa.library()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert sorted(pa.EXPORTED) == _declared()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        getattr(lib, name)
+
+
+def test_status_strings_and_device_words(lib):
+    for code, name in pa.STATUS.items():
+        assert lib.pa_status_string(code).decode().startswith(name)
+    assert lib.pa_status_from_device(0) == 0
+    assert lib.pa_status_from_device(pa.PA_DEV_BAD_BLOCK | pa.PA_DEV_BAD_SLOT) == -5
+    assert lib.pa_status_from_device(pa.PA_DEV_BAD_SLOT) == -6
+    assert lib.pa_status_from_device(pa.PA_DEV_BAD_CONTEXT) == -9
+    assert lib.pa_status_from_device(pa.PA_DEV_TIMEOUT) == -10
+    assert lib.pa_version() >= 100
+
+
+def _geom(**kw):
+    base = dict(num_blocks=100, n_h=32, n_kv=8, d_h=128, block_size=16, kv_dtype=0, reserved=0)
+    base.update(kw)
+    return pa.pa_geom(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n_h=30), -2),           # n_h % n_kv != 0
+    (dict(n_kv=0), -2),
+    (dict(num_blocks=0), -2),
+    (dict(kv_dtype=7), -3),
+    (dict(d_h=96), -4),
+    (dict(block_size=32), -4),
+    (dict(n_h=24, n_kv=1), -4),   # group 24 not compiled
+    (dict(reserved=1), -2),
+    (dict(num_blocks=1 << 27), -4),  # TMA row coordinate overflow
+])
+def test_cache_write_rejects_bad_geometry_before_launch(lib, kw, status):
+    fake = ctypes.c_void_p(256)  # never dereferenced: the call returns before any launch
+    st = lib.pa_cache_write(fake, fake, fake, 4, fake, fake, None, None, _geom(**kw), None, None)
+    assert st == status
+
+
+def test_cache_write_argument_checks(lib):
+    fake = ctypes.c_void_p(256)
+    g = _geom()
+    assert lib.pa_cache_write(fake, fake, fake, 0, fake, fake, None, None, g, None, None) == 0
+    assert lib.pa_cache_write(fake, fake, fake, -1, fake, fake, None, None, g, None, None) == -2
+    assert lib.pa_cache_write(None, fake, fake, 4, fake, fake, None, None, g, None, None) == -1
+    # bf16 pools take no scales; int8 pools need them
+    assert lib.pa_cache_write(fake, fake, fake, 4, fake, fake, fake, fake, g, None, None) == -2
+    g8 = _geom(kv_dtype=1)
+    assert lib.pa_cache_write(fake, fake, fake, 4, fake, fake, None, None, g8, None, None) == -1
+    odd = ctypes.c_void_p(258)
+    assert lib.pa_cache_write(odd, fake, fake, 4, fake, fake, None, None, g, None, None) == -11
+
+
+def test_decode_argument_checks(lib):
+    fake = ctypes.c_void_p(256)
+    g = _geom()
+    args = lambda **o: [o.get("q", fake), fake, fake, o.get("ks"), o.get("vs"), fake,
+                        o.get("mb", 16), fake, o.get("B", 4), 0.1, fake, o.get("ws", fake),
+                        1 << 20, o.get("g", g), None, None]
+    assert lib.pa_decode(*args(B=0)) == 0          # nothing to do
+    assert lib.pa_decode(*args(B=-1)) == -2
+    assert lib.pa_decode(*args(B=9000)) == -2
+    assert lib.pa_decode(*args(mb=0)) == -2
+    assert lib.pa_decode(*args(q=None)) == -1
+    assert lib.pa_decode(*args(ws=None)) == -7
+    assert lib.pa_decode(*args(ks=fake, vs=fake)) == -2
+    assert lib.pa_decode(*args(g=_geom(kv_dtype=1))) == -1
+    assert lib.pa_decode(*args(q=ctypes.c_void_p(264))) == -11
+    assert lib.pa_decode(*args(ws=ctypes.c_void_p(272))) == -11
+    assert lib.pa_decode_ex(*args(), 0) == -2
+    assert lib.pa_decode_workspace_size(_geom(n_h=30), 4, 0) == 0
+
+
+def test_plan_owner_matches_brute_force(lib):
+    for W, G in [(1, 1), (8, 12), (13, 4), (100, 7), (65536, 304), (163840, 152), (999, 1000)]:
+        lo = [c * W // G for c in range(G + 1)]
+        owner = [None] * W
+        for c in range(G):
+            for x in range(lo[c], lo[c + 1]):
+                owner[x] = c
+        step = max(1, W // 2000)
+        for x in list(range(0, W, step)) + [W - 1]:
+            assert lib.pa_plan_owner(x, W, G) == owner[x], (W, G, x)
+        # every CTA's range is within one item of W/G
+        sizes = [lo[c + 1] - lo[c] for c in range(G)]
+        assert max(sizes) - min(sizes) <= 1
+    assert lib.pa_plan_owner(5, 5, 3) == -1
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 4, 64, dtype=torch.bfloat16)
+    kc = torch.zeros(2, 2, 16, 64, dtype=torch.bfloat16)
+    bt = torch.zeros(1, 1, dtype=torch.int32)
+    cl = torch.ones(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        pa.pa_decode(q, kc, kc, bt, cl, 0.125)

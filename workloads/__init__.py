@@ -136,16 +136,25 @@ class Workload:
         return self.block_tables[b, pos // bs].astype(np.int64) * bs + pos % bs
 
     def new_token_slots(self) -> np.ndarray:
-        """int64 [B]: slot of each sequence's new token (position ctx-1)."""
+        """int64 [B]: slot of each sequence's new token (position ctx-1); -1 for an
+        empty sequence (a padding row the append skips)."""
         return np.array([self.slot_of(b, np.array([self.context_lens[b] - 1]))[0]
+                         if self.context_lens[b] > 0 else -1
                          for b in range(self.B)], dtype=np.int64)
 
     def new_kv(self, device="cpu") -> tuple[torch.Tensor, torch.Tensor]:
-        """K/V rows of the new token of every sequence: bf16 [B, n_kv, d_h]."""
+        """K/V rows of the new token of every sequence: bf16 [B, n_kv, d_h]
+        (zeros for an empty sequence)."""
         ks, vs = [], []
         for b in range(self.B):
             ctx = int(self.context_lens[b])
             p = int(self.prefix_len[b])
+            if ctx == 0:
+                z = torch.zeros((self.geom.n_kv, self.geom.d_h), dtype=torch.bfloat16,
+                                device=device)
+                ks.append(z)
+                vs.append(z)
+                continue
             assert ctx - 1 >= p, "new token must be private to its sequence"
             ko, vo = self._gen_rows(b, ctx - p, device)
             ks.append(ko[-1])
