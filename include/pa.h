@@ -211,8 +211,9 @@ int32_t pa_decode_default_ctas(pa_geom geom, int32_t num_seqs);
 
 /* Host-only: how pa_decode splits work. The W = n_kv * sum_b ceil(ctx_b / bs)
  * (sequence, kv head, block) items are laid out sequence-major, kv-head next;
- * CTA c takes items [floor(c*W/G), floor((c+1)*W/G)). For item x this returns
- * the CTA that owns it. Exposed so the split can be checked on a CPU. */
+ * with G = min(num_ctas, W), CTA c < G takes items [floor(c*W/G),
+ * floor((c+1)*W/G)) and CTAs c >= G do nothing. For item x this returns the
+ * CTA that owns it. Exposed so the split can be checked on a CPU. */
 int32_t pa_plan_owner(int64_t item, int64_t total_items, int32_t num_ctas);
 
 /* Human-readable name of a status. Never NULL. */

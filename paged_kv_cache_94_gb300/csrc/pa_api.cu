@@ -332,7 +332,7 @@ int32_t pa_plan_owner(int64_t item, int64_t total_items, int32_t num_ctas)
 {
     if (total_items <= 0 || num_ctas <= 0 || item < 0 || item >= total_items)
         return -1;
-    return (int32_t)pa::plan_owner(item, total_items, num_ctas);
+    return (int32_t)pa::plan_owner(item, total_items, pa::plan_ctas(num_ctas, total_items));
 }
 
 const char *pa_status_string(pa_status s)

@@ -184,7 +184,7 @@ __device__ __forceinline__ void zero_empty_sequences(const DecodeParams &p, cons
 template <int D, int GQ, int NW>
 __device__ __forceinline__ void finish_segment(const DecodeParams &p, const float *merge,
                                                int32_t *misc, int b, int kvh, int64_t unit_start,
-                                               int nb, int64_t W, bool whole)
+                                               int nb, int64_t W, int64_t G, bool whole)
 {
     constexpr int NT = NW * 32;
     constexpr int REC = D + 2;
@@ -226,8 +226,8 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const floa
     // Publish the partial; the last of the nseg CTAs of this unit merges.
     __threadfence();
     __syncthreads();
-    const int64_t c_first = plan_owner(unit_start, W, p.num_ctas);
-    const int64_t c_last = plan_owner(unit_start + nb - 1, W, p.num_ctas);
+    const int64_t c_first = plan_owner(unit_start, W, G);
+    const int64_t c_last = plan_owner(unit_start + nb - 1, W, G);
     if (threadIdx.x == 0) {
         const int nseg = (int)(c_last - c_first + 1);
         const int old = atomicAdd(&p.counters[u], 1);

@@ -449,12 +449,14 @@ __global__ void __launch_bounds__(Pol::NW * 32)
     __syncthreads();
     zero_empty_sequences<D>(p, P, n_h);
     const int64_t W = (int64_t)p.n_kv * P[p.num_seqs];
-    if (W == 0)
+    // At most one CTA per item: then every CTA owns at least one item, and the
+    // CTAs owning a (sequence, kv head) are exactly plan_owner(first) ..
+    // plan_owner(last), which the split merge counts on.
+    const int64_t G = plan_ctas(p.num_ctas, W);
+    if ((int64_t)blockIdx.x >= G)
         return;
-    const int64_t lo = plan_lo(blockIdx.x, W, p.num_ctas);
-    const int64_t hi = plan_lo(blockIdx.x + 1, W, p.num_ctas);
-    if (lo >= hi)
-        return;
+    const int64_t lo = plan_lo(blockIdx.x, W, G);
+    const int64_t hi = plan_lo(blockIdx.x + 1, W, G);
 
     if (lane == 0)
         for (int s = 0; s < S; ++s)
@@ -551,7 +553,7 @@ __global__ void __launch_bounds__(Pol::NW * 32)
         }
         Pol::to_merge(st, merge);
         __syncthreads();
-        finish_segment<D, GQ, NW>(p, merge, misc, b, kvh, unit_start, nb, W, whole);
+        finish_segment<D, GQ, NW>(p, merge, misc, b, kvh, unit_start, nb, W, G, whole);
         seg_lo = seg_hi;
     }
 

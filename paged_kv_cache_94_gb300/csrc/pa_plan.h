@@ -1,7 +1,7 @@
 // Work split of the decode kernels, shared by host and device code.
 //
-// W items (sequence, kv head, block) on one line; CTA c of G owns
-// [floor(c*W/G), floor((c+1)*W/G)).
+// W items (sequence, kv head, block) on one line; CTA c of G = min(grid, W)
+// owns [floor(c*W/G), floor((c+1)*W/G)); CTAs c >= G do no work.
 #pragma once
 
 #include <stdint.h>
@@ -14,7 +14,11 @@
 
 namespace pa {
 
-// First item of CTA c.
+// CTAs that take part: never more than there are items, so that every
+// participating CTA owns at least one item.
+PA_HD int64_t plan_ctas(int64_t grid, int64_t W) { return grid < W ? grid : W; }
+
+// First item of CTA c (G = plan_ctas(grid, W)).
 PA_HD int64_t plan_lo(int64_t c, int64_t W, int64_t G) { return c * W / G; }
 
 // The CTA that owns item x (0 <= x < W): the largest c with plan_lo(c) <= x,

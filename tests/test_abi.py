@@ -107,7 +107,8 @@ def test_decode_argument_checks(lib):
 
 
 def test_plan_owner_matches_brute_force(lib):
-    for W, G in [(1, 1), (8, 12), (13, 4), (100, 7), (65536, 304), (163840, 152), (999, 1000)]:
+    for W, grid in [(1, 1), (8, 12), (13, 4), (100, 7), (65536, 304), (163840, 152), (999, 1000)]:
+        G = min(grid, W)  # never more CTAs than items
         lo = [c * W // G for c in range(G + 1)]
         owner = [None] * W
         for c in range(G):
@@ -115,10 +116,11 @@ def test_plan_owner_matches_brute_force(lib):
                 owner[x] = c
         step = max(1, W // 2000)
         for x in list(range(0, W, step)) + [W - 1]:
-            assert lib.pa_plan_owner(x, W, G) == owner[x], (W, G, x)
-        # every CTA's range is within one item of W/G
+            assert lib.pa_plan_owner(x, W, grid) == owner[x], (W, grid, x)
+        # every CTA's range is non-empty and within one item of W/G, so the
+        # owners of a run of items are a run of CTAs with no gaps
         sizes = [lo[c + 1] - lo[c] for c in range(G)]
-        assert max(sizes) - min(sizes) <= 1
+        assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
     assert lib.pa_plan_owner(5, 5, 3) == -1
 
 
