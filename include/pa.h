@@ -205,6 +205,32 @@ pa_status pa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
                        float scale, void *out, void *workspace, size_t workspace_bytes,
                        pa_geom geom, int32_t *dev_status, void *stream, int32_t num_ctas);
 
+/*
+ * pa_decode_noalloc -- pa_decode without a caller workspace, for callers that
+ * cannot allocate device memory (for example a plugin whose host framework
+ * owns all device memory and forbids allocating inside its execute callback).
+ * The pages have no counterpart: this is a deployment convenience.
+ *
+ * Same arguments and results as pa_decode, minus workspace/workspace_bytes.
+ * The split scratch lives in one fixed array of PA_NOALLOC_SCRATCH_BYTES that
+ * every GPU loading the library holds until the process exits; nothing is
+ * allocated per call. A batch whose pa_decode_workspace_size(geom, num_seqs, 0)
+ * exceeds that size is refused with PA_ERR_WORKSPACE before anything is
+ * enqueued (use pa_decode with a workspace of its own instead).
+ * The first call on a device looks up the array's device address (which may
+ * load the library's device code); make that first call before any stream
+ * capture. Each call clears the array's counter area on `stream`, then runs
+ * the decode there. All calls on a device share the one array, so calls whose
+ * GPU work can overlap (different streams without ordering) race and give
+ * wrong results: order them on one stream.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+pa_status pa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                            const float *k_scale, const float *v_scale,
+                            const int32_t *block_tables, int32_t max_blocks_per_seq,
+                            const int32_t *context_lens, int32_t num_seqs, float scale, void *out,
+                            pa_geom geom, int32_t *dev_status, void *stream);
+
 /* Default CTA count pa_decode uses for this geometry on the current device
  * (>= 1), or a negative pa_status. */
 int32_t pa_decode_default_ctas(pa_geom geom, int32_t num_seqs);

@@ -37,7 +37,8 @@ STATUS = {
     -10: "PA_ERR_TIMEOUT", -11: "PA_ERR_ALIGNMENT",
 }
 EXPORTED = ["pa_cache_write", "pa_decode_workspace_size", "pa_decode_workspace_init",
-            "pa_decode", "pa_decode_ex", "pa_decode_default_ctas", "pa_plan_owner",
+            "pa_decode", "pa_decode_ex", "pa_decode_noalloc", "pa_decode_default_ctas",
+            "pa_plan_owner",
             "pa_status_string", "pa_status_from_device", "pa_version"]
 
 
@@ -85,6 +86,8 @@ def _lib():
         lib.pa_decode.argtypes = dec
         lib.pa_decode_ex.restype = ctypes.c_int
         lib.pa_decode_ex.argtypes = dec + [i32]
+        lib.pa_decode_noalloc.restype = ctypes.c_int
+        lib.pa_decode_noalloc.argtypes = [P, P, P, P, P, P, i32, P, i32, f32, P, pa_geom, P, P]
         lib.pa_decode_default_ctas.restype = i32
         lib.pa_decode_default_ctas.argtypes = [pa_geom, i32]
         lib.pa_plan_owner.restype = i32

@@ -29,6 +29,7 @@ SOURCES = [
     "pa_decode_bf16_d64.cu",
     "pa_decode_int8_d128.cu",
     "pa_decode_int8_d64.cu",
+    "pa_decode_noalloc.cu",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

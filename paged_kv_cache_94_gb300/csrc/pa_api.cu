@@ -370,3 +370,19 @@ pa_status pa_status_from_device(int32_t w)
 int32_t pa_version(void) { return 100; }
 
 } // extern "C"
+
+namespace pa {
+// pa_decode_ex's body with a caller-chosen workspace, for entry points in
+// other translation units (num_ctas = 0: the default grid).
+pa_status decode_with_workspace(const void *q, const void *k_cache, const void *v_cache,
+                                const float *k_scale, const float *v_scale,
+                                const int32_t *block_tables, int32_t max_blocks,
+                                const int32_t *context_lens, int32_t num_seqs, float scale,
+                                void *out, void *workspace, size_t workspace_bytes, pa_geom g,
+                                int32_t *dev_status, void *stream)
+{
+    return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks,
+                       context_lens, num_seqs, scale, out, workspace, workspace_bytes, g,
+                       dev_status, stream, 0);
+}
+} // namespace pa
