@@ -43,9 +43,6 @@ def nvcc() -> str:
     return path if os.path.exists(path) else (shutil.which("nvcc") or "nvcc")
 
 
-STAMP = os.path.join(LIBDIR, "BUILD_STAMP")
-
-
 def _stamp() -> str:
     """Machine + hash of every source the library is built from."""
     h = hashlib.sha256(platform.machine().encode())
@@ -56,9 +53,10 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, build_dir: str, defines: list) -> str:
+    obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *[f"-D{d}" for d in defines], "-c",
+           os.path.join(CSRC, src), "-o", obj]
     if verbose_ptxas:
         cmd[1:1] = ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -69,26 +67,37 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, jobs: int = 0) -> str:
-    """Compile (if stale) and return the path of libpa.so."""
-    stamp = _stamp()
-    if not force and os.path.exists(LIB) and os.path.exists(STAMP) and \
-            open(STAMP).read() == stamp:
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
-    os.makedirs(LIBDIR, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, jobs: int = 0,
+          out_dir: str = "", defines: tuple = ()) -> str:
+    """Compile (if stale) and return the path of libpa.so.
+
+    out_dir/defines build a variant elsewhere (tuning: e.g. defines
+    ("PA_BF16_D128_NW=8",) change the warps per CTA); the default is the
+    in-tree library the package loads.
+    """
+    lib_dir = out_dir or LIBDIR
+    build_dir = os.path.join(out_dir, "_build") if out_dir else BUILD
+    lib = os.path.join(lib_dir, "libpa.so")
+    stamp_path = os.path.join(lib_dir, "BUILD_STAMP")
+    stamp = _stamp() + ":" + ",".join(defines)
+    if not force and os.path.exists(lib) and os.path.exists(stamp_path) and \
+            open(stamp_path).read() == stamp:
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
+    os.makedirs(lib_dir, exist_ok=True)
     jobs = jobs or min(len(SOURCES), os.cpu_count() or 4)
     with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    tmp = LIB + f".{os.getpid()}.tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, build_dir, list(defines)),
+                           SOURCES))
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    with open(STAMP, "w") as f:
+    os.replace(tmp, lib)
+    with open(stamp_path, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

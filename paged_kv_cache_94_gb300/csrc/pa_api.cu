@@ -7,7 +7,7 @@
 #include <cmath>
 #include <mutex>
 
-#include "../../include/pa.h"
+#include "pa.h"
 #include "pa_decode.cuh"
 #include "pa_internal.h"
 

@@ -75,7 +75,7 @@ struct SmemLayout {
     static constexpr int kQ = NW * Q_PER_WARP;                          // per-warp query copy
     static constexpr int kBars = NW * S * 8;
     static constexpr int kMeta = NW * S * 4;
-    static constexpr int kMerge = NW * GQ * (D + 2) * 4;
+    static constexpr int kMerge = NW * GQ * (D + 2) * 4;                // per-warp (m, l, acc)
     static constexpr int kMisc = 64;
     static constexpr int kOffExtra = kRing;
     static constexpr int kOffQ = kOffExtra + kExtra;
@@ -176,10 +176,25 @@ __device__ __forceinline__ void zero_empty_sequences(const DecodeParams &p, cons
     }
 }
 
+// atom.add with acquire-release semantics at GPU scope: releases this CTA's
+// partial record (ordered before it by a CTA barrier) and acquires the
+// records of the CTAs that arrived earlier.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t *addr, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(addr), "r"(v)
+                 : "memory");
+    return old;
+}
+
 // ---------------------------------------------------------------------------
-// End of a segment: merge the NW warp states in `merge` ([NW][GQ][D+2]:
-// m, l, acc[D]) and write the output or a partial; the last CTA of a split
-// (sequence, kv head) merges the partials. Called by all threads.
+// End of a segment: merge the NW warp states (`merge`, [NW][GQ][D+2]: m, l,
+// acc[D], each warp against its own running base) and write the output, or
+// a partial record when the (sequence, kv head) is split over CTAs; the last
+// CTA to publish a record for it merges all records. Called by all threads.
+//   M = max_w m_w,  O = sum_w 2^(m_w-M) acc_w,  L = sum_w 2^(m_w-M) l_w
 // ---------------------------------------------------------------------------
 template <int D, int GQ, int NW>
 __device__ __forceinline__ void finish_segment(const DecodeParams &p, const float *merge,
@@ -193,20 +208,23 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const floa
     __nv_bfloat16 *out = p.out + ((size_t)b * n_h + (size_t)kvh * GQ) * D;
     float *rec = p.partials + ((size_t)blockIdx.x + u) * (GQ * REC);
 
+#pragma unroll 1
     for (int idx = threadIdx.x; idx < GQ * D; idx += NT) {
         const int h = idx / D, d = idx - h * D;
+        float mw[NW];
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w)
-            M = fmaxf(M, merge[(w * GQ + h) * REC]);
+        for (int w = 0; w < NW; ++w) {
+            mw[w] = merge[(w * GQ + h) * REC];
+            M = fmaxf(M, mw[w]);
+        }
         float O = 0.f, L = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
-                const float mw = merge[(w * GQ + h) * REC];
-                const float sc = fast_exp2(mw - M);
-                L += sc * merge[(w * GQ + h) * REC + 1];
-                O += sc * merge[(w * GQ + h) * REC + 2 + d];
+                const float sc = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
+                L = fmaf(sc, merge[(w * GQ + h) * REC + 1], L);
+                O = fmaf(sc, merge[(w * GQ + h) * REC + 2 + d], O);
             }
         }
         if (whole) {
@@ -219,46 +237,59 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const floa
             rec[h * REC + 2 + d] = O;
         }
     }
-    if (whole) {
-        __syncthreads();
+    __syncthreads(); // also: every record store of this CTA is done (CTA scope)
+    if (whole)
         return;
-    }
-    // Publish the partial; the last of the nseg CTAs of this unit merges.
-    __threadfence();
-    __syncthreads();
     const int64_t c_first = plan_owner(unit_start, W, G);
-    const int64_t c_last = plan_owner(unit_start + nb - 1, W, G);
+    const int nseg = (int)(plan_owner(unit_start + nb - 1, W, G) - c_first + 1);
     if (threadIdx.x == 0) {
-        const int nseg = (int)(c_last - c_first + 1);
-        const int old = atomicAdd(&p.counters[u], 1);
+        const int old = atomic_add_acq_rel_gpu(&p.counters[u], 1);
         const int last = (old == nseg - 1);
         if (last)
             p.counters[u] = 0; // every arrival of this launch is in: reset for the next call
         misc[0] = last;
-        __threadfence();
     }
     __syncthreads();
-    if (misc[0]) {
-        const float *base = p.partials + ((size_t)c_first + u) * (GQ * REC);
-        const int nseg = (int)(c_last - c_first + 1);
-        for (int idx = threadIdx.x; idx < GQ * D; idx += NT) {
-            const int h = idx / D, d = idx - h * D;
-            float M = -INFINITY;
-            for (int s = 0; s < nseg; ++s)
-                M = fmaxf(M, __ldcg(base + (size_t)s * GQ * REC + h * REC));
-            float O = 0.f, L = 0.f;
-            if (M != -INFINITY) {
-                for (int s = 0; s < nseg; ++s) {
-                    const float *r = base + (size_t)s * GQ * REC + h * REC;
-                    const float sc = fast_exp2(__ldcg(r) - M);
-                    L += sc * __ldcg(r + 1);
-                    O += sc * __ldcg(r + 2 + d);
+    if (!misc[0])
+        return;
+    // Last arrival: merge the nseg records, loads issued four at a time.
+    const float *base = p.partials + ((size_t)c_first + u) * (GQ * REC);
+#pragma unroll 1
+    for (int idx = threadIdx.x; idx < GQ * D; idx += NT) {
+        const int h = idx / D, d = idx - h * D;
+        float M = -INFINITY;
+#pragma unroll 1
+        for (int s0 = 0; s0 < nseg; s0 += 4) {
+            float m4[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                m4[j] = (s0 + j < nseg) ? __ldcg(base + (size_t)(s0 + j) * GQ * REC + h * REC)
+                                        : -INFINITY;
+            M = fmaxf(M, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+        }
+        float O = 0.f, L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll 1
+            for (int s0 = 0; s0 < nseg; s0 += 4) {
+                float m4[4], l4[4], o4[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = s0 + j < nseg;
+                    const float *r = base + (size_t)(in ? s0 + j : s0) * GQ * REC + h * REC;
+                    m4[j] = in ? __ldcg(r) : -INFINITY;
+                    l4[j] = in ? __ldcg(r + 1) : 0.f;
+                    o4[j] = in ? __ldcg(r + 2 + d) : 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float sc = (m4[j] == -INFINITY) ? 0.f : fast_exp2(m4[j] - M);
+                    L = fmaf(sc, l4[j], L);
+                    O = fmaf(sc, o4[j], O);
                 }
             }
-            out[h * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
         }
+        out[h * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
     }
-    __syncthreads();
 }
 
 // Byte offset of 16-byte chunk `c` of row `r` in a TMA-swizzled tile whose
@@ -280,26 +311,30 @@ struct WarpRing {
     int64_t n_items;   // items this warp owns
     int warp;
     int64_t issued;    // items whose loads were issued
-    int64_t batch;     // index of the 32-item batch held in meta_cur
-    int32_t meta_cur;  // lane l: tile row (phys*n_kv + kvh) of item 32*batch + l, or -1
-    int32_t meta_next; // the same for batch + 1
+    int64_t batch;     // index of the 32-item batch held in the *_cur registers
+    int32_t phys_cur;  // lane l: physical block of item 32*batch + l (raw table entry)
+    int32_t kvh_cur;   //         and its kv head
+    int32_t phys_next; // the same for batch + 1
+    int32_t kvh_next;
 };
 
+// Block-table entry and kv head of this warp's item k. The loaded value is
+// not used here, so the load's latency overlaps other work; the entry is
+// checked when the item is issued.
 template <int NW>
-__device__ __forceinline__ int32_t load_item_row(const DecodeParams &p, const int32_t *P,
-                                                 const WarpRing &r, int64_t k)
+__device__ __forceinline__ void load_item(const DecodeParams &p, const int32_t *P,
+                                          const WarpRing &r, int64_t k, int32_t &phys,
+                                          int32_t &kvh)
 {
-    if (k >= r.n_items)
-        return -1;
-    const int64_t x = r.lo + r.warp + k * NW;
-    int b, kvh, i, nb;
-    locate_item(x, P, p.num_seqs, p.n_kv, b, kvh, i, nb);
-    const int32_t phys = __ldg(p.block_tables + (size_t)b * p.max_blocks + i);
-    if (phys < 0 || (int64_t)phys >= p.num_blocks) {
-        flag_error(p.dev_status, PA_DEV_BAD_BLOCK_BIT);
-        return -1;
+    if (k >= r.n_items) {
+        phys = -1;
+        kvh = 0;
+        return;
     }
-    return phys * p.n_kv + kvh;
+    const int64_t x = r.lo + r.warp + k * NW;
+    int b, i, nb;
+    locate_item(x, P, p.num_seqs, p.n_kv, b, kvh, i, nb);
+    phys = __ldg(p.block_tables + (size_t)b * p.max_blocks + i);
 }
 
 } // namespace pa

@@ -1,6 +1,15 @@
 // Compiled decode kernels: bf16 K/V, head dim 64, group sizes 1..16.
 #include "pa_decode_kernel.cuh"
 
+// Warps per CTA and ring stages per warp (overridable when building for a
+// tuning sweep).
+#ifndef PA_BF16_D64_NW
+#define PA_BF16_D64_NW 4
+#endif
+#ifndef PA_BF16_D64_STAGES
+#define PA_BF16_D64_STAGES 6
+#endif
+
 namespace pa {
 namespace {
 
@@ -19,7 +28,7 @@ cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const Decode
 }
 
 template <int G>
-using Pol = Bf16Policy<64, G, 4, 6>;
+using Pol = Bf16Policy<64, G, PA_BF16_D64_NW, PA_BF16_D64_STAGES>;
 
 template <int G>
 const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G>>),

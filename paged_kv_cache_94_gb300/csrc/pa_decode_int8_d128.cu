@@ -1,6 +1,15 @@
 // Compiled decode kernels: int8 K/V, head dim 128, group sizes 1..16.
 #include "pa_decode_kernel.cuh"
 
+// Warps per CTA and ring stages per warp (overridable when building for a
+// tuning sweep).
+#ifndef PA_INT8_D128_NW
+#define PA_INT8_D128_NW 4
+#endif
+#ifndef PA_INT8_D128_STAGES
+#define PA_INT8_D128_STAGES 3
+#endif
+
 namespace pa {
 namespace {
 
@@ -19,7 +28,7 @@ cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const Decode
 }
 
 template <int G>
-using Pol = Int8Policy<128, G, 4, 6>;
+using Pol = Int8Policy<128, G, PA_INT8_D128_NW, PA_INT8_D128_STAGES>;
 
 template <int G>
 const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G>>),

@@ -18,6 +18,10 @@
 
 namespace pa {
 
+// The running softmax base moves only when a tile's max exceeds it by more
+// than this (log2 units): softmax weights stay <= 2^8 between rescales.
+constexpr float kRescaleLog2 = 8.0f;
+
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -156,55 +160,87 @@ struct Bf16Policy {
                 sc[2] = -INFINITY;
                 sc[3] = -INFINITY;
             }
+            // Lazy rescale: the running base m only moves when a tile's max
+            // exceeds it by more than 2^kRescaleLog2; otherwise weights up to
+            // 2^kRescaleLog2 are accumulated against the old base (exact: acc
+            // and l always share one base).
+            float alpha[2];
+            bool need = false;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 float mx = fmaxf(sc[e], sc[e + 2]);
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float mnew = fmaxf(st.m[nt][e], mx);
-                const float base = (mnew == -INFINITY) ? 0.f : mnew;
-                const float alpha = fast_exp2(st.m[nt][e] - base);
+                const bool up = mx > st.m[nt][e] + kRescaleLog2;
+                const float mnew = up ? mx : st.m[nt][e];
+                alpha[e] = up ? fast_exp2(st.m[nt][e] - mnew) : 1.f;
+                need |= up;
                 st.m[nt][e] = mnew;
+                const float base = (mnew == -INFINITY) ? 0.f : mnew;
                 sc[e] = fast_exp2(sc[e] - base);
                 sc[e + 2] = fast_exp2(sc[e + 2] - base);
-                st.l[nt][e] = st.l[nt][e] * alpha + sc[e] + sc[e + 2];
+            }
+            if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    st.acc[nt][mt][e] *= alpha;
-                    st.acc[nt][mt][e + 2] *= alpha;
+                for (int e = 0; e < 2; ++e) {
+                    st.l[nt][e] *= alpha[e];
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        st.acc[nt][mt][e] *= alpha[e];
+                        st.acc[nt][mt][e + 2] *= alpha[e];
+                    }
                 }
             }
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                st.l[nt][e] += sc[e] + sc[e + 2];
             pb0[nt] = movmatrix_trans(pack_bf16x2(sc[0], sc[1]));
             pb1[nt] = movmatrix_trans(pack_bf16x2(sc[2], sc[3]));
         }
 
-        // ---- O^T += V^T P^T
-        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-        if (valid < kBlockTokens) {
+        // ---- O^T += V^T P^T. Rows of V past `valid` may hold anything (even
+        // NaN): their operand halves are zeroed, since 0 * NaN is NaN.
+        if (valid == kBlockTokens) {
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4_trans(v_addr(vt, mt, mi, rr), a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_bf16_16816(st.acc[nt][mt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+            }
+        } else {
             const int t0 = 2 * t4;
-            mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-            mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
-        }
+            const uint32_t mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+            const uint32_t mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            const int tok = rr + ((mi >> 1) << 3);
-            const int chunk = 2 * mt + (mi & 1);
-            const uint32_t addr = vt + (chunk >> 3) * (TILE / HALVES) + (uint32_t)(tok * 128) +
-                                  (uint32_t)(((chunk & 7) ^ rr) << 4);
-            uint32_t a0, a1, a2, a3;
-            ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-            a0 &= mlo;
-            a1 &= mlo;
-            a2 &= mhi;
-            a3 &= mhi;
+            for (int mt = 0; mt < KS; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4_trans(v_addr(vt, mt, mi, rr), a0, a1, a2, a3);
+                a0 &= mlo;
+                a1 &= mlo;
+                a2 &= mhi;
+                a3 &= mhi;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                mma_bf16_16816(st.acc[nt][mt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_bf16_16816(st.acc[nt][mt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+            }
         }
     }
 
-    __device__ static void to_merge(State &st, float *merge)
+    // ldmatrix.trans row address of V^T m-tile mt: matrices (tokens 0-7 | 8-15)
+    // x (d 16mt..+7 | +8..+15) in the order a0..a3 expects.
+    __device__ static uint32_t v_addr(uint32_t vt, int mt, int mi, int rr)
+    {
+        const int tok = rr + ((mi >> 1) << 3);
+        const int chunk = 2 * mt + (mi & 1);
+        return vt + (chunk >> 3) * (TILE / HALVES) + (uint32_t)(tok * 128) +
+               (uint32_t)(((chunk & 7) ^ rr) << 4);
+    }
+
+    // This warp's state -> its slice of the merge area: [warp][h] = (m, l, acc[D]).
+    __device__ static void to_merge(const State &st, float *merge)
     {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
 #pragma unroll
@@ -358,16 +394,19 @@ struct Int8Policy {
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float mnew = fmaxf(st.m[h], mx);
-            const float base = (mnew == -INFINITY) ? 0.f : mnew;
-            const float alpha = fast_exp2(st.m[h] - base);
-            st.m[h] = mnew;
-            const float pj = fast_exp2(s - base);
-            st.l[h] = st.l[h] * alpha + (half == 0 ? pj : 0.f);
-            pv[h] = ok ? pj * vsc : 0.f;
+            // lazy rescale, as in the bf16 policy (mx is the same in all lanes)
+            if (mx > st.m[h] + kRescaleLog2) {
+                const float alpha = fast_exp2(st.m[h] - mx);
+                st.m[h] = mx;
+                st.l[h] *= alpha;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i)
-                st.acc[h][i] *= alpha;
+                for (int i = 0; i < CPL; ++i)
+                    st.acc[h][i] *= alpha;
+            }
+            const float base = (st.m[h] == -INFINITY) ? 0.f : st.m[h];
+            const float pj = fast_exp2(s - base);
+            st.l[h] += (half == 0 ? pj : 0.f);
+            pv[h] = ok ? pj * vsc : 0.f;
         }
 
         // ---- P.V: lane owns d = lane*CPL .. +CPL-1
@@ -397,7 +436,7 @@ struct Int8Policy {
         }
     }
 
-    __device__ static void to_merge(State &st, float *merge)
+    __device__ static void to_merge(const State &st, float *merge)
     {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
@@ -471,39 +510,47 @@ __global__ void __launch_bounds__(Pol::NW * 32)
     r.n_items = (hi - lo > warp) ? (hi - lo - warp + NW - 1) / NW : 0;
     r.issued = 0;
     r.batch = 0;
-    r.meta_cur = load_item_row<NW>(p, P, r, lane);
-    r.meta_next = load_item_row<NW>(p, P, r, 32 + lane);
+    load_item<NW>(p, P, r, lane, r.phys_cur, r.kvh_cur);
+    load_item<NW>(p, P, r, 32 + lane, r.phys_next, r.kvh_next);
     const uint64_t pol = l2_policy_evict_first();
     const uint32_t ring_base = smem_u32(smem) + (uint32_t)(warp * S * Pol::STAGE);
     const uint32_t extra_base = smem_u32(smem + L::kOffExtra) + (uint32_t)(warp * S * Pol::EXTRA);
     const uint32_t bar_base = smem_u32(&bars[warp * S]);
+    int32_t *wmeta = meta + warp * S;
     float *qsm = reinterpret_cast<float *>(smem + L::kOffQ) + warp * (Pol::QBYTES / 4);
-    bool dead = false;      // a wait timed out: stop issuing, skip work
-    int64_t fail_k = -1;    // first item whose wait timed out
+    bool dead = false;    // a wait timed out: stop issuing, skip work
+    int64_t fail_k = -1;  // first item whose wait timed out
+    int istage = 0;       // ring stage the next issue goes to
 
     auto issue_next = [&]() {
         const int64_t k = r.issued;
         const int64_t bt = k >> 5;
         if (bt != r.batch) {
-            r.meta_cur = r.meta_next;
+            r.phys_cur = r.phys_next;
+            r.kvh_cur = r.kvh_next;
             r.batch = bt;
-            r.meta_next = load_item_row<NW>(p, P, r, (bt + 1) * 32 + lane);
+            load_item<NW>(p, P, r, (bt + 1) * 32 + lane, r.phys_next, r.kvh_next);
         }
-        const int32_t row = __shfl_sync(0xffffffffu, r.meta_cur, (int)(k & 31));
+        const int32_t phys = __shfl_sync(0xffffffffu, r.phys_cur, (int)(k & 31));
+        const int32_t kvh = __shfl_sync(0xffffffffu, r.kvh_cur, (int)(k & 31));
         if (lane == 0) {
-            const int st = (int)(k % S);
-            const uint32_t bar = bar_base + 8u * st;
-            meta[warp * S + st] = row;
-            if (row < 0) {
-                mbar_arrive(bar);
+            const uint32_t bar = bar_base + 8u * istage;
+            const bool bad = phys < 0 || (int64_t)phys >= p.num_blocks;
+            const int32_t row = bad ? -1 : phys * p.n_kv + kvh;
+            wmeta[istage] = row;
+            if (bad) {
+                flag_error(p.dev_status, PA_DEV_BAD_BLOCK_BIT);
+                mbar_arrive(bar); // completes the phase with no data: the item is skipped
             } else {
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar, Pol::TX);
-                Pol::issue(ring_base + (uint32_t)(st * Pol::STAGE),
-                           extra_base + (uint32_t)(st * Pol::EXTRA), row, bar, &tmK, &tmV, p, pol);
+                Pol::issue(ring_base + (uint32_t)(istage * Pol::STAGE),
+                           extra_base + (uint32_t)(istage * Pol::EXTRA), row, bar, &tmK, &tmV, p,
+                           pol);
             }
         }
         __syncwarp();
+        istage = (istage + 1 == S) ? 0 : istage + 1;
         r.issued = k + 1;
     };
 
@@ -512,7 +559,9 @@ __global__ void __launch_bounds__(Pol::NW * 32)
             issue_next();
 
     typename Pol::State st;
-    int64_t k = 0; // items of this warp consumed so far
+    int64_t k = 0;        // items of this warp consumed so far
+    int cstage = 0;       // ring stage of item k
+    uint32_t cphase = 0;  // barrier phase parity of item k
     int64_t seg_lo = lo;
     while (seg_lo < hi) {
         int b, kvh, i0, nb;
@@ -525,31 +574,32 @@ __global__ void __launch_bounds__(Pol::NW * 32)
 
         Pol::load_q(st, p, b, kvh, qsm);
         Pol::reset(st);
-        while (k < r.n_items) {
-            const int64_t x = lo + warp + k * NW;
-            if (x >= seg_hi)
-                break;
-            const int sidx = (int)(k % S);
-            const uint32_t parity = (uint32_t)((k / S) & 1);
+        int64_t x = lo + warp + k * NW;
+        while (k < r.n_items && x < seg_hi) {
             bool ok = !dead;
             // every lane waits (acquire); the warp agrees on the outcome
-            if (ok && !__all_sync(0xffffffffu, mbar_wait(bar_base + 8u * sidx, parity))) {
+            if (ok && !__all_sync(0xffffffffu, mbar_wait(bar_base + 8u * cstage, cphase))) {
                 ok = false;
                 dead = true;
                 fail_k = k;
                 if (lane == 0)
                     flag_error(p.dev_status, PA_DEV_TIMEOUT_BIT);
             }
-            if (ok && meta[warp * S + sidx] >= 0) {
+            if (ok && wmeta[cstage] >= 0) {
                 const int bi = (int)(x - unit_start);
                 const int valid = (bi == nb - 1) ? last_valid : kBlockTokens;
-                Pol::compute(st, ring_base + (uint32_t)(sidx * Pol::STAGE),
-                             extra_base + (uint32_t)(sidx * Pol::EXTRA), valid, p.scale_log2);
+                Pol::compute(st, ring_base + (uint32_t)(cstage * Pol::STAGE),
+                             extra_base + (uint32_t)(cstage * Pol::EXTRA), valid, p.scale_log2);
             }
             __syncwarp();
             if (!dead && r.issued < r.n_items)
                 issue_next();
             ++k;
+            x += NW;
+            if (++cstage == S) {
+                cstage = 0;
+                cphase ^= 1u;
+            }
         }
         Pol::to_merge(st, merge);
         __syncthreads();

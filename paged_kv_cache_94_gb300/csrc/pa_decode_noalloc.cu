@@ -18,7 +18,7 @@
 
 #include <mutex>
 
-#include "../../include/pa.h"
+#include "pa.h"
 
 namespace pa {
 pa_status decode_with_workspace(const void *q, const void *k_cache, const void *v_cache,
