@@ -9,6 +9,11 @@
 #ifndef PA_BF16_D128_STAGES
 #define PA_BF16_D128_STAGES 2
 #endif
+// g = 16 keeps four warps: its per-warp merge slices (16 heads x 128 fp32)
+// would not fit next to an 8-warp ring at large batch sizes.
+#ifndef PA_BF16_D128_NW_G16
+#define PA_BF16_D128_NW_G16 4
+#endif
 
 namespace pa {
 namespace {
@@ -28,7 +33,7 @@ cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const Decode
 }
 
 template <int G>
-using Pol = Bf16Policy<128, G, PA_BF16_D128_NW, PA_BF16_D128_STAGES>;
+using Pol = Bf16Policy<128, G, (G >= 16 ? PA_BF16_D128_NW_G16 : PA_BF16_D128_NW), PA_BF16_D128_STAGES>;
 
 template <int G>
 const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G>>),
