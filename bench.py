@@ -44,7 +44,7 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB of L2
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=CONFIG_NAMES, default=DEFAULT_WORKLOAD)
@@ -109,10 +109,16 @@ def peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+# Device code of the decode kernel: its DRAM counters depend on these files only.
+DECODE_DEVICE_SOURCES = ["pa_ptx.cuh", "pa_plan.h", "pa_internal.h", "pa_decode.cuh",
+                         "pa_decode_kernel.cuh", "pa_decode_bf16_d128.cu", "pa_decode_bf16_d64.cu",
+                         "pa_decode_int8_d128.cu", "pa_decode_int8_d64.cu"]
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_94_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in DECODE_DEVICE_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -147,7 +153,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None

@@ -175,6 +175,7 @@ def pa_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
 
 
 _WS: dict = {}
+_WS_SIZES: dict = {}
 _WS_LOCK = threading.Lock()
 
 
@@ -190,10 +191,14 @@ def decode_workspace(g: pa_geom, num_seqs: int, device: torch.device, num_ctas: 
     so the cache only re-zeroes it when a call needs a larger counter area
     than the buffer has had zeroed so far.
     """
-    nbytes = _lib().pa_decode_workspace_size(g, num_seqs, num_ctas)
-    if nbytes == 0:
-        raise PAError(-2, "pa_decode_workspace_size")
     key = device.index if device.index is not None else torch.cuda.current_device()
+    size_key = (key, g.num_blocks, g.n_h, g.n_kv, g.d_h, g.kv_dtype, num_seqs, num_ctas)
+    nbytes = _WS_SIZES.get(size_key)
+    if nbytes is None:
+        nbytes = _lib().pa_decode_workspace_size(g, num_seqs, num_ctas)
+        if nbytes == 0:
+            raise PAError(-2, "pa_decode_workspace_size")
+        _WS_SIZES[size_key] = nbytes
     need_zero = _counter_bytes(g, num_seqs)
     with _WS_LOCK:
         ent = _WS.get(key)

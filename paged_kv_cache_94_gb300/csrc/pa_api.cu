@@ -71,15 +71,54 @@ pa_status current_device(int &dev, int &sms)
     return PA_OK;
 }
 
-// Resident CTAs per SM of a kernel at a given shared-memory size. Sets the
-// kernel's dynamic shared-memory limit on the current device first.
+// Resident CTAs per SM of a kernel at a given shared-memory size on the
+// current device. The kernel's dynamic shared-memory limit is raised once per
+// (kernel, device) to the device maximum; results are cached per (kernel,
+// device, size), so steady-state calls make no CUDA runtime queries.
+struct OccEntry {
+    const void *fn;
+    int dev;
+    size_t smem;
+    int per_sm;
+};
+constexpr int kOccCache = 64;
+OccEntry g_occ[kOccCache];
+int g_occ_n = 0;
+struct AttrEntry {
+    const void *fn;
+    int dev;
+};
+AttrEntry g_attr[kOccCache];
+int g_attr_n = 0;
+
 pa_status ctas_per_sm(const DecodeKernel *kd, size_t smem, int &n)
 {
-    if (cudaFuncSetAttribute(kd->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
         return PA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_occ_n; ++i)
+        if (g_occ[i].fn == kd->fn && g_occ[i].dev == dev && g_occ[i].smem == smem) {
+            n = g_occ[i].per_sm;
+            return n > 0 ? PA_OK : PA_ERR_UNSUPPORTED;
+        }
+    bool attr_set = false;
+    for (int i = 0; i < g_attr_n; ++i)
+        attr_set |= (g_attr[i].fn == kd->fn && g_attr[i].dev == dev);
+    if (!attr_set) {
+        int max_optin = 0;
+        if (cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(kd->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin) !=
+                cudaSuccess)
+            return PA_ERR_CUDA;
+        if (g_attr_n < kOccCache)
+            g_attr[g_attr_n++] = {kd->fn, dev};
+    }
+    n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kd->fn, kd->threads, smem) != cudaSuccess)
         return PA_ERR_CUDA;
+    g_occ[g_occ_n < kOccCache ? g_occ_n++ : (int)(smem % kOccCache)] = {kd->fn, dev, smem, n};
     if (n <= 0)
         return PA_ERR_UNSUPPORTED; // does not fit on an SM
     return PA_OK;
@@ -134,7 +173,7 @@ EncodeTiledFn encode_fn()
 // 2-D view of a pool: rows of d_h elements, one row per (block, head, offset);
 // a box is one 16-row tile of at most 128 bytes per row, swizzled so that
 // ldmatrix/ld.shared of 8 consecutive rows hit distinct banks.
-pa_status encode_pool(CUtensorMap &m, const void *base, const pa_geom &g)
+pa_status encode_pool_uncached(CUtensorMap &m, const void *base, const pa_geom &g)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -153,6 +192,44 @@ pa_status encode_pool(CUtensorMap &m, const void *base, const pa_geom &g)
            const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+// Encoded maps are cached by (pool address, geometry): a decode step reuses
+// the same pools call after call. A map only describes the pool's address and
+// shape, so a hit is exact.
+struct MapEntry {
+    const void *base;
+    int64_t num_blocks;
+    int32_t n_kv, d_h, kv_dtype;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 64;
+MapEntry g_maps[kMapCache];
+int g_maps_n = 0, g_maps_next = 0;
+
+pa_status encode_pool(CUtensorMap &m, const void *base, const pa_geom &g)
+{
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (int i = 0; i < g_maps_n; ++i) {
+            const MapEntry &e = g_maps[i];
+            if (e.base == base && e.num_blocks == g.num_blocks && e.n_kv == g.n_kv &&
+                e.d_h == g.d_h && e.kv_dtype == g.kv_dtype) {
+                m = e.map;
+                return PA_OK;
+            }
+        }
+    }
+    const pa_status st = encode_pool_uncached(m, base, g);
+    if (st != PA_OK)
+        return st;
+    std::lock_guard<std::mutex> lk(g_mu);
+    MapEntry &e = g_maps[g_maps_next];
+    e = {base, g.num_blocks, g.n_kv, g.d_h, g.kv_dtype, m};
+    g_maps_next = (g_maps_next + 1) % kMapCache;
+    if (g_maps_n < kMapCache)
+        ++g_maps_n;
+    return PA_OK;
 }
 
 pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, const float *k_scale,
