@@ -111,7 +111,7 @@ def peaks() -> dict:
 
 # Device code of the decode kernel: its DRAM counters depend on these files only.
 DECODE_DEVICE_SOURCES = ["pa_ptx.cuh", "pa_plan.h", "pa_internal.h", "pa_decode.cuh",
-                         "pa_decode_kernel.cuh", "pa_decode_bf16_d128.cu", "pa_decode_bf16_d64.cu",
+                         "pa_decode_kernel.cuh", "pa_decode_int8.cuh", "pa_decode_bf16_d128.cu", "pa_decode_bf16_d64.cu",
                          "pa_decode_int8_d128.cu", "pa_decode_int8_d64.cu"]
 
 

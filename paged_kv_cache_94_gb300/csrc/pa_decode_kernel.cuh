@@ -7,16 +7,23 @@
 //              Tokens sit on the M side, so the query group only pads N to 8;
 //              P^T is moved from the accumulator layout to the B-operand
 //              layout with movmatrix.
-//  Int8Policy: K/V tiles as int8 codes plus an fp32 scale per row
-//              ("kv-cache-guide" (guijiagi.com) §4.2, dequantize_kv:
-//              x = code * scale); codes become exact fp32 values and the
-//              dot products run as fp32 FMA. The K scale multiplies the score,
-//              the V scale multiplies the softmax weight.
+//  Int8MmaPolicy (pa_decode_int8.cuh): K/V tiles as int8 codes plus an
+//              fp32 scale per row ("kv-cache-guide" (guijiagi.com) §4.2,
+//              dequantize_kv: x = code * scale); codes become exact fp16
+//              values and both contractions run as mma.sync f16. The K scale
+//              multiplies the score, the V scale the softmax weight.
 #pragma once
 
 #include "pa_decode.cuh"
 
 namespace pa {
+
+// L2 policy of the K/V tile loads: evict_first (the KV stream is read once;
+// measured faster than evict_normal on every bf16 workload, and no slower on
+// the shared-prefix INT8 one).
+#ifndef PA_KV_EVICT_FIRST
+#define PA_KV_EVICT_FIRST 1
+#endif
 
 // The running softmax base moves only when a tile's max exceeds it by more
 // than this (log2 units): softmax weights stay <= 2^8 between rescales.
@@ -25,18 +32,6 @@ constexpr float kRescaleLog2 = 8.0f;
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-// Exact fp32 value of signed byte k of `w` (k = 0..3). Adding 2^23 + 128 to an
-// unsigned byte u gives a float whose low mantissa bits are u; subtracting
-// 2^23 + 128 again recovers u - 128 = the signed value exactly.
-__device__ __forceinline__ void s8x4_to_f32(uint32_t w, float (&f)[4])
-{
-    const uint32_t u = w ^ 0x80808080u;
-    f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - 8388736.f;
-    f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - 8388736.f;
-    f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - 8388736.f;
-    f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - 8388736.f;
 }
 
 // ---------------------------------------------------------------------------
@@ -268,194 +263,11 @@ struct Bf16Policy {
     }
 };
 
-// ---------------------------------------------------------------------------
-// INT8 K/V (codes + fp32 per-row scales), fp32 FMA contractions.
-// ---------------------------------------------------------------------------
-template <int D_, int GQ_, int NW_, int S_>
-struct Int8Policy {
-    static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_;
-    static constexpr bool kInt8 = true;
-    static constexpr int ROWB = D;                 // bytes per tile row: 128 or 64
-    static constexpr int TILE = kBlockTokens * D;  // bytes of a K (or V) code tile
-    static constexpr int STAGE = 2 * TILE;
-    static constexpr int EXTRA = 128;              // 16 K scales + 16 V scales
-    static constexpr int QBYTES = GQ > 1 ? GQ * D * 4 : 0;
-    static constexpr uint32_t TX = STAGE + EXTRA;
-    static constexpr int HALF = D / 2;             // d values per lane in the score loop
-    static constexpr int CH = HALF / 16;           // 16-byte chunks per half row
-    static constexpr int CPL = D / 32;             // d values per lane in the P.V loop
-    using Layout = SmemLayout<D, GQ, NW, S, STAGE, EXTRA, QBYTES>;
+} // namespace pa
 
-    struct State {
-        float qr[GQ == 1 ? HALF : 1]; // query half-row in registers (g == 1)
-        const float *qs;              // per-warp fp32 query copy [GQ][D] (g > 1)
-        float m[GQ], l[GQ];
-        float acc[GQ][CPL];
-    };
+#include "pa_decode_int8.cuh"
 
-    __device__ static void issue(uint32_t dst, uint32_t extra, int32_t row, uint32_t bar,
-                                 const CUtensorMap *tk, const CUtensorMap *tv,
-                                 const DecodeParams &p, uint64_t pol)
-    {
-        const int32_t y = row * kBlockTokens;
-        tma_load_2d(dst, tk, 0, y, bar, pol);
-        tma_load_2d(dst + TILE, tv, 0, y, bar, pol);
-        bulk_load_1d(extra, p.k_scale + (size_t)row * kBlockTokens, 64, bar, pol);
-        bulk_load_1d(extra + 64, p.v_scale + (size_t)row * kBlockTokens, 64, bar, pol);
-    }
-
-    __device__ static void load_q(State &st, const DecodeParams &p, int b, int kvh, float *qsm)
-    {
-        const int lane = threadIdx.x & 31;
-        const int n_h = p.n_kv * GQ;
-        const __nv_bfloat16 *qb = p.q + ((size_t)b * n_h + (size_t)kvh * GQ) * D;
-        if constexpr (GQ == 1) {
-            const int half = lane & 1;
-#pragma unroll
-            for (int i = 0; i < HALF; i += 2) {
-                const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(qb + half * HALF + i));
-                st.qr[i] = __uint_as_float(w << 16);
-                st.qr[i + 1] = __uint_as_float(w & 0xffff0000u);
-            }
-            st.qs = nullptr;
-        } else {
-            __syncwarp();
-            for (int i = lane; i < GQ * D; i += 32)
-                qsm[i] = __bfloat162float(qb[i]);
-            __syncwarp();
-            st.qs = qsm;
-        }
-    }
-
-    __device__ static void reset(State &st)
-    {
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) {
-            st.m[h] = -INFINITY;
-            st.l[h] = 0.f;
-#pragma unroll
-            for (int i = 0; i < CPL; ++i)
-                st.acc[h][i] = 0.f;
-        }
-    }
-
-    __device__ static void compute(State &st, uint32_t kt, uint32_t extra, int valid,
-                                   float scale_log2)
-    {
-        const int lane = threadIdx.x & 31;
-        const int j = lane >> 1, half = lane & 1;
-        const uint32_t vt = kt + TILE;
-
-        // ---- scores: lane pair (2j, 2j+1) covers token j, one half-row each
-        float dot[GQ];
-#pragma unroll
-        for (int h = 0; h < GQ; ++h)
-            dot[h] = 0.f;
-#pragma unroll
-        for (int c = 0; c < CH; ++c) {
-            const int chunk = half * CH + c;
-            uint32_t w0, w1, w2, w3;
-            const uint32_t addr = kt + (ROWB == 128 ? (uint32_t)(j * 128 + ((chunk ^ (j & 7)) << 4))
-                                                    : (uint32_t)(j * 64 + ((chunk ^ ((j >> 1) & 3)) << 4)));
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                         : "r"(addr));
-            const uint32_t ws[4] = {w0, w1, w2, w3};
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float f[4];
-                s8x4_to_f32(ws[q4], f);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int dl = c * 16 + q4 * 4 + e; // d within this lane's half
-                    if constexpr (GQ == 1) {
-                        dot[0] = fmaf(st.qr[dl], f[e], dot[0]);
-                    } else {
-#pragma unroll
-                        for (int h = 0; h < GQ; ++h)
-                            dot[h] = fmaf(st.qs[h * D + half * HALF + dl], f[e], dot[h]);
-                    }
-                }
-            }
-        }
-        float ksc, vsc;
-        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(ksc) : "r"(extra + 4 * j));
-        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(vsc) : "r"(extra + 64 + 4 * j));
-        const bool ok = j < valid;
-
-        // ---- online softmax over the 16 tokens (lane pairs hold equal values)
-        float pv[GQ];
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) {
-            float d = dot[h] + __shfl_xor_sync(0xffffffffu, dot[h], 1);
-            float s = ok ? d * ksc * scale_log2 : -INFINITY;
-            float mx = s;
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            // lazy rescale, as in the bf16 policy (mx is the same in all lanes)
-            if (mx > st.m[h] + kRescaleLog2) {
-                const float alpha = fast_exp2(st.m[h] - mx);
-                st.m[h] = mx;
-                st.l[h] *= alpha;
-#pragma unroll
-                for (int i = 0; i < CPL; ++i)
-                    st.acc[h][i] *= alpha;
-            }
-            const float base = (st.m[h] == -INFINITY) ? 0.f : st.m[h];
-            const float pj = fast_exp2(s - base);
-            st.l[h] += (half == 0 ? pj : 0.f);
-            pv[h] = ok ? pj * vsc : 0.f;
-        }
-
-        // ---- P.V: lane owns d = lane*CPL .. +CPL-1
-#pragma unroll
-        for (int jj = 0; jj < kBlockTokens; ++jj) {
-            float f[4];
-            if constexpr (CPL == 4) {
-                uint32_t w;
-                const uint32_t addr = vt + (uint32_t)(jj * 128 + (((lane >> 2) ^ (jj & 7)) << 4) +
-                                                      (lane & 3) * 4);
-                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(addr));
-                s8x4_to_f32(w, f);
-            } else {
-                uint16_t w;
-                const uint32_t addr = vt + (uint32_t)(jj * 64 + (((lane >> 3) ^ ((jj >> 1) & 3)) << 4) +
-                                                      (lane & 7) * 2);
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(w) : "r"(addr));
-                s8x4_to_f32((uint32_t)w, f);
-            }
-#pragma unroll
-            for (int h = 0; h < GQ; ++h) {
-                const float wgt = __shfl_sync(0xffffffffu, pv[h], 2 * jj);
-#pragma unroll
-                for (int i = 0; i < CPL; ++i)
-                    st.acc[h][i] = fmaf(wgt, f[i], st.acc[h][i]);
-            }
-        }
-    }
-
-    __device__ static void to_merge(const State &st, float *merge)
-    {
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) {
-            float l = st.l[h];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1)
-                l += __shfl_xor_sync(0xffffffffu, l, o);
-            float *mb = merge + (warp * GQ + h) * (D + 2);
-            if (lane == 0) {
-                mb[0] = st.m[h];
-                mb[1] = l;
-            }
-#pragma unroll
-            for (int i = 0; i < CPL; ++i)
-                mb[2 + lane * CPL + i] = st.acc[h][i];
-        }
-    }
-};
+namespace pa {
 
 // ---------------------------------------------------------------------------
 // The kernel: split, ring, segments, merge.
@@ -512,7 +324,7 @@ __global__ void __launch_bounds__(Pol::NW * 32)
     r.batch = 0;
     load_item<NW>(p, P, r, lane, r.phys_cur, r.kvh_cur);
     load_item<NW>(p, P, r, 32 + lane, r.phys_next, r.kvh_next);
-    const uint64_t pol = l2_policy_evict_first();
+    const uint64_t pol = PA_KV_EVICT_FIRST ? l2_policy_evict_first() : l2_policy_evict_normal();
     const uint32_t ring_base = smem_u32(smem) + (uint32_t)(warp * S * Pol::STAGE);
     const uint32_t extra_base = smem_u32(smem + L::kOffExtra) + (uint32_t)(warp * S * Pol::EXTRA);
     const uint32_t bar_base = smem_u32(&bars[warp * S]);
