@@ -11,6 +11,8 @@ decode kernel's fraction of the measured HBM peak and sequences/s.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
+  python bench.py --op block_copy        # copy-on-write block copies, HBM GB/s
+  python bench.py --op allocator         # host block manager, appends/s
 
 With N > 1 (torchrun) every rank runs an independent replica of the same
 workload on its own GPU (the path has no cross-GPU exchange): weak scaling,
@@ -53,6 +55,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--num-ctas", type=int, default=0, help="force the decode split (tuning)")
+    ap.add_argument("--op", choices=["step", "block_copy", "allocator"], default="step",
+                    help="step: the decode step (default); block_copy: pa_block_copy; "
+                         "allocator: the host block manager")
+    ap.add_argument("--pairs", type=int, default=4096, help="block pairs per pa_block_copy")
     return ap.parse_args()
 
 
@@ -373,6 +379,197 @@ def run_native(args, rank, world, local_rank):
     return result
 
 
+# ---------------------------------------------------------------- block copy
+def block_copy_bytes(g, pairs: int) -> int:
+    """Read + write of every copied block: K and V tiles (+ INT8 scales)."""
+    tile = g.n_kv * 16 * g.d_h * (1 if g.kv_dtype == "int8" else 2)
+    scales = 2 * g.n_kv * 16 * 4 if g.kv_dtype == "int8" else 0
+    return 2 * pairs * (2 * tile + scales) + 8 * pairs
+
+
+def run_block_copy(args, rank, world, local_rank):
+    """pa_block_copy of --pairs (source, destination) blocks of the workload's
+    pool geometry, one launch per step, L2 flushed between launches."""
+    import paged_kv_cache_94_gb300 as pa
+    from paged_kv_cache_94_gb300 import build as pa_build
+    from workloads import block_copy_pairs
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    pa_build.build()
+    w = named_workload(args.workload)
+    g = w.geom
+    nb = max(w.num_blocks, 2 * args.pairs)
+    kc, vc, ks, vs = pa.allocate_pool(nb, g.n_kv, g.d_h, g.kv_dtype, dev)
+    kc.view(torch.uint8).random_(0, 256) if kc.dtype == torch.int8 else kc.normal_()
+    vc.view(torch.uint8).random_(0, 256) if vc.dtype == torch.int8 else vc.normal_()
+    pairs_h = block_copy_pairs(7, nb, args.pairs)
+    pairs = torch.from_numpy(pairs_h).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        pa.pa_block_copy(kc, vc, pairs, ks, vs, dev_status=status)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        pa.pa_block_copy(kc, vc, pairs, ks, vs, dev_status=status)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    total_ms = sum(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    nbytes = block_copy_bytes(g, args.pairs)
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    pk = peaks()
+    result = {
+        "metric": "copy-on-write block copy: HBM GB/s", "value": round(world * achieved, 2),
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8" if g.kv_dtype == "int8" else "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"pa_block_copy of {args.pairs} blocks, {w.name} pool geometry "
+                               f"(n_kv={g.n_kv}, d_h={g.d_h}, {g.kv_dtype})",
+                   "l2": "flushed between timed launches (512 MiB write); "
+                         f"{nbytes / 2e6:.0f} MB read per launch",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "bytes_per_step": nbytes,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                     "traffic": None, "kernel": "pa::block_copy_kernel",
+                     "peak_source": pk["source"], "algorithmic_bytes_per_launch": nbytes},
+        "gpu_launches": args.steps, "clocks": clocks,
+    }
+    if not args.no_e2e:
+        # the copy list comes from the host each step (pinned), as a block manager hands it over
+        hp = pairs.cpu().pin_memory()
+        dp = torch.empty_like(pairs)
+        e2e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        hst = torch.empty(1, dtype=torch.int32).pin_memory()
+        for i in range(args.steps):
+            flush.zero_()
+            e2e[i][0].record(stream)
+            dp.copy_(hp, non_blocking=True)
+            pa.pa_block_copy(kc, vc, dp, ks, vs, dev_status=status)
+            hst.copy_(status, non_blocking=True)
+            e2e[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = sum(a.elapsed_time(b) for a, b in e2e) / args.steps
+        result["e2e"] = {"value": round(world * nbytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                         "ms_per_step": round(e_ms, 5), "h2d_bytes_per_step": hp.numel() * 4,
+                         "d2h_bytes_per_step": 4}
+        result["gpu_launches"] += args.steps
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle.allocator import block_copy as oracle_copy
+        def host(t):
+            return t.cpu().numpy() if t.dtype == torch.int8 else t.view(torch.int16).cpu().numpy()
+        k_h, v_h = host(kc), host(vc)
+        ks_h = ks.cpu().numpy() if ks is not None else None
+        vs_h = vs.cpu().numpy() if vs is not None else None
+        n, spent = 0, 0.0
+        while spent < min(args.cpu_seconds, 5.0) and n < args.pairs:
+            t0 = time.perf_counter()
+            oracle_copy(k_h, v_h, pairs_h[n:n + 256].tolist(), ks_h, vs_h)
+            spent += time.perf_counter() - t0
+            n = min(args.pairs, n + 256)
+        result["cpu_baseline"] = {"value": round(block_copy_bytes(g, n) / spent / 1e9, 3),
+                                  "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                  "sample": f"{n} of {args.pairs} pairs, numpy block copy"}
+    return result
+
+
+# ----------------------------------------------------------------- allocator
+def allocator_trace(seed: int, num_seqs: int, prompt_len: int, shared: int, steps: int):
+    """A serving trace for the block manager: num_seqs prompts whose first
+    `shared` tokens are common (prefix-cache hits), four-way parallel
+    sampling of each, then `steps` decode steps of one token per branch."""
+    rng = np.random.default_rng(seed)
+    common = rng.integers(0, 32000, shared).tolist()
+    prompts = [common + rng.integers(0, 32000, prompt_len - shared).tolist()
+               for _ in range(num_seqs)]
+    tokens = rng.integers(0, 32000, (steps, 4 * num_seqs)).astype(np.int32)
+    return prompts, tokens
+
+
+def run_allocator(args):
+    """Host block manager: appends/s over a serving trace (prefill with prefix
+    hits, fork, decode steps with copy-on-write), native vs the oracle."""
+    import paged_kv_cache_94_gb300 as pa
+    from paged_kv_cache_94_gb300 import build as pa_build
+    pa_build.build()
+    B, P, S, T = 64, 1000, 512, 256
+    cap = (P + T) // 16 + 2
+    prompts, tokens = allocator_trace(5, B, P, S, T)
+    nblocks = 4 * B * cap
+
+    def native_once():
+        a = pa.BlockAllocator(nblocks)
+        tables = np.zeros((4 * B, cap), np.int32)
+        nb = np.zeros(4 * B, np.int32)
+        for i, p in enumerate(prompts):
+            t, _ = a.allocate_prompt(p)
+            for j in range(4):
+                row = a.fork(t) if j else t
+                tables[4 * i + j, :len(row)] = row
+                nb[4 * i + j] = len(row)
+        t0 = time.perf_counter()
+        for s in range(T):
+            a.append_slots(tables, nb, tokens[s])
+        return time.perf_counter() - t0
+
+    def oracle_once(steps):
+        from oracle.allocator import Allocator
+        a = Allocator(nblocks)
+        tabs = []
+        for p in prompts:
+            t, _ = a.allocate_for_prompt(p)
+            tabs += [t] + [a.fork(t) for _ in range(3)]
+        t0 = time.perf_counter()
+        for s in range(steps):
+            for i, t in enumerate(tabs):
+                a.append_slot(t, int(tokens[s, i]))
+        return time.perf_counter() - t0
+
+    for _ in range(max(1, args.warmup)):
+        native_once()
+    reps = max(1, min(args.steps, 20))
+    secs = [native_once() for _ in range(reps)]
+    per = statistics.median(secs)
+    appends = 4 * B * T
+    o_steps = 32
+    o_secs = oracle_once(o_steps)
+    return {
+        "metric": "block manager: appended tokens/s (decode step with copy-on-write)",
+        "value": round(appends / per, 1), "unit": "tokens/s", "n_gpus": 0, "steps": reps,
+        "warmup": max(1, args.warmup), "ms_per_step": round(1e3 * per / T, 5),
+        "higher_is_better": True, "scaling": "none", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": f"{B} prompts of {P} tokens sharing a {S}-token prefix, "
+                               f"4 sampled branches each, {T} decode steps of {4 * B} appends",
+                   "ms_per_step": "per decode step of the batch (one append_slots call)"},
+        "gpu_launches": 0,
+        "cpu_baseline": {"value": round(4 * B * o_steps / o_secs, 1), "unit": "tokens/s",
+                         "cores": 1, "kind": "oracle",
+                         "sample": f"{o_steps} of {T} decode steps, Python oracle allocator"},
+    }
+
+
 # ---------------------------------------------------------------- reference
 def run_reference(args):
     """The CPU oracle as the reference arm: each step is the oracle on a
@@ -412,11 +609,18 @@ def main():
             return
         print(json.dumps(run_reference(args)), flush=True)
         return
+    if args.op == "allocator":
+        if rank == 0:
+            print(json.dumps(run_allocator(args)), flush=True)
+        return
     if world > 1:
         torch.distributed.init_process_group(
             backend="nccl", device_id=torch.device(f"cuda:{local_rank}"))
     try:
-        res = run_native(args, rank, world, local_rank)
+        if args.op == "block_copy":
+            res = run_block_copy(args, rank, world, local_rank)
+        else:
+            res = run_native(args, rank, world, local_rank)
         if rank == 0:
             print(json.dumps(res), flush=True)
     finally:

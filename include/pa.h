@@ -73,7 +73,10 @@ typedef enum pa_status {
     PA_ERR_CUDA = -8,        /* a CUDA runtime or driver call failed */
     PA_ERR_BAD_CONTEXT = -9, /* device: a context length < 0 or > max_blocks_per_seq * block_size */
     PA_ERR_TIMEOUT = -10,    /* device: a pipeline wait gave up after about one second */
-    PA_ERR_ALIGNMENT = -11   /* a pointer lacks the alignment its entry point documents */
+    PA_ERR_ALIGNMENT = -11,  /* a pointer lacks the alignment its entry point documents */
+    PA_ERR_OUT_OF_BLOCKS = -12, /* allocator: not enough free blocks; nothing was changed */
+    PA_ERR_STATE = -13       /* allocator: a table names a block outside the pool or one
+                                that no holder references */
 } pa_status;
 
 /* Bits the kernels OR into *dev_status. */
@@ -251,6 +254,31 @@ pa_status pa_status_from_device(int32_t dev_word);
 
 /* Library ABI version (major * 10000 + minor * 100 + patch). */
 int32_t pa_version(void);
+
+/*
+ * pa_block_copy -- the device half of copy-on-write ([F] "Prefix Caching 与
+ * Copy-on-Write": a branch that appends to a shared, partly filled last
+ * block gets a new block holding a copy of the filled slots; [T] 考点 4:
+ * only that one 16-token block is copied).
+ *
+ * For each pair p: every kv head and all block_size slots of block
+ * pairs[p][0] are copied to block pairs[p][1], in k_cache and v_cache and,
+ * for PA_KV_INT8, in k_scale and v_scale. Copying all slots is the plainest
+ * reading: slots past the filled ones hold nothing a reader may use.
+ *
+ *   k_cache, v_cache  pool (read and written), layout above
+ *   k_scale, v_scale  fp32 scales for PA_KV_INT8, NULL for PA_KV_BF16
+ *   pairs         int32 [num_pairs][2] device array of (source, destination)
+ *                 block ids, as pa_allocator_append_slots hands them out.
+ *                 Destinations are distinct and none is a source of another
+ *                 pair (otherwise the result is undefined).
+ *   num_pairs     >= 0 (0 enqueues nothing)
+ *   dev_status    optional; a pair with a block id outside [0, num_blocks)
+ *                 is skipped and sets PA_DEV_BAD_BLOCK
+ */
+pa_status pa_block_copy(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
+                        const int32_t *pairs, int32_t num_pairs, pa_geom geom,
+                        int32_t *dev_status, void *stream);
 
 #ifdef __cplusplus
 }

@@ -17,6 +17,7 @@ import os
 import threading
 from typing import Optional
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -34,12 +35,20 @@ STATUS = {
     0: "PA_OK", -1: "PA_ERR_NULL", -2: "PA_ERR_SHAPE", -3: "PA_ERR_DTYPE",
     -4: "PA_ERR_UNSUPPORTED", -5: "PA_ERR_BAD_BLOCK", -6: "PA_ERR_BAD_SLOT",
     -7: "PA_ERR_WORKSPACE", -8: "PA_ERR_CUDA", -9: "PA_ERR_BAD_CONTEXT",
-    -10: "PA_ERR_TIMEOUT", -11: "PA_ERR_ALIGNMENT",
+    -10: "PA_ERR_TIMEOUT", -11: "PA_ERR_ALIGNMENT", -12: "PA_ERR_OUT_OF_BLOCKS",
+    -13: "PA_ERR_STATE",
 }
+PA_ERR_OUT_OF_BLOCKS = -12
+PA_ERR_STATE = -13
 EXPORTED = ["pa_cache_write", "pa_decode_workspace_size", "pa_decode_workspace_init",
             "pa_decode", "pa_decode_ex", "pa_decode_noalloc", "pa_decode_default_ctas",
-            "pa_plan_owner",
-            "pa_status_string", "pa_status_from_device", "pa_version"]
+            "pa_plan_owner", "pa_block_copy",
+            "pa_status_string", "pa_status_from_device", "pa_version",
+            # host block manager (include/pa_alloc.h)
+            "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate_prompt",
+            "pa_allocator_append_slots", "pa_allocator_fork", "pa_allocator_free",
+            "pa_allocator_num_free", "pa_allocator_block_info", "pa_allocator_free_order",
+            "pa_block_hash"]
 
 
 class PAError(RuntimeError):
@@ -98,6 +107,29 @@ def _lib():
         lib.pa_status_from_device.argtypes = [i32]
         lib.pa_version.restype = i32
         lib.pa_version.argtypes = []
+        lib.pa_block_copy.restype = ctypes.c_int
+        lib.pa_block_copy.argtypes = [P, P, P, P, P, i32, pa_geom, P, P]
+        u64 = ctypes.c_uint64
+        lib.pa_allocator_create.restype = ctypes.c_int
+        lib.pa_allocator_create.argtypes = [i64, i32, ctypes.POINTER(P)]
+        lib.pa_allocator_destroy.restype = None
+        lib.pa_allocator_destroy.argtypes = [P]
+        lib.pa_allocator_allocate_prompt.restype = ctypes.c_int
+        lib.pa_allocator_allocate_prompt.argtypes = [P, P, i32, P, i32, P, P]
+        lib.pa_allocator_append_slots.restype = ctypes.c_int
+        lib.pa_allocator_append_slots.argtypes = [P, P, i32, P, P, i32, P, P, P, P]
+        lib.pa_allocator_fork.restype = ctypes.c_int
+        lib.pa_allocator_fork.argtypes = [P, P, i32]
+        lib.pa_allocator_free.restype = ctypes.c_int
+        lib.pa_allocator_free.argtypes = [P, P, i32]
+        lib.pa_allocator_num_free.restype = i64
+        lib.pa_allocator_num_free.argtypes = [P]
+        lib.pa_allocator_block_info.restype = ctypes.c_int
+        lib.pa_allocator_block_info.argtypes = [P, i64, P, P, P, P]
+        lib.pa_allocator_free_order.restype = ctypes.c_int
+        lib.pa_allocator_free_order.argtypes = [P, P, i64, P]
+        lib.pa_block_hash.restype = u64
+        lib.pa_block_hash.argtypes = [u64, P, i32]
         _LIB = lib
         return lib
 
@@ -305,3 +337,140 @@ def allocate_pool(num_blocks: int, n_kv: int, d_h: int, kv_dtype: str = "bf16",
         vs = torch.zeros(shape[:3], dtype=torch.float32, device=device)
         return kc, vc, ks, vs
     raise ValueError(kv_dtype)
+
+
+def pa_block_copy(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs: torch.Tensor,
+                  k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                  dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Copy pool blocks pairs[p][0] -> pairs[p][1] (int32 [n, 2] on the device),
+    K, V and (INT8) scales: the device half of copy-on-write."""
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
+    _need_cuda("pairs", pairs, torch.int32)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("v_cache must have the shape of k_cache")
+    if pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be [num_pairs, 2]")
+    g = geometry(k_cache, n_h=k_cache.shape[1])
+    if g.kv_dtype == PA_KV_INT8:
+        for nm, s in (("k_scale", k_scale), ("v_scale", v_scale)):
+            if s is None:
+                raise ValueError(f"{nm} is required for an int8 pool")
+            _need_cuda(nm, s, torch.float32)
+            if tuple(s.shape) != tuple(k_cache.shape[:3]):
+                raise ValueError(f"{nm} must be [num_blocks, n_kv, block_size]")
+    if dev_status is not None:
+        _need_cuda("dev_status", dev_status, torch.int32)
+    st = _lib().pa_block_copy(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                              _ptr(pairs), pairs.shape[0], g, _ptr(dev_status),
+                              _stream_ptr(stream))
+    _check(st, "pa_block_copy")
+
+
+def _np_ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _i32(a, name: str) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    if a.ndim != 1:
+        raise ValueError(f"{name} must be one-dimensional")
+    return a
+
+
+def block_hash(parent: int, token_ids) -> int:
+    """One link of the chained block hash (pa_block_hash)."""
+    t = _i32(token_ids, "token_ids")
+    return int(_lib().pa_block_hash(ctypes.c_uint64(parent), _np_ptr(t), t.shape[0]))
+
+
+class BlockAllocator:
+    """Host block manager of libpa.so (include/pa_alloc.h): reference counts,
+    chained-hash prefix caching with an LRU evictable pool, fork, and
+    copy-on-write. Block tables are held by the caller as int32 arrays."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16):
+        h = ctypes.c_void_p()
+        _check(_lib().pa_allocator_create(num_blocks, block_size, ctypes.byref(h)),
+               "pa_allocator_create")
+        self._h = h
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _lib().pa_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def allocate_prompt(self, token_ids):
+        """-> (block table as an int32 array, cached tokens)."""
+        t = _i32(token_ids, "token_ids")
+        cap = (t.shape[0] + self.block_size - 1) // self.block_size
+        table = np.empty(max(cap, 1), np.int32)
+        n, cached = ctypes.c_int32(), ctypes.c_int32()
+        _check(_lib().pa_allocator_allocate_prompt(self._h, _np_ptr(t), t.shape[0],
+                                                   _np_ptr(table), cap, ctypes.byref(n),
+                                                   ctypes.byref(cached)),
+               "pa_allocator_allocate_prompt")
+        return table[:n.value].copy(), cached.value
+
+    def append_slots(self, tables: np.ndarray, n_blocks: np.ndarray, token_ids):
+        """Append one token to each row of `tables` (int32 [B, capacity], updated in
+        place with `n_blocks` int32 [B]) -> (slots int64 [B], cow pairs int32 [k, 2]).
+        On an error the raised PAError carries .num_done."""
+        if tables.dtype != np.int32 or not tables.flags.c_contiguous or tables.ndim != 2:
+            raise ValueError("tables must be a C-contiguous int32 [B, capacity] array")
+        if n_blocks.dtype != np.int32 or not n_blocks.flags.c_contiguous or \
+                n_blocks.shape != (tables.shape[0],):
+            raise ValueError("n_blocks must be a C-contiguous int32 [B] array")
+        t = _i32(token_ids, "token_ids")
+        B = tables.shape[0]
+        if t.shape[0] != B:
+            raise ValueError("one token id per sequence")
+        slots = np.empty(B, np.int64)
+        cow = np.empty((max(B, 1), 2), np.int32)
+        ncow, ndone = ctypes.c_int32(), ctypes.c_int32()
+        st = _lib().pa_allocator_append_slots(self._h, _np_ptr(tables), tables.shape[1],
+                                              _np_ptr(n_blocks), _np_ptr(t), B, _np_ptr(slots),
+                                              _np_ptr(cow), ctypes.byref(ncow),
+                                              ctypes.byref(ndone))
+        if st != 0:
+            e = PAError(st, "pa_allocator_append_slots")
+            e.num_done = ndone.value
+            e.cow_pairs = cow[:ncow.value].copy()
+            raise e
+        return slots, cow[:ncow.value].copy()
+
+    def fork(self, table) -> np.ndarray:
+        t = _i32(table, "table")
+        _check(_lib().pa_allocator_fork(self._h, _np_ptr(t), t.shape[0]), "pa_allocator_fork")
+        return t.copy()
+
+    def free(self, table) -> None:
+        t = _i32(table, "table")
+        _check(_lib().pa_allocator_free(self._h, _np_ptr(t), t.shape[0]), "pa_allocator_free")
+
+    def num_free(self) -> int:
+        return int(_lib().pa_allocator_num_free(self._h))
+
+    def block_info(self, block: int):
+        """-> (ref_count, num_tokens, hash or None)."""
+        r, n, hh = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        h = ctypes.c_uint64()
+        _check(_lib().pa_allocator_block_info(self._h, block, ctypes.byref(r), ctypes.byref(n),
+                                              ctypes.byref(h), ctypes.byref(hh)),
+               "pa_allocator_block_info")
+        return r.value, n.value, (h.value if hh.value else None)
+
+    def free_order(self) -> list:
+        out = np.empty(self.num_blocks, np.int32)
+        n = ctypes.c_int64()
+        _check(_lib().pa_allocator_free_order(self._h, _np_ptr(out), self.num_blocks,
+                                              ctypes.byref(n)), "pa_allocator_free_order")
+        return out[:n.value].tolist()

@@ -30,6 +30,8 @@ SOURCES = [
     "pa_decode_int8_d128.cu",
     "pa_decode_int8_d64.cu",
     "pa_decode_noalloc.cu",
+    "pa_block_copy.cu",
+    "pa_alloc.cpp",
 ]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -47,7 +49,8 @@ def _stamp() -> str:
     """Machine + hash of every source the library is built from."""
     h = hashlib.sha256(platform.machine().encode())
     files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC))
-    files += [os.path.join(INCLUDE, "pa.h"), os.path.abspath(__file__)]
+    files += sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE))
+    files.append(os.path.abspath(__file__))
     for f in files:
         h.update(open(f, "rb").read())
     return h.hexdigest()

@@ -349,6 +349,33 @@ pa_status pa_cache_write(const void *k, const void *v, const int64_t *slot_mappi
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status pa_block_copy(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
+                        const int32_t *pairs, int32_t num_pairs, pa_geom geom,
+                        int32_t *dev_status, void *stream)
+{
+    pa_status st = check_geom(geom);
+    if (st != PA_OK)
+        return st;
+    if (num_pairs < 0)
+        return PA_ERR_SHAPE;
+    if (num_pairs == 0)
+        return PA_OK;
+    if (!k_cache || !v_cache || !pairs)
+        return PA_ERR_NULL;
+    const bool i8 = geom.kv_dtype == PA_KV_INT8;
+    if (i8 && (!k_scale || !v_scale))
+        return PA_ERR_NULL;
+    if (!i8 && (k_scale || v_scale))
+        return PA_ERR_SHAPE;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(pairs, 4) ||
+        (i8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16))))
+        return PA_ERR_ALIGNMENT;
+    const cudaError_t e = pa::launch_block_copy(k_cache, v_cache, k_scale, v_scale, pairs,
+                                                num_pairs, geom.num_blocks, geom.n_kv, geom.d_h,
+                                                i8, dev_status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 size_t pa_decode_workspace_size(pa_geom geom, int32_t num_seqs, int32_t num_ctas)
 {
     if (check_geom(geom) != PA_OK || num_seqs < 0 || num_seqs > kMaxSeqs || num_ctas < 0)
@@ -427,6 +454,8 @@ const char *pa_status_string(pa_status s)
     case PA_ERR_BAD_CONTEXT: return "PA_ERR_BAD_CONTEXT: context length outside the block table";
     case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a pipeline wait gave up";
     case PA_ERR_ALIGNMENT: return "PA_ERR_ALIGNMENT: a pointer is not aligned as required";
+    case PA_ERR_OUT_OF_BLOCKS: return "PA_ERR_OUT_OF_BLOCKS: not enough free KV cache blocks";
+    case PA_ERR_STATE: return "PA_ERR_STATE: a block table names a block that is not held";
     }
     return "unknown pa_status";
 }

@@ -1,6 +1,6 @@
 """Host-side checks of the C ABI (no GPU needed, no compute calls).
 
-The library must load and export every entry point include/pa.h declares;
+The library must load and export every entry point include/*.h declares;
 argument checks that return before any CUDA call are exercised; the work
 split (pa_plan_owner) is compared with a brute-force assignment.
 """
@@ -23,9 +23,13 @@ def lib():
 
 
 def _declared():
-    text = open(os.path.join(ROOT, "include", "pa.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, f)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_binding_names():
@@ -132,3 +136,18 @@ def test_binding_refuses_cpu_tensors():
     cl = torch.ones(1, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA"):
         pa.pa_decode(q, kc, kc, bt, cl, 0.125)
+
+
+def test_block_copy_argument_checks(lib):
+    fake = ctypes.c_void_p(256)
+    odd = ctypes.c_void_p(258)
+    g = _geom()
+    assert lib.pa_block_copy(fake, fake, None, None, fake, 0, g, None, None) == 0  # nothing to do
+    assert lib.pa_block_copy(fake, fake, None, None, fake, -1, g, None, None) == -2
+    assert lib.pa_block_copy(None, fake, None, None, fake, 3, g, None, None) == -1
+    assert lib.pa_block_copy(fake, fake, None, None, None, 3, g, None, None) == -1
+    assert lib.pa_block_copy(fake, fake, fake, None, fake, 3, g, None, None) == -2  # bf16 + scales
+    gi = _geom(kv_dtype=1)
+    assert lib.pa_block_copy(fake, fake, None, None, fake, 3, gi, None, None) == -1
+    assert lib.pa_block_copy(odd, fake, None, None, fake, 3, g, None, None) == -11
+    assert lib.pa_block_copy(fake, fake, None, None, fake, 3, _geom(d_h=96), None, None) == -4

@@ -314,3 +314,28 @@ def named_workload(name: str) -> Workload:
             name, Geometry(n_h=32, n_kv=8, d_h=128), [131072, 98304, 65536, 32768], seed,
             description="long context: B=4, ctx {131072,98304,65536,32768}, n_h=32, n_kv=8, d_h=128")
     raise KeyError(name)
+
+
+# ------------------------------------------------------------ free-form inputs
+def random_rows(seed: int, n: int, n_kv: int, d_h: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """Seeded K and V rows, bf16 [n, n_kv, d_h] on the CPU (standard normal)."""
+    gen = torch.Generator()
+    gen.manual_seed(seed)
+    k = torch.randn((n, n_kv, d_h), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn((n, n_kv, d_h), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    return k, v
+
+
+def random_queries(seed: int, B: int, n_h: int, d_h: int) -> torch.Tensor:
+    """Seeded query rows, bf16 [B, n_h, d_h] on the CPU (standard normal)."""
+    gen = torch.Generator()
+    gen.manual_seed(seed)
+    return torch.randn((B, n_h, d_h), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+
+
+def block_copy_pairs(seed: int, num_blocks: int, n: int) -> np.ndarray:
+    """n (source, destination) block pairs: distinct destinations, none of
+    them a source, drawn from a seeded permutation of the pool. int32 [n, 2]."""
+    assert 2 * n <= num_blocks
+    perm = np.random.default_rng(seed).permutation(num_blocks).astype(np.int32)
+    return np.ascontiguousarray(np.stack([perm[:n], perm[n:2 * n]], axis=1))
