@@ -68,6 +68,9 @@ def _load():
         lib.oracle_decode.restype = ctypes.c_int
         lib.oracle_decode.argtypes = [P, P, P, P, P, i32, P, i32, P, i32, i32, i32, i32, i32, i64,
                                       dbl, P]
+        lib.oracle_decode_window.restype = ctypes.c_int
+        lib.oracle_decode_window.argtypes = [P, P, P, P, P, i32, P, i32, P, i32, i32, i32, i32,
+                                             i32, i64, dbl, i32, i32, P, P, P]
         _lib = lib
     return _lib
 
@@ -154,6 +157,36 @@ def decode(q_bits: np.ndarray, pool: Pool, block_tables: np.ndarray, context_len
                            _ptr(pool.v_scale), 1 if pool.kv_dtype == "int8" else 0, _ptr(bt),
                            bt.shape[1], _ptr(ctx), B, n_h, pool.n_kv, pool.d_h, pool.block_size,
                            pool.num_blocks, float(scale), _ptr(out))
+    return out, st
+
+
+def decode_window(q_bits: np.ndarray, pool: Pool, block_tables: np.ndarray,
+                  context_lens: np.ndarray, n_h: int, scale: float, window: int = 0,
+                  n_sink: int = 0, sink_k_bits: Optional[np.ndarray] = None,
+                  sink_v_bits: Optional[np.ndarray] = None) -> tuple[np.ndarray, int]:
+    """Decode attention over the last `window` tokens (0 = all), with the
+    first n_sink positions read from bf16 sink rows [B, n_kv, n_sink, d_h]
+    (INT8 pools only). float64 [B, n_h, d_h] and status."""
+    lib = _load()
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B = ctx.shape[0]
+    assert q_bits.shape == (B, n_h, pool.d_h)
+    if n_sink:
+        assert pool.kv_dtype == "int8"
+        sink_k_bits = np.ascontiguousarray(sink_k_bits, dtype=np.uint16)
+        sink_v_bits = np.ascontiguousarray(sink_v_bits, dtype=np.uint16)
+        assert sink_k_bits.shape == (B, pool.n_kv, n_sink, pool.d_h)
+        assert sink_v_bits.shape == sink_k_bits.shape
+    else:
+        sink_k_bits = sink_v_bits = None
+    out = np.zeros((B, n_h, pool.d_h), dtype=np.float64)
+    st = lib.oracle_decode_window(_ptr(q_bits), _ptr(pool.k), _ptr(pool.v), _ptr(pool.k_scale),
+                                  _ptr(pool.v_scale), 1 if pool.kv_dtype == "int8" else 0,
+                                  _ptr(bt), bt.shape[1], _ptr(ctx), B, n_h, pool.n_kv, pool.d_h,
+                                  pool.block_size, pool.num_blocks, float(scale), int(window),
+                                  int(n_sink), _ptr(sink_k_bits), _ptr(sink_v_bits), _ptr(out))
     return out, st
 
 

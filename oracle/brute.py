@@ -79,3 +79,19 @@ def paged_decode(q_bits, k_cache_bits, v_cache_bits, block_tables, context_lens,
                                              int(context_lens[b]), scale))
         out.append(per_head)
     return out
+
+
+def attend_rows(q_row, k_rows, v_rows, scale):
+    """Softmax attention of one query over an explicit list of K/V rows
+    (lists of floats): the plain definition, for the window and sink pins."""
+    if not k_rows:
+        return [0.0] * len(q_row)
+    scores = [sum(a * b for a, b in zip(q_row, k)) * scale for k in k_rows]
+    m = max(scores)
+    e = [math.exp(s - m) for s in scores]
+    z = sum(e)
+    out = [0.0] * len(q_row)
+    for w, v in zip(e, v_rows):
+        for d in range(len(out)):
+            out[d] += (w / z) * v[d]
+    return out

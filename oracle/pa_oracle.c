@@ -259,3 +259,111 @@ int oracle_decode(const uint16_t *q, const void *k_cache, const void *v_cache, c
     free(scores);
     return status;
 }
+
+/* ------------------------------------------------------------------------
+ * Decode attention with a sliding window and INT8 attention-sink rows.
+ *
+ * Sliding window ([G] §5.1 `SlidingWindowKVCache`: only the latest w tokens
+ * are kept and attended): with window > 0, sequence b attends positions
+ * j in [max(0, ctx_b - window), ctx_b); window == 0 attends all ctx_b.
+ * Block-table entries of logical blocks wholly before the window are never
+ * read (a sliding-window cache may have released them).
+ *
+ * Attention sink ([G] §4.3: the first k tokens, typically 4, stay
+ * unquantised in an INT8 cache): for an INT8 pool and n_sink > 0, an attended
+ * position j < n_sink takes its K and V rows from the bf16 sink rows
+ * sink_k/sink_v[b][kv][j][:] ([B][n_kv][n_sink][d_h] bit patterns) instead of
+ * dequantising the pool. Every other position reads the pool as in
+ * oracle_decode. n_sink must be 0 for a bf16 pool.
+ *
+ * Validation: a context length outside [0, max_blocks*block_size] and a
+ * block id outside the pool among the blocks the window reads (positions
+ * >= max(window start, n_sink)) are reported; that sequence's output is 0.
+ * The softmax and the two passes are those of oracle_decode.
+ * ---------------------------------------------------------------------- */
+int oracle_decode_window(const uint16_t *q, const void *k_cache, const void *v_cache,
+                         const float *k_scale, const float *v_scale, int kv_is_int8,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, int B, int n_h, int n_kv, int d_h,
+                         int block_size, int64_t num_blocks, double scale, int window, int n_sink,
+                         const uint16_t *sink_k, const uint16_t *sink_v, double *out)
+{
+    int status = 0;
+    int g = n_h / n_kv;
+    double *scores = NULL;
+    int64_t cap = 0;
+    for (int b = 0; b < B; ++b) {
+        int64_t ctx = context_lens[b];
+        int bad = 0;
+        if (ctx < 0 || ctx > (int64_t)max_blocks_per_seq * block_size) {
+            status |= ORC_BAD_CTX;
+            bad = 1;
+        }
+        int64_t start = (window > 0 && ctx > window) ? ctx - window : 0;
+        int64_t pool_from = start > n_sink ? start : n_sink; /* first position read from the pool */
+        for (int64_t j = pool_from; !bad && j < ctx; ++j) {
+            int32_t blk = block_tables[(int64_t)b * max_blocks_per_seq + j / block_size];
+            if (blk < 0 || blk >= num_blocks) {
+                status |= ORC_BAD_BLOCK;
+                bad = 1;
+            }
+        }
+        if (bad || ctx == 0) {
+            for (int h = 0; h < n_h; ++h)
+                for (int d = 0; d < d_h; ++d)
+                    out[((int64_t)b * n_h + h) * d_h + d] = 0.0;
+            continue;
+        }
+        int64_t n = ctx - start;
+        if (n > cap) {
+            free(scores);
+            cap = n;
+            scores = (double *)malloc(sizeof(double) * (size_t)cap);
+        }
+        for (int h = 0; h < n_h; ++h) {
+            int kvh = h / g;
+            const uint16_t *qh = q + ((int64_t)b * n_h + h) * d_h;
+            double m = -INFINITY;
+            for (int64_t j = start; j < ctx; ++j) {
+                double dot = 0.0;
+                if (j < n_sink) {
+                    const uint16_t *kr = sink_k + (((int64_t)b * n_kv + kvh) * n_sink + j) * d_h;
+                    for (int d = 0; d < d_h; ++d)
+                        dot += (double)bf16_bits_to_float(qh[d]) * (double)bf16_bits_to_float(kr[d]);
+                } else {
+                    int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + j / block_size];
+                    int64_t row = (blk * n_kv + kvh) * block_size + j % block_size;
+                    for (int d = 0; d < d_h; ++d)
+                        dot += (double)bf16_bits_to_float(qh[d]) *
+                               cached_elem(k_cache, k_scale, kv_is_int8, row, d, d_h);
+                }
+                scores[j - start] = dot * scale;
+                if (scores[j - start] > m)
+                    m = scores[j - start];
+            }
+            double denom = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                scores[j] = exp(scores[j] - m);
+                denom += scores[j];
+            }
+            double *o = out + ((int64_t)b * n_h + h) * d_h;
+            for (int d = 0; d < d_h; ++d)
+                o[d] = 0.0;
+            for (int64_t j = start; j < ctx; ++j) {
+                double w = scores[j - start] / denom;
+                if (j < n_sink) {
+                    const uint16_t *vr = sink_v + (((int64_t)b * n_kv + kvh) * n_sink + j) * d_h;
+                    for (int d = 0; d < d_h; ++d)
+                        o[d] += w * (double)bf16_bits_to_float(vr[d]);
+                } else {
+                    int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + j / block_size];
+                    int64_t row = (blk * n_kv + kvh) * block_size + j % block_size;
+                    for (int d = 0; d < d_h; ++d)
+                        o[d] += w * cached_elem(v_cache, v_scale, kv_is_int8, row, d, d_h);
+                }
+            }
+        }
+    }
+    free(scores);
+    return status;
+}
