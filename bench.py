@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from workloads import CONFIG_NAMES, named_workload  # noqa: E402
+from workloads import CONFIG_NAMES, EXTRA_NAMES, named_workload  # noqa: E402
 
 METRIC = "paged GQA decode attention: KV-read HBM GB/s, % of peak, seqs/s"
 DEFAULT_WORKLOAD = "llama3_8b"
@@ -49,7 +49,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=CONFIG_NAMES, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", choices=CONFIG_NAMES + EXTRA_NAMES, default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -73,26 +73,33 @@ def decode_bytes(w, unique_blocks: bool = True) -> dict:
     Per sequence: ctx*2*n_kv*d_h*b_kv of K and V (+ ctx*2*n_kv*4 of fp32
     scales for INT8), 4*ceil(ctx/16) of block table, 4 of context length, and
     2*2*n_h*d_h of q and out. Shared prefix blocks count once (unique bytes).
+    Under a sliding window only the window's tokens and blocks count.
     """
     g = w.geom
     bkv = kv_bytes_per_elem(w)
     per_token = 2 * g.n_kv * g.d_h * bkv + (2 * g.n_kv * 4 if g.kv_dtype == "int8" else 0)
-    tok_logical = int(w.context_lens.sum())
+
+    def span(b):  # attended positions [lo, ctx) and the blocks they touch
+        ctx = int(w.context_lens[b])
+        lo = max(0, ctx - w.window) if w.window else 0
+        return lo, ctx, range(lo // 16, -(-ctx // 16))
+
+    tok_logical = sum(span(b)[1] - span(b)[0] for b in range(w.B))
     if unique_blocks:
-        # tokens in unique physical blocks (shared prefixes once)
+        # attended tokens in unique physical blocks (shared prefixes once)
         seen = set()
         tok = 0
         for b in range(w.B):
-            ctx = int(w.context_lens[b])
-            for i in range(w.num_seq_blocks(b)):
+            lo, ctx, blocks_b = span(b)
+            for i in blocks_b:
                 blk = int(w.block_tables[b, i])
                 if blk in seen:
                     continue
                 seen.add(blk)
-                tok += min(16, ctx - 16 * i)
+                tok += min(16 * i + 16, ctx) - max(16 * i, lo)
     else:
         tok = tok_logical
-    blocks = sum(w.num_seq_blocks(b) for b in range(w.B))
+    blocks = sum(len(span(b)[2]) for b in range(w.B))
     other = 4 * blocks + 4 * w.B + 2 * 2 * w.B * g.n_h * g.d_h
     return {"bytes": tok * per_token + other, "logical_bytes": tok_logical * per_token + other,
             "flops": 4 * g.n_h * g.d_h * tok_logical}
@@ -216,13 +223,20 @@ def oracle_sample(w, gen_device, seconds: float):
         pool.write(oracle.bf16_bits(k), oracle.bf16_bits(v), np.arange(ctx))
         table = np.arange(nblk, dtype=np.int32)[None]
         t0 = time.perf_counter()
-        oracle.decode(q_all[b:b + 1], pool, table, np.array([ctx], np.int32), g.n_h, w.scale)
+        if w.window:
+            oracle.decode_window(q_all[b:b + 1], pool, table, np.array([ctx], np.int32), g.n_h,
+                                 w.scale, window=w.window)
+        else:
+            oracle.decode(q_all[b:b + 1], pool, table, np.array([ctx], np.int32), g.n_h, w.scale)
         spent += time.perf_counter() - t0
-        done_bytes += ctx * per_token + 4 * nblk + 4 + 4 * g.n_h * g.d_h
+        lo = max(0, ctx - w.window) if w.window else 0
+        done_bytes += (ctx - lo) * per_token + 4 * (nblk - lo // 16) + 4 + 4 * g.n_h * g.d_h
         seqs.append(b)
         if spent >= seconds:
             break
-    desc = (f"{len(seqs)} of {w.B} sequences ({int(sum(w.context_lens[s] for s in seqs))} tokens), "
+    attended = sum(min(int(w.context_lens[s]), w.window) if w.window else int(w.context_lens[s])
+                   for s in seqs)
+    desc = (f"{len(seqs)} of {w.B} sequences ({attended} attended tokens), "
             f"single-threaded C fp64 oracle")
     return done_bytes, spent, desc
 
@@ -256,7 +270,7 @@ def run_native(args, rank, world, local_rank):
     def step():
         pa.pa_cache_write(kn, vn, slots_new, kc, vc, ks, vs, dev_status=status)
         pa.pa_decode(q, kc, vc, bt, cl, w.scale, out=out, k_scale=ks, v_scale=vs, workspace=ws,
-                     dev_status=status, num_ctas=args.num_ctas)
+                     dev_status=status, num_ctas=args.num_ctas, window=w.window)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -277,7 +291,7 @@ def run_native(args, rank, world, local_rank):
         pa.pa_cache_write(kn, vn, slots_new, kc, vc, ks, vs, dev_status=status)
         ev[i][1].record(stream)
         pa.pa_decode(q, kc, vc, bt, cl, w.scale, out=out, k_scale=ks, v_scale=vs, workspace=ws,
-                     dev_status=status, num_ctas=args.num_ctas)
+                     dev_status=status, num_ctas=args.num_ctas, window=w.window)
         ev[i][2].record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
@@ -344,7 +358,7 @@ def run_native(args, rank, world, local_rank):
                 d.copy_(h, non_blocking=True)
             pa.pa_cache_write(dk, dv, ds, kc, vc, ks, vs, dev_status=status)
             pa.pa_decode(dq, kc, vc, dbt, dcl, w.scale, out=out, k_scale=ks, v_scale=vs,
-                         workspace=ws, dev_status=status)
+                         workspace=ws, dev_status=status, window=w.window)
             hout.copy_(out, non_blocking=True)
 
         for _ in range(args.warmup):

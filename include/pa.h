@@ -209,6 +209,63 @@ pa_status pa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
                        pa_geom geom, int32_t *dev_status, void *stream, int32_t num_ctas);
 
 /*
+ * Options of pa_decode_opt (zero-initialise, then set what is needed).
+ *
+ *   window    > 0: sliding-window attention ([G] §5.1 `SlidingWindowKVCache`:
+ *             only the latest w tokens are kept and attended). Sequence b
+ *             attends positions [max(0, ctx_b - window), ctx_b). Block-table
+ *             entries of logical blocks wholly before that start are never
+ *             read (a windowed cache may have released them). 0 = attend all.
+ *   n_sink    INT8 pools only, 0..16: attention-sink rows ([G] §4.3: the first
+ *             k tokens, typically 4, stay unquantised in an INT8 cache). An
+ *             attended position j < n_sink takes its K and V from the bf16
+ *             rows sink_k/sink_v[b][kv head][j][:] instead of the pool; the
+ *             pool's codes for those positions are not read. 0 = none.
+ *   sink_k, sink_v  bf16 [num_seqs][n_kv][n_sink][d_h] (device, read;
+ *             2-byte aligned), required when n_sink > 0, else NULL.
+ *             pa_sink_write fills them.
+ *   num_ctas  > 0: the CTA count as in pa_decode_ex; 0: the default.
+ */
+typedef struct pa_decode_opts {
+    int32_t window;
+    int32_t n_sink;
+    const void *sink_k;
+    const void *sink_v;
+    int32_t num_ctas;
+    int32_t reserved; /* must be 0 */
+} pa_decode_opts;
+
+/* pa_decode with options (opts may be NULL: plain pa_decode). Extra
+ * errors: PA_ERR_SHAPE for window < 0, n_sink outside 0..16, n_sink > 0 on
+ * a bf16 pool, num_ctas < 0 or reserved != 0; PA_ERR_NULL for missing sink
+ * rows; PA_ERR_ALIGNMENT for odd sink pointers. The workspace is sized as
+ * for pa_decode_ex with the same num_ctas (0: pa_decode's size). */
+pa_status pa_decode_opt(const void *q, const void *k_cache, const void *v_cache,
+                        const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                        int32_t max_blocks_per_seq, const int32_t *context_lens,
+                        int32_t num_seqs, float scale, void *out, void *workspace,
+                        size_t workspace_bytes, pa_geom geom, const pa_decode_opts *opts,
+                        int32_t *dev_status, void *stream);
+
+/*
+ * pa_sink_write -- store bf16 attention-sink rows of new tokens.
+ *
+ * For each row t with 0 <= positions[t] < n_sink and 0 <= seq_rows[t] <
+ * num_seqs: sink_k[seq_rows[t]][h][positions[t]][:] = k[t][h][:] for every
+ * kv head h (same for v). Other rows are skipped. Call it beside
+ * pa_cache_write for the same tokens; the INT8 pool keeps its own codes.
+ *
+ *   k, v        bf16 [num_tokens][n_kv][d_h] (16-byte aligned)
+ *   seq_rows    int32 [num_tokens]: the batch row of each token's sequence
+ *   positions   int32 [num_tokens]: each token's position in its sequence
+ *   sink_k, sink_v  bf16 [num_seqs][n_kv][n_sink][d_h] (written, 16-byte aligned)
+ *   n_sink      1..16
+ */
+pa_status pa_sink_write(const void *k, const void *v, const int32_t *seq_rows,
+                        const int32_t *positions, int64_t num_tokens, void *sink_k, void *sink_v,
+                        int32_t n_sink, int32_t num_seqs, pa_geom geom, void *stream);
+
+/*
  * pa_decode_noalloc -- pa_decode without a caller workspace, for callers that
  * cannot allocate device memory (for example a plugin whose host framework
  * owns all device memory and forbids allocating inside its execute callback).

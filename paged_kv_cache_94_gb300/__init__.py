@@ -42,7 +42,7 @@ PA_ERR_OUT_OF_BLOCKS = -12
 PA_ERR_STATE = -13
 EXPORTED = ["pa_cache_write", "pa_decode_workspace_size", "pa_decode_workspace_init",
             "pa_decode", "pa_decode_ex", "pa_decode_noalloc", "pa_decode_default_ctas",
-            "pa_plan_owner", "pa_block_copy",
+            "pa_plan_owner", "pa_block_copy", "pa_decode_opt", "pa_sink_write",
             "pa_status_string", "pa_status_from_device", "pa_version",
             # host block manager (include/pa_alloc.h)
             "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate_prompt",
@@ -63,6 +63,12 @@ class pa_geom(ctypes.Structure):
                 ("n_kv", ctypes.c_int32), ("d_h", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
+
+
+class pa_decode_opts(ctypes.Structure):
+    _fields_ = [("window", ctypes.c_int32), ("n_sink", ctypes.c_int32),
+                ("sink_k", ctypes.c_void_p), ("sink_v", ctypes.c_void_p),
+                ("num_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _LIB = None
@@ -107,6 +113,10 @@ def _lib():
         lib.pa_status_from_device.argtypes = [i32]
         lib.pa_version.restype = i32
         lib.pa_version.argtypes = []
+        lib.pa_decode_opt.restype = ctypes.c_int
+        lib.pa_decode_opt.argtypes = dec[:14] + [P] + dec[14:]
+        lib.pa_sink_write.restype = ctypes.c_int
+        lib.pa_sink_write.argtypes = [P, P, P, P, i64, P, P, i32, i32, pa_geom, P]
         lib.pa_block_copy.restype = ctypes.c_int
         lib.pa_block_copy.argtypes = [P, P, P, P, P, i32, pa_geom, P, P]
         u64 = ctypes.c_uint64
@@ -254,12 +264,16 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
               block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
               out: Optional[torch.Tensor] = None, k_scale: Optional[torch.Tensor] = None,
               v_scale: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-              dev_status: Optional[torch.Tensor] = None, stream=None, num_ctas: int = 0
-              ) -> torch.Tensor:
+              dev_status: Optional[torch.Tensor] = None, stream=None, num_ctas: int = 0,
+              window: int = 0, sink_k: Optional[torch.Tensor] = None,
+              sink_v: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Decode attention: q [B, n_h, d_h] bf16 over the paged pool -> out [B, n_h, d_h] bf16.
 
     block_tables [B, max_blocks] int32 and context_lens [B] int32 live on the device.
     num_ctas > 0 forces the number of CTAs the work is split over (pa_decode_ex).
+    window > 0 attends the last `window` tokens of each sequence; sink_k/sink_v
+    (bf16 [B, n_kv, n_sink, d_h], INT8 pools) hold the unquantised rows of the
+    first n_sink positions (pa_decode_opt).
     """
     _need_cuda("q", q, torch.bfloat16)
     _need_cuda("k_cache", k_cache)
@@ -295,12 +309,48 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
             _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, float(scale),
             _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), g,
             _ptr(dev_status), _stream_ptr(stream)]
-    if num_ctas > 0:
+    if window or sink_k is not None or sink_v is not None:
+        n_sink = 0
+        if sink_k is not None or sink_v is not None:
+            _need_cuda("sink_k", sink_k, torch.bfloat16)
+            _need_cuda("sink_v", sink_v, torch.bfloat16)
+            n_sink = sink_k.shape[2]
+            if sink_k.shape != (B, g.n_kv, n_sink, g.d_h) or sink_v.shape != sink_k.shape:
+                raise ValueError("sink_k, sink_v must be [num_seqs, n_kv, n_sink, d_h]")
+        opts = pa_decode_opts(window=int(window), n_sink=n_sink, sink_k=_ptr(sink_k),
+                              sink_v=_ptr(sink_v), num_ctas=int(num_ctas), reserved=0)
+        st = lib.pa_decode_opt(*args[:14], ctypes.byref(opts), *args[14:])
+    elif num_ctas > 0:
         st = lib.pa_decode_ex(*args, int(num_ctas))
     else:
         st = lib.pa_decode(*args)
     _check(st, "pa_decode")
     return out
+
+
+def pa_sink_write(k: torch.Tensor, v: torch.Tensor, seq_rows: torch.Tensor,
+                  positions: torch.Tensor, sink_k: torch.Tensor, sink_v: torch.Tensor,
+                  stream=None) -> None:
+    """Store the bf16 rows of tokens at positions < n_sink into the sink rows
+    sink_k/sink_v [num_seqs, n_kv, n_sink, d_h] (seq_rows, positions: int32 [T])."""
+    _need_cuda("k", k, torch.bfloat16)
+    _need_cuda("v", v, torch.bfloat16)
+    _need_cuda("seq_rows", seq_rows, torch.int32)
+    _need_cuda("positions", positions, torch.int32)
+    _need_cuda("sink_k", sink_k, torch.bfloat16)
+    _need_cuda("sink_v", sink_v, torch.bfloat16)
+    if sink_k.dim() != 4 or sink_v.shape != sink_k.shape:
+        raise ValueError("sink_k, sink_v must be [num_seqs, n_kv, n_sink, d_h]")
+    B, n_kv, n_sink, d = sink_k.shape
+    T = k.shape[0]
+    if k.shape != (T, n_kv, d) or v.shape != k.shape or seq_rows.shape != (T,) or \
+            positions.shape != (T,):
+        raise ValueError("k, v [T, n_kv, d_h], seq_rows and positions [T] must agree")
+    g = pa_geom(num_blocks=1, n_h=n_kv, n_kv=n_kv, d_h=d, block_size=16, kv_dtype=PA_KV_INT8,
+                reserved=0)
+    _check(_lib().pa_sink_write(_ptr(k), _ptr(v), _ptr(seq_rows), _ptr(positions), T,
+                                _ptr(sink_k), _ptr(sink_v), n_sink, B, g, _stream_ptr(stream)),
+           "pa_sink_write")
 
 
 def pa_decode_default_ctas(k_cache: torch.Tensor, n_h: int, num_seqs: int) -> int:

@@ -236,11 +236,23 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
                       const float *v_scale, const int32_t *block_tables, int32_t max_blocks,
                       const int32_t *context_lens, int32_t num_seqs, float scale, void *out,
                       void *workspace, size_t workspace_bytes, pa_geom g, int32_t *dev_status,
-                      void *stream, int32_t num_ctas)
+                      void *stream, int32_t num_ctas, const pa_decode_opts *opts = nullptr)
 {
     pa_status st = check_geom(g);
     if (st != PA_OK)
         return st;
+    const pa_decode_opts none = {0, 0, nullptr, nullptr, 0, 0};
+    const pa_decode_opts &o = opts ? *opts : none;
+    if (o.window < 0 || o.n_sink < 0 || o.n_sink > 16 || o.reserved != 0)
+        return PA_ERR_SHAPE;
+    if (o.n_sink > 0) {
+        if (g.kv_dtype != PA_KV_INT8)
+            return PA_ERR_SHAPE;
+        if (!o.sink_k || !o.sink_v)
+            return PA_ERR_NULL;
+        if (!aligned(o.sink_k, 2) || !aligned(o.sink_v, 2))
+            return PA_ERR_ALIGNMENT;
+    }
     if (num_seqs < 0 || num_seqs > kMaxSeqs || max_blocks <= 0 || num_ctas < 0)
         return PA_ERR_SHAPE;
     if ((int64_t)num_seqs * max_blocks >= (int64_t(1) << 31))
@@ -292,6 +304,10 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     p.max_blocks = max_blocks;
     p.num_ctas = grid;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.window = o.window;
+    p.n_sink = o.n_sink;
+    p.sink_k = static_cast<const __nv_bfloat16 *>(o.n_sink > 0 ? o.sink_k : nullptr);
+    p.sink_v = static_cast<const __nv_bfloat16 *>(o.n_sink > 0 ? o.sink_v : nullptr);
     const cudaError_t e =
         kd->launch(tk, tv, p, grid, smem, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -418,6 +434,42 @@ pa_status pa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
     return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
                        context_lens, num_seqs, scale, out, workspace, workspace_bytes, geom,
                        dev_status, stream, num_ctas);
+}
+
+pa_status pa_decode_opt(const void *q, const void *k_cache, const void *v_cache,
+                        const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                        int32_t max_blocks_per_seq, const int32_t *context_lens,
+                        int32_t num_seqs, float scale, void *out, void *workspace,
+                        size_t workspace_bytes, pa_geom geom, const pa_decode_opts *opts,
+                        int32_t *dev_status, void *stream)
+{
+    return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, scale, out, workspace, workspace_bytes, geom,
+                       dev_status, stream, opts ? opts->num_ctas : 0, opts);
+}
+
+pa_status pa_sink_write(const void *k, const void *v, const int32_t *seq_rows,
+                        const int32_t *positions, int64_t num_tokens, void *sink_k, void *sink_v,
+                        int32_t n_sink, int32_t num_seqs, pa_geom geom, void *stream)
+{
+    pa_status st = check_geom(geom);
+    if (st != PA_OK)
+        return st;
+    if (num_tokens < 0 || n_sink < 1 || n_sink > 16 || num_seqs < 1)
+        return PA_ERR_SHAPE;
+    if (num_tokens == 0)
+        return PA_OK;
+    if (num_tokens * geom.n_kv > (int64_t(1) << 33))
+        return PA_ERR_UNSUPPORTED;
+    if (!k || !v || !seq_rows || !positions || !sink_k || !sink_v)
+        return PA_ERR_NULL;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(sink_k, 16) || !aligned(sink_v, 16) ||
+        !aligned(seq_rows, 4) || !aligned(positions, 4))
+        return PA_ERR_ALIGNMENT;
+    const cudaError_t e = pa::launch_sink_write(
+        k, v, seq_rows, positions, num_tokens, geom.n_kv, geom.d_h, n_sink, num_seqs, sink_k,
+        sink_v, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int32_t pa_decode_default_ctas(pa_geom geom, int32_t num_seqs)

@@ -111,7 +111,47 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Attention-sink rows: row (t, h) with 0 <= positions[t] < n_sink and a valid
+// batch row goes to sink[seq_rows[t]][h][positions[t]][:] unchanged (bf16).
+// One warp per (token, kv head) row, 16-byte copies.
+__global__ void __launch_bounds__(256)
+    sink_write_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                      const int32_t *__restrict__ seq_rows, const int32_t *__restrict__ positions,
+                      int64_t rows, int n_kv, int chunks, int n_sink, int num_seqs, uint4 *sink_k,
+                      uint4 *sink_v)
+{
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= rows)
+        return;
+    const int lane = threadIdx.x & 31;
+    const int64_t t = row / n_kv;
+    const int h = (int)(row - t * n_kv);
+    const int32_t pos = positions[t], b = seq_rows[t];
+    if (pos < 0 || pos >= n_sink || b < 0 || b >= num_seqs)
+        return;
+    const int64_t dst = (((int64_t)b * n_kv + h) * n_sink + pos) * chunks;
+    for (int c = lane; c < chunks; c += 32) {
+        sink_k[dst + c] = k[row * chunks + c];
+        sink_v[dst + c] = v[row * chunks + c];
+    }
+}
+
 } // namespace
+
+cudaError_t launch_sink_write(const void *k, const void *v, const int32_t *seq_rows,
+                              const int32_t *positions, int64_t T, int n_kv, int d_h, int n_sink,
+                              int num_seqs, void *sink_k, void *sink_v, cudaStream_t stream)
+{
+    const int64_t rows = T * n_kv;
+    const int64_t blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffff)
+        return cudaErrorInvalidValue;
+    sink_write_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), seq_rows, positions, rows,
+        n_kv, d_h * 2 / 16, n_sink, num_seqs, static_cast<uint4 *>(sink_k),
+        static_cast<uint4 *>(sink_v));
+    return cudaGetLastError();
+}
 
 cudaError_t launch_cache_write(const void *k, const void *v, const int64_t *slots, int64_t T,
                                int n_kv, int d_h, bool int8, int64_t num_slots, void *k_cache,

@@ -57,7 +57,17 @@ struct DecodeParams {
     int32_t max_blocks;
     int32_t num_ctas;
     float scale_log2;            // softmax scale * log2(e)
+    int32_t window;              // > 0: attend the last `window` tokens only
+    int32_t n_sink;              // INT8: positions < n_sink read the bf16 sink rows
+    const __nv_bfloat16 *sink_k; // [B][n_kv][n_sink][D]
+    const __nv_bfloat16 *sink_v;
 };
+
+// First position a sequence attends: max(0, ctx - window) under a window.
+__device__ __forceinline__ int32_t window_start(const DecodeParams &p, int32_t ctx)
+{
+    return (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
+}
 
 __device__ __forceinline__ void flag_error(int32_t *dev_status, int32_t bit)
 {
@@ -76,20 +86,24 @@ struct SmemLayout {
     static constexpr int kBars = NW * S * 8;
     static constexpr int kMeta = NW * S * 4;
     static constexpr int kMerge = NW * GQ * (D + 2) * 4;                // per-warp (m, l, acc)
+    static constexpr int kSinkSc = GQ * 16 * 4;                         // sink-row scores
     static constexpr int kMisc = 64;
     static constexpr int kOffExtra = kRing;
     static constexpr int kOffQ = kOffExtra + kExtra;
     static constexpr int kOffBars = (kOffQ + kQ + 15) / 16 * 16;
     static constexpr int kOffMeta = kOffBars + kBars;
     static constexpr int kOffMerge = (kOffMeta + kMeta + 15) / 16 * 16;
-    static constexpr int kOffMisc = kOffMerge + kMerge;
+    static constexpr int kOffSinkSc = kOffMerge + kMerge;
+    static constexpr int kOffMisc = kOffSinkSc + kSinkSc;
     static constexpr int kOffPrefix = kOffMisc + kMisc;
     static size_t bytes(int num_seqs) { return 1024 + kOffPrefix + 4 * (size_t)(num_seqs + 1); }
 };
 
 // ---------------------------------------------------------------------------
-// Prefix over sequences: P[b] = sum_{b' < b} ceil(ctx_b' / 16). A context
-// length outside [0, max_blocks*16] counts as 0 blocks (and is reported).
+// Prefix over sequences: P[b] = sum_{b' < b} of the blocks sequence b' reads:
+// ceil(ctx / 16), less the blocks wholly before a sliding window's start. A
+// context length outside [0, max_blocks*16] counts as 0 blocks (and is
+// reported).
 // ---------------------------------------------------------------------------
 template <int NT>
 __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P, int32_t *wsum)
@@ -108,7 +122,8 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
                 if (blockIdx.x == 0)
                     flag_error(p.dev_status, PA_DEV_BAD_CONTEXT_BIT);
             } else {
-                v = (ctx + kBlockTokens - 1) / kBlockTokens;
+                // blocks from the one holding the window's first position
+                v = (ctx + kBlockTokens - 1) / kBlockTokens - window_start(p, ctx) / kBlockTokens;
             }
         }
         int32_t x = v;
@@ -196,10 +211,37 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t *addr, int v)
 // CTA to publish a record for it merges all records. Called by all threads.
 //   M = max_w m_w,  O = sum_w 2^(m_w-M) acc_w,  L = sum_w 2^(m_w-M) l_w
 // ---------------------------------------------------------------------------
+// Scores (log2 domain) of the bf16 sink rows [s_lo, s_hi) of (b, kvh) for
+// the GQ heads: sc[h * 16 + j - s_lo]. One warp per (head, row) pair, lanes
+// over d. Called by all threads; ends with a CTA barrier.
+template <int D, int GQ, int NW>
+__device__ __forceinline__ void sink_scores(const DecodeParams &p, int b, int kvh, int s_lo,
+                                            int s_hi, float *sc)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ns = s_hi - s_lo;
+    const __nv_bfloat16 *q = p.q + ((size_t)b * p.n_kv * GQ + (size_t)kvh * GQ) * D;
+    const __nv_bfloat16 *k = p.sink_k + ((size_t)b * p.n_kv + kvh) * p.n_sink * D;
+    for (int t = warp; t < GQ * ns; t += NW) {
+        const int h = t / ns, j = s_lo + t % ns;
+        float a = 0.f;
+#pragma unroll
+        for (int d = lane; d < D; d += 32)
+            a = fmaf(__bfloat162float(q[h * D + d]), __bfloat162float(k[j * D + d]), a);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0)
+            sc[h * 16 + (j - s_lo)] = a * p.scale_log2;
+    }
+    __syncthreads();
+}
+
 template <int D, int GQ, int NW>
 __device__ __forceinline__ void finish_segment(const DecodeParams &p, const float *merge,
-                                               int32_t *misc, int b, int kvh, int64_t unit_start,
-                                               int nb, int64_t W, int64_t G, bool whole)
+                                               int32_t *misc, float *sink_sc, int b, int kvh,
+                                               int64_t unit_start, int nb, int64_t W, int64_t G,
+                                               bool whole, int s_lo, int s_hi)
 {
     constexpr int NT = NW * 32;
     constexpr int REC = D + 2;
@@ -207,6 +249,12 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const floa
     const int u = b * p.n_kv + kvh;
     __nv_bfloat16 *out = p.out + ((size_t)b * n_h + (size_t)kvh * GQ) * D;
     float *rec = p.partials + ((size_t)blockIdx.x + u) * (GQ * REC);
+    // Sink rows [s_lo, s_hi) join this segment's merge as one more partial
+    // state (the segment that holds the sequence's first block has them).
+    const int ns = s_hi - s_lo;
+    if (ns > 0)
+        sink_scores<D, GQ, NW>(p, b, kvh, s_lo, s_hi, sink_sc);
+    const __nv_bfloat16 *sv = p.sink_v + ((size_t)b * p.n_kv + kvh) * p.n_sink * D;
 
 #pragma unroll 1
     for (int idx = threadIdx.x; idx < GQ * D; idx += NT) {
@@ -218,6 +266,8 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const floa
             mw[w] = merge[(w * GQ + h) * REC];
             M = fmaxf(M, mw[w]);
         }
+        for (int j = 0; j < ns; ++j)
+            M = fmaxf(M, sink_sc[h * 16 + j]);
         float O = 0.f, L = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
@@ -225,6 +275,11 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const floa
                 const float sc = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
                 L = fmaf(sc, merge[(w * GQ + h) * REC + 1], L);
                 O = fmaf(sc, merge[(w * GQ + h) * REC + 2 + d], O);
+            }
+            for (int j = 0; j < ns; ++j) {
+                const float e = fast_exp2(sink_sc[h * 16 + j] - M);
+                L += e;
+                O = fmaf(e, __bfloat162float(sv[(s_lo + j) * D + d]), O);
             }
         }
         if (whole) {
@@ -334,6 +389,8 @@ __device__ __forceinline__ void load_item(const DecodeParams &p, const int32_t *
     const int64_t x = r.lo + r.warp + k * NW;
     int b, i, nb;
     locate_item(x, P, p.num_seqs, p.n_kv, b, kvh, i, nb);
+    if (p.window > 0)
+        i += window_start(p, __ldg(p.context_lens + b)) / kBlockTokens;
     phys = __ldg(p.block_tables + (size_t)b * p.max_blocks + i);
 }
 

@@ -181,8 +181,8 @@ struct Int8MmaPolicy {
     }
 
     // One 16-token block: K codes at kt, V codes at kt + TILE, scales at extra
-    // (16 K scales, then 16 V scales).
-    __device__ static void compute(State &st, uint32_t kt, uint32_t extra, int valid,
+    // (16 K scales, then 16 V scales). Rows [lo, valid) are attended.
+    __device__ static void compute(State &st, uint32_t kt, uint32_t extra, int lo, int valid,
                                    float scale_log2)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
@@ -219,7 +219,7 @@ struct Int8MmaPolicy {
         }
 
         // ---- scores in the log2 domain; rows gid, gid+8 are tokens
-        const bool lo_ok = gid < valid, hi_ok = gid + 8 < valid;
+        const bool lo_ok = gid >= lo && gid < valid, hi_ok = gid + 8 >= lo && gid + 8 < valid;
         const float f_lo = st.qexp * lds_f32(extra + 4 * gid) * scale_log2;
         const float f_hi = st.qexp * lds_f32(extra + 4 * (gid + 8)) * scale_log2;
         float pr[NT][4];

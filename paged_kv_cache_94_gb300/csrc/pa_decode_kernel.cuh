@@ -107,7 +107,8 @@ struct Bf16Policy {
     }
 
     // One 16-token block: K tile at kt, V tile at kt + TILE (shared addresses).
-    __device__ static void compute(State &st, uint32_t kt, uint32_t /*extra*/, int valid,
+    // Rows [lo, valid) of the block are attended; the others are masked.
+    __device__ static void compute(State &st, uint32_t kt, uint32_t /*extra*/, int lo, int valid,
                                    float scale_log2)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
@@ -139,7 +140,7 @@ struct Bf16Policy {
         }
 
         // ---- online softmax (columns = heads; rows = tokens gid, gid+8)
-        const bool lo_ok = gid < valid, hi_ok = gid + 8 < valid;
+        const bool lo_ok = gid >= lo && gid < valid, hi_ok = gid + 8 >= lo && gid + 8 < valid;
         uint32_t pb0[NT], pb1[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -194,9 +195,9 @@ struct Bf16Policy {
             pb1[nt] = movmatrix_trans(pack_bf16x2(sc[2], sc[3]));
         }
 
-        // ---- O^T += V^T P^T. Rows of V past `valid` may hold anything (even
-        // NaN): their operand halves are zeroed, since 0 * NaN is NaN.
-        if (valid == kBlockTokens) {
+        // ---- O^T += V^T P^T. Rows of V outside [lo, valid) may hold anything
+        // (even NaN): their operand halves are zeroed, since 0 * NaN is NaN.
+        if (lo == 0 && valid == kBlockTokens) {
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 uint32_t a0, a1, a2, a3;
@@ -207,8 +208,9 @@ struct Bf16Policy {
             }
         } else {
             const int t0 = 2 * t4;
-            const uint32_t mlo = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
-            const uint32_t mhi = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+            auto in = [&](int t) { return t >= lo && t < valid; };
+            const uint32_t mlo = (in(t0) ? 0x0000ffffu : 0u) | (in(t0 + 1) ? 0xffff0000u : 0u);
+            const uint32_t mhi = (in(t0 + 8) ? 0x0000ffffu : 0u) | (in(t0 + 9) ? 0xffff0000u : 0u);
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 uint32_t a0, a1, a2, a3;
@@ -286,6 +288,7 @@ __global__ void __launch_bounds__(Pol::NW * 32)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBars);
     int32_t *meta = reinterpret_cast<int32_t *>(smem + L::kOffMeta);
     float *merge = reinterpret_cast<float *>(smem + L::kOffMerge);
+    float *sink_sc = reinterpret_cast<float *>(smem + L::kOffSinkSc);
     int32_t *misc = reinterpret_cast<int32_t *>(smem + L::kOffMisc);
     int32_t *P = reinterpret_cast<int32_t *>(smem + L::kOffPrefix);
 
@@ -382,7 +385,12 @@ __global__ void __launch_bounds__(Pol::NW * 32)
         const int64_t unit_end = unit_start + nb;
         const int64_t seg_hi = unit_end < hi ? unit_end : hi;
         const bool whole = (i0 == 0) && (unit_end <= hi);
-        const int last_valid = __ldg(p.context_lens + b) - (nb - 1) * kBlockTokens;
+        // Attended positions: [ws, ctx); the pool serves [max(ws, n_sink), ctx)
+        // from logical block fb on, the sink rows serve [ws, min(n_sink, ctx)).
+        const int32_t ctx = __ldg(p.context_lens + b);
+        const int32_t ws = window_start(p, ctx);
+        const int32_t pool_from = ws > p.n_sink ? ws : p.n_sink;
+        const int32_t fb = ws / kBlockTokens;
 
         Pol::load_q(st, p, b, kvh, qsm);
         Pol::reset(st);
@@ -398,10 +406,12 @@ __global__ void __launch_bounds__(Pol::NW * 32)
                     flag_error(p.dev_status, PA_DEV_TIMEOUT_BIT);
             }
             if (ok && wmeta[cstage] >= 0) {
-                const int bi = (int)(x - unit_start);
-                const int valid = (bi == nb - 1) ? last_valid : kBlockTokens;
+                const int32_t t0 = (fb + (int32_t)(x - unit_start)) * kBlockTokens;
+                const int lo = pool_from > t0 ? (int)min(pool_from - t0, kBlockTokens) : 0;
+                const int valid = (int)min(ctx - t0, kBlockTokens);
                 Pol::compute(st, ring_base + (uint32_t)(cstage * Pol::STAGE),
-                             extra_base + (uint32_t)(cstage * Pol::EXTRA), valid, p.scale_log2);
+                             extra_base + (uint32_t)(cstage * Pol::EXTRA), lo, valid,
+                             p.scale_log2);
             }
             __syncwarp();
             if (!dead && r.issued < r.n_items)
@@ -415,7 +425,9 @@ __global__ void __launch_bounds__(Pol::NW * 32)
         }
         Pol::to_merge(st, merge);
         __syncthreads();
-        finish_segment<D, GQ, NW>(p, merge, misc, b, kvh, unit_start, nb, W, G, whole);
+        const int32_t s_hi = (i0 == 0 && p.n_sink > ws) ? min(p.n_sink, ctx) : 0;
+        finish_segment<D, GQ, NW>(p, merge, misc, sink_sc, b, kvh, unit_start, nb, W, G, whole,
+                                  ws, s_hi > ws ? s_hi : ws);
         seg_lo = seg_hi;
     }
 

@@ -33,6 +33,10 @@ cudaError_t launch_cache_write(const void *k, const void *v, const int64_t *slot
                                void *v_cache, float *k_scale, float *v_scale, int32_t *dev_status,
                                cudaStream_t stream);
 
+cudaError_t launch_sink_write(const void *k, const void *v, const int32_t *seq_rows,
+                              const int32_t *positions, int64_t T, int n_kv, int d_h, int n_sink,
+                              int num_seqs, void *sink_k, void *sink_v, cudaStream_t stream);
+
 cudaError_t launch_block_copy(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
                               const int32_t *pairs, int32_t num_pairs, int64_t num_blocks,
                               int n_kv, int d_h, bool int8, int32_t *dev_status,

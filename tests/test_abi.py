@@ -151,3 +151,23 @@ def test_block_copy_argument_checks(lib):
     assert lib.pa_block_copy(fake, fake, None, None, fake, 3, gi, None, None) == -1
     assert lib.pa_block_copy(odd, fake, None, None, fake, 3, g, None, None) == -11
     assert lib.pa_block_copy(fake, fake, None, None, fake, 3, _geom(d_h=96), None, None) == -4
+
+
+def test_decode_opt_argument_checks(lib):
+    fake = ctypes.c_void_p(256)
+    dec = [fake, fake, fake, None, None, fake, 4, fake, 2, ctypes.c_float(0.1), fake, fake,
+           ctypes.c_size_t(1 << 20)]
+
+    def call(g, **kw):
+        o = pa.pa_decode_opts(**{**dict(window=0, n_sink=0, sink_k=None, sink_v=None,
+                                        num_ctas=0, reserved=0), **kw})
+        return lib.pa_decode_opt(*dec, g, ctypes.byref(o), None, None)
+
+    g = _geom()
+    assert call(g, window=-1) == -2
+    assert call(g, reserved=3) == -2
+    assert call(g, n_sink=4, sink_k=256, sink_v=256) == -2          # sink rows need INT8
+    gi = _geom(kv_dtype=1)
+    assert call(gi, n_sink=17, sink_k=256, sink_v=256) == -2
+    assert call(gi, n_sink=4, sink_k=None, sink_v=256) == -1
+    assert call(gi, n_sink=4, sink_k=257, sink_v=256) == -11

@@ -69,6 +69,7 @@ class Workload:
     prefix_len: np.ndarray            # int32 [B]: shared-prefix tokens of each seq (0 = none)
     group: np.ndarray                 # int32 [B]: shared-prefix group id (-1 = none)
     description: str = ""
+    window: int = 0                   # > 0: the step attends the last `window` tokens only
     # streams are generated lazily; cache of (stream id) -> (k, v) on a device
     _cache: dict = field(default_factory=dict, repr=False)
 
@@ -238,7 +239,8 @@ def _deal_tables(rng_perm: np.ndarray, context_lens: np.ndarray, block_size: int
 def make_workload(name: str, geom: Geometry, context_lens, seed: int,
                   pool_factor: float = 1.1, num_blocks: Optional[int] = None,
                   prefix_len=None, group=None, scale: Optional[float] = None,
-                  extra_table_cols: int = 0, description: str = "") -> Workload:
+                  extra_table_cols: int = 0, description: str = "",
+                  window: int = 0) -> Workload:
     """Build a workload from explicit context lengths.
 
     pool_factor: the physical pool holds ceil(pool_factor * blocks needed) blocks
@@ -270,7 +272,7 @@ def make_workload(name: str, geom: Geometry, context_lens, seed: int,
         scale = 1.0 / math.sqrt(geom.d_h)
     return Workload(name=name, geom=geom, seed=seed, context_lens=ctx, block_tables=tables,
                     num_blocks=int(num_blocks), scale=float(scale), prefix_len=pl, group=gr,
-                    description=description)
+                    description=description, window=int(window))
 
 
 # ---------------------------------------------------------------------------
@@ -278,11 +280,13 @@ def make_workload(name: str, geom: Geometry, context_lens, seed: int,
 # ---------------------------------------------------------------------------
 
 CONFIG_NAMES = ["tiny", "llama3_8b", "llama3_70b", "llama2_7b_int8_prefix", "long_context"]
+# further workloads of the variants built beside the decode step
+EXTRA_NAMES = ["mistral_7b_window"]
 
 
 def named_workload(name: str) -> Workload:
-    """The five layer-decode workloads, seeded with 94 + their index."""
-    idx = CONFIG_NAMES.index(name)
+    """The named workloads, seeded with 94 + their index in CONFIG_NAMES + EXTRA_NAMES."""
+    idx = (CONFIG_NAMES + EXTRA_NAMES).index(name)
     seed = 94 + idx
     if name == "tiny":
         return make_workload(
@@ -309,6 +313,15 @@ def named_workload(name: str) -> Workload:
             prefix_len=np.full(32, prefix), group=grp,
             description="LLaMA-2-7B MHA layer, INT8 KV: B=32 in 4 groups of 8 sharing a "
                         "2048-token prefix, suffix lognormal(6,1) clipped to [16,4096]")
+    if name == "mistral_7b_window":
+        # "kv-cache-guide" (guijiagi.com) §5.2: window w = 4096 over sequences
+        # of up to s = 32768 tokens; Mistral-7B layer shape (GQA 32/8, d 128)
+        rng = np.random.default_rng(seed)
+        ctx = rng.integers(16384, 32768, size=16, endpoint=True)
+        return make_workload(
+            name, Geometry(n_h=32, n_kv=8, d_h=128), ctx, seed, window=4096,
+            description="Mistral-7B layer, sliding window 4096: B=16, ctx U[16384,32768], "
+                        "n_h=32, n_kv=8, d_h=128, bf16")
     if name == "long_context":
         return make_workload(
             name, Geometry(n_h=32, n_kv=8, d_h=128), [131072, 98304, 65536, 32768], seed,
