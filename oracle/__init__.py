@@ -65,6 +65,10 @@ def _load():
         lib.oracle_cache_write_int8.argtypes = [P, P, P, i64, i32, i32, i32, i64, P, P, P, P]
         lib.oracle_quantize_row_int8.restype = None
         lib.oracle_quantize_row_int8.argtypes = [P, i32, P, P]
+        lib.oracle_cache_write_int4.restype = ctypes.c_int
+        lib.oracle_cache_write_int4.argtypes = [P, P, P, i64, i32, i32, i32, i64, P, P, P, P]
+        lib.oracle_quantize_row_int4.restype = None
+        lib.oracle_quantize_row_int4.argtypes = [P, i32, P, P]
         lib.oracle_decode.restype = ctypes.c_int
         lib.oracle_decode.argtypes = [P, P, P, P, P, i32, P, i32, P, i32, i32, i32, i32, i32, i64,
                                       dbl, P]
@@ -104,9 +108,13 @@ class Pool:
             self.k = np.full(shape, fill, dtype=np.uint16)
             self.v = np.full(shape, fill, dtype=np.uint16)
             self.k_scale = self.v_scale = None
-        elif kv_dtype == "int8":
-            self.k = np.full(shape, 0, dtype=np.int8)
-            self.v = np.full(shape, 0, dtype=np.int8)
+        elif kv_dtype in ("int8", "int4"):
+            if kv_dtype == "int8":
+                self.k = np.full(shape, 0, dtype=np.int8)
+                self.v = np.full(shape, 0, dtype=np.int8)
+            else:  # two codes per byte
+                self.k = np.full(shape[:3] + (d_h // 2,), 0, dtype=np.uint8)
+                self.v = np.full(shape[:3] + (d_h // 2,), 0, dtype=np.uint8)
             sfill = np.nan if fill_nan else 0.0
             self.k_scale = np.full(shape[:3], sfill, dtype=np.float32)
             self.v_scale = np.full(shape[:3], sfill, dtype=np.float32)
@@ -125,14 +133,27 @@ class Pool:
             return lib.oracle_cache_write_bf16(_ptr(k_bits), _ptr(v_bits), _ptr(slots), T, self.n_kv,
                                                self.d_h, self.block_size, self.num_blocks,
                                                _ptr(self.k), _ptr(self.v))
-        return lib.oracle_cache_write_int8(_ptr(k_bits), _ptr(v_bits), _ptr(slots), T, self.n_kv,
-                                           self.d_h, self.block_size, self.num_blocks, _ptr(self.k),
-                                           _ptr(self.v), _ptr(self.k_scale), _ptr(self.v_scale))
+        fn = lib.oracle_cache_write_int8 if self.kv_dtype == "int8" else lib.oracle_cache_write_int4
+        return fn(_ptr(k_bits), _ptr(v_bits), _ptr(slots), T, self.n_kv, self.d_h,
+                  self.block_size, self.num_blocks, _ptr(self.k), _ptr(self.v),
+                  _ptr(self.k_scale), _ptr(self.v_scale))
 
     def decode(self, q_bits: np.ndarray, block_tables: np.ndarray, context_lens: np.ndarray,
                n_h: int, scale: float) -> tuple[np.ndarray, int]:
         """Decode attention for every sequence and head: float64 [B, n_h, d_h] and status."""
         return decode(q_bits, self, block_tables, context_lens, n_h, scale)
+
+
+KV_KIND = {"bf16": 0, "int8": 1, "int4": 2}
+
+
+def quantize_row_int4(x_bits: np.ndarray) -> tuple[np.ndarray, np.float32]:
+    """Quantise one bf16 row (uint16 bits) -> (INT4 codes, one per int8, fp32 scale)."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    code = np.zeros(x_bits.shape[0], dtype=np.int8)
+    sc = np.zeros(1, dtype=np.float32)
+    _load().oracle_quantize_row_int4(_ptr(x_bits), x_bits.shape[0], _ptr(code), _ptr(sc))
+    return code, sc[0]
 
 
 def quantize_row_int8(x_bits: np.ndarray) -> tuple[np.ndarray, np.float32]:
@@ -154,7 +175,7 @@ def decode(q_bits: np.ndarray, pool: Pool, block_tables: np.ndarray, context_len
     assert q_bits.shape == (B, n_h, pool.d_h)
     out = np.zeros((B, n_h, pool.d_h), dtype=np.float64)
     st = lib.oracle_decode(_ptr(q_bits), _ptr(pool.k), _ptr(pool.v), _ptr(pool.k_scale),
-                           _ptr(pool.v_scale), 1 if pool.kv_dtype == "int8" else 0, _ptr(bt),
+                           _ptr(pool.v_scale), KV_KIND[pool.kv_dtype], _ptr(bt),
                            bt.shape[1], _ptr(ctx), B, n_h, pool.n_kv, pool.d_h, pool.block_size,
                            pool.num_blocks, float(scale), _ptr(out))
     return out, st
@@ -174,7 +195,7 @@ def decode_window(q_bits: np.ndarray, pool: Pool, block_tables: np.ndarray,
     B = ctx.shape[0]
     assert q_bits.shape == (B, n_h, pool.d_h)
     if n_sink:
-        assert pool.kv_dtype == "int8"
+        assert pool.kv_dtype in ("int8", "int4")
         sink_k_bits = np.ascontiguousarray(sink_k_bits, dtype=np.uint16)
         sink_v_bits = np.ascontiguousarray(sink_v_bits, dtype=np.uint16)
         assert sink_k_bits.shape == (B, pool.n_kv, n_sink, pool.d_h)
@@ -183,7 +204,7 @@ def decode_window(q_bits: np.ndarray, pool: Pool, block_tables: np.ndarray,
         sink_k_bits = sink_v_bits = None
     out = np.zeros((B, n_h, pool.d_h), dtype=np.float64)
     st = lib.oracle_decode_window(_ptr(q_bits), _ptr(pool.k), _ptr(pool.v), _ptr(pool.k_scale),
-                                  _ptr(pool.v_scale), 1 if pool.kv_dtype == "int8" else 0,
+                                  _ptr(pool.v_scale), KV_KIND[pool.kv_dtype],
                                   _ptr(bt), bt.shape[1], _ptr(ctx), B, n_h, pool.n_kv, pool.d_h,
                                   pool.block_size, pool.num_blocks, float(scale), int(window),
                                   int(n_sink), _ptr(sink_k_bits), _ptr(sink_v_bits), _ptr(out))

@@ -153,14 +153,88 @@ int oracle_cache_write_int8(const uint16_t *k, const uint16_t *v, const int64_t 
     return status;
 }
 
-/* One cached K or V element in double precision. INT8: the fp32 product
- * code*scale ([G] §4.2 `dequantize_kv`), then widened. */
-static double cached_elem(const void *cache, const float *scales, int kv_is_int8, int64_t row, int d,
+/* ------------------------------------------------------------------------
+ * INT4 symmetric quantiser, [G] §4.2 `quantize_kv_cache` (num_bits == 4):
+ *   scale = max_d |x_d| / 7
+ *   code  = clamp(round(x / scale), -8, 7)
+ * with the same fp32 steps as the INT8 quantiser. Codes are returned one per
+ * int8 here; the cache packs two per byte (see oracle_cache_write_int4).
+ * ---------------------------------------------------------------------- */
+void oracle_quantize_row_int4(const uint16_t *x, int d_h, int8_t *code, float *scale_out)
+{
+    volatile float amax = 0.0f;
+    for (int d = 0; d < d_h; ++d) {
+        float a = fabsf(bf16_bits_to_float(x[d]));
+        if (a > amax)
+            amax = a;
+    }
+    volatile float scale = amax / 7.0f;
+    *scale_out = scale;
+    for (int d = 0; d < d_h; ++d) {
+        if (scale == 0.0f) {
+            code[d] = 0;
+            continue;
+        }
+        volatile float r = bf16_bits_to_float(x[d]) / scale;
+        float n = nearbyintf(r);
+        if (n < -8.0f)
+            n = -8.0f;
+        if (n > 7.0f)
+            n = 7.0f;
+        code[d] = (int8_t)n;
+    }
+}
+
+/* INT4 append: each (token, head) row of d_h values becomes d_h/2 bytes, the
+ * code of element 2i in the low nibble of byte i and that of 2i+1 in the high
+ * nibble, each a 4-bit two's-complement number (the pages say only "packed
+ * two per byte"; this order is the plainest reading). */
+int oracle_cache_write_int4(const uint16_t *k, const uint16_t *v, const int64_t *slots, int64_t T,
+                            int n_kv, int d_h, int block_size, int64_t num_blocks,
+                            uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale)
+{
+    int status = 0;
+    int8_t *codes = (int8_t *)malloc((size_t)d_h);
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t s = slots[t];
+        if (s < 0)
+            continue;
+        if (s >= num_blocks * block_size) {
+            status |= ORC_BAD_SLOT;
+            continue;
+        }
+        int64_t blk = s / block_size, off = s % block_size;
+        for (int h = 0; h < n_kv; ++h) {
+            int64_t row = (blk * n_kv + h) * block_size + off;
+            for (int which = 0; which < 2; ++which) {
+                const uint16_t *x = (which ? v : k) + (t * n_kv + h) * (int64_t)d_h;
+                uint8_t *dst = (which ? v_cache : k_cache) + row * (d_h / 2);
+                oracle_quantize_row_int4(x, d_h, codes, which ? &v_scale[row] : &k_scale[row]);
+                for (int i = 0; i < d_h / 2; ++i)
+                    dst[i] = (uint8_t)((codes[2 * i] & 0xF) | ((codes[2 * i + 1] & 0xF) << 4));
+            }
+        }
+    }
+    free(codes);
+    return status;
+}
+
+/* One cached K or V element in double precision. kv_kind: 0 bf16, 1 INT8,
+ * 2 INT4. INT8/INT4: the fp32 product code*scale ([G] §4.2
+ * `dequantize_kv`), then widened. */
+static double cached_elem(const void *cache, const float *scales, int kv_kind, int64_t row, int d,
                           int d_h)
 {
-    if (kv_is_int8) {
+    if (kv_kind == 1) {
         const int8_t *c = (const int8_t *)cache;
         float x = (float)c[row * d_h + d] * scales[row];
+        return (double)x;
+    }
+    if (kv_kind == 2) {
+        const uint8_t *c = (const uint8_t *)cache;
+        int nib = (c[row * (d_h / 2) + d / 2] >> (4 * (d & 1))) & 0xF;
+        int code = nib >= 8 ? nib - 16 : nib;
+        float x = (float)code * scales[row];
         return (double)x;
     }
     const uint16_t *c = (const uint16_t *)cache;
@@ -185,7 +259,7 @@ static double cached_elem(const void *cache, const float *scales, int kv_is_int8
  * out: double [B][n_h][d_h].
  * ---------------------------------------------------------------------- */
 int oracle_decode(const uint16_t *q, const void *k_cache, const void *v_cache, const float *k_scale,
-                  const float *v_scale, int kv_is_int8, const int32_t *block_tables,
+                  const float *v_scale, int kv_kind, const int32_t *block_tables,
                   int max_blocks_per_seq, const int32_t *context_lens, int B, int n_h, int n_kv,
                   int d_h, int block_size, int64_t num_blocks, double scale, double *out)
 {
@@ -231,7 +305,7 @@ int oracle_decode(const uint16_t *q, const void *k_cache, const void *v_cache, c
                 double dot = 0.0;
                 for (int d = 0; d < d_h; ++d)
                     dot += (double)bf16_bits_to_float(qh[d]) *
-                           cached_elem(k_cache, k_scale, kv_is_int8, row, d, d_h);
+                           cached_elem(k_cache, k_scale, kv_kind, row, d, d_h);
                 scores[j] = dot * scale;
                 if (scores[j] > m)
                     m = scores[j];
@@ -252,7 +326,7 @@ int oracle_decode(const uint16_t *q, const void *k_cache, const void *v_cache, c
                 int64_t row = (blk * n_kv + kvh) * block_size + off;
                 double w = scores[j] / denom;
                 for (int d = 0; d < d_h; ++d)
-                    o[d] += w * cached_elem(v_cache, v_scale, kv_is_int8, row, d, d_h);
+                    o[d] += w * cached_elem(v_cache, v_scale, kv_kind, row, d, d_h);
             }
         }
     }
@@ -270,7 +344,7 @@ int oracle_decode(const uint16_t *q, const void *k_cache, const void *v_cache, c
  * read (a sliding-window cache may have released them).
  *
  * Attention sink ([G] §4.3: the first k tokens, typically 4, stay
- * unquantised in an INT8 cache): for an INT8 pool and n_sink > 0, an attended
+ * unquantised in a quantised cache): for an INT8 or INT4 pool and n_sink > 0, an attended
  * position j < n_sink takes its K and V rows from the bf16 sink rows
  * sink_k/sink_v[b][kv][j][:] ([B][n_kv][n_sink][d_h] bit patterns) instead of
  * dequantising the pool. Every other position reads the pool as in
@@ -282,7 +356,7 @@ int oracle_decode(const uint16_t *q, const void *k_cache, const void *v_cache, c
  * The softmax and the two passes are those of oracle_decode.
  * ---------------------------------------------------------------------- */
 int oracle_decode_window(const uint16_t *q, const void *k_cache, const void *v_cache,
-                         const float *k_scale, const float *v_scale, int kv_is_int8,
+                         const float *k_scale, const float *v_scale, int kv_kind,
                          const int32_t *block_tables, int max_blocks_per_seq,
                          const int32_t *context_lens, int B, int n_h, int n_kv, int d_h,
                          int block_size, int64_t num_blocks, double scale, int window, int n_sink,
@@ -335,7 +409,7 @@ int oracle_decode_window(const uint16_t *q, const void *k_cache, const void *v_c
                     int64_t row = (blk * n_kv + kvh) * block_size + j % block_size;
                     for (int d = 0; d < d_h; ++d)
                         dot += (double)bf16_bits_to_float(qh[d]) *
-                               cached_elem(k_cache, k_scale, kv_is_int8, row, d, d_h);
+                               cached_elem(k_cache, k_scale, kv_kind, row, d, d_h);
                 }
                 scores[j - start] = dot * scale;
                 if (scores[j - start] > m)
@@ -359,7 +433,7 @@ int oracle_decode_window(const uint16_t *q, const void *k_cache, const void *v_c
                     int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + j / block_size];
                     int64_t row = (blk * n_kv + kvh) * block_size + j % block_size;
                     for (int d = 0; d < d_h; ++d)
-                        o[d] += w * cached_elem(v_cache, v_scale, kv_is_int8, row, d, d_h);
+                        o[d] += w * cached_elem(v_cache, v_scale, kv_kind, row, d, d_h);
                 }
             }
         }
