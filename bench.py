@@ -63,8 +63,12 @@ def parse_args():
 
 
 # --------------------------------------------------------------------- bytes
-def kv_bytes_per_elem(w) -> int:
-    return 1 if w.geom.kv_dtype == "int8" else 2
+def kv_bits_per_elem(w) -> int:
+    return {"bf16": 16, "int8": 8, "int4": 4}[w.geom.kv_dtype]
+
+
+def scale_bytes_per_row(w) -> int:
+    return 0 if w.geom.kv_dtype == "bf16" else 4
 
 
 def decode_bytes(w, unique_blocks: bool = True) -> dict:
@@ -76,8 +80,7 @@ def decode_bytes(w, unique_blocks: bool = True) -> dict:
     Under a sliding window only the window's tokens and blocks count.
     """
     g = w.geom
-    bkv = kv_bytes_per_elem(w)
-    per_token = 2 * g.n_kv * g.d_h * bkv + (2 * g.n_kv * 4 if g.kv_dtype == "int8" else 0)
+    per_token = 2 * g.n_kv * g.d_h * kv_bits_per_elem(w) // 8 + 2 * g.n_kv * scale_bytes_per_row(w)
 
     def span(b):  # attended positions [lo, ctx) and the blocks they touch
         ctx = int(w.context_lens[b])
@@ -110,7 +113,7 @@ def cache_write_bytes(w) -> int:
     g = w.geom
     rows = w.B * g.n_kv
     read = 2 * rows * g.d_h * 2 + 8 * w.B
-    write = 2 * rows * g.d_h * kv_bytes_per_elem(w) + (2 * rows * 4 if g.kv_dtype == "int8" else 0)
+    write = 2 * rows * g.d_h * kv_bits_per_elem(w) // 8 + 2 * rows * scale_bytes_per_row(w)
     return read + write
 
 
@@ -124,8 +127,9 @@ def peaks() -> dict:
 
 # Device code of the decode kernel: its DRAM counters depend on these files only.
 DECODE_DEVICE_SOURCES = ["pa_ptx.cuh", "pa_plan.h", "pa_internal.h", "pa_decode.cuh",
-                         "pa_decode_kernel.cuh", "pa_decode_int8.cuh", "pa_decode_bf16_d128.cu", "pa_decode_bf16_d64.cu",
-                         "pa_decode_int8_d128.cu", "pa_decode_int8_d64.cu"]
+                         "pa_decode_kernel.cuh", "pa_decode_quant.cuh", "pa_decode_bf16_d128.cu",
+                         "pa_decode_bf16_d64.cu", "pa_decode_int8_d128.cu", "pa_decode_int8_d64.cu",
+                         "pa_decode_int4_d128.cu", "pa_decode_int4_d64.cu"]
 
 
 def kernel_source_hash() -> str:
@@ -214,7 +218,7 @@ def oracle_sample(w, gen_device, seconds: float):
     done_bytes, spent, seqs = 0, 0.0, []
     order = list(range(w.B))
     q_all = oracle.bf16_bits(w.q(gen_device))
-    per_token = 2 * g.n_kv * g.d_h * kv_bytes_per_elem(w) + (2 * g.n_kv * 4 if g.kv_dtype == "int8" else 0)
+    per_token = 2 * g.n_kv * g.d_h * kv_bits_per_elem(w) // 8 + 2 * g.n_kv * scale_bytes_per_row(w)
     for b in order:
         k, v = w.seq_kv(b, gen_device)
         ctx = int(w.context_lens[b])
@@ -323,7 +327,7 @@ def run_native(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8" if g.kv_dtype == "int8" else "bf16", "data": "synthetic",
+        "dtype": g.kv_dtype, "data": "synthetic",
         "config": {"workload": f"{w.name}: {w.description}", "num_seqs": w.B,
                    "context_tokens": int(w.context_lens.sum()),
                    "l2": "flushed between timed steps (512 MiB write); KV working set "
@@ -395,9 +399,9 @@ def run_native(args, rank, world, local_rank):
 
 # ---------------------------------------------------------------- block copy
 def block_copy_bytes(g, pairs: int) -> int:
-    """Read + write of every copied block: K and V tiles (+ INT8 scales)."""
-    tile = g.n_kv * 16 * g.d_h * (1 if g.kv_dtype == "int8" else 2)
-    scales = 2 * g.n_kv * 16 * 4 if g.kv_dtype == "int8" else 0
+    """Read + write of every copied block: K and V tiles (+ INT8/INT4 scales)."""
+    tile = g.n_kv * 16 * g.d_h * {"bf16": 16, "int8": 8, "int4": 4}[g.kv_dtype] // 8
+    scales = 2 * g.n_kv * 16 * 4 if g.kv_dtype != "bf16" else 0
     return 2 * pairs * (2 * tile + scales) + 8 * pairs
 
 
@@ -415,8 +419,8 @@ def run_block_copy(args, rank, world, local_rank):
     g = w.geom
     nb = max(w.num_blocks, 2 * args.pairs)
     kc, vc, ks, vs = pa.allocate_pool(nb, g.n_kv, g.d_h, g.kv_dtype, dev)
-    kc.view(torch.uint8).random_(0, 256) if kc.dtype == torch.int8 else kc.normal_()
-    vc.view(torch.uint8).random_(0, 256) if vc.dtype == torch.int8 else vc.normal_()
+    for t in (kc, vc):
+        t.view(torch.uint8).random_(0, 256) if t.dtype != torch.bfloat16 else t.normal_()
     pairs_h = block_copy_pairs(7, nb, args.pairs)
     pairs = torch.from_numpy(pairs_h).to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -455,7 +459,7 @@ def run_block_copy(args, rank, world, local_rank):
         "metric": "copy-on-write block copy: HBM GB/s", "value": round(world * achieved, 2),
         "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int8" if g.kv_dtype == "int8" else "bf16",
+        "vs_baseline": None, "dtype": g.kv_dtype,
         "data": "synthetic",
         "config": {"workload": f"pa_block_copy of {args.pairs} blocks, {w.name} pool geometry "
                                f"(n_kv={g.n_kv}, d_h={g.d_h}, {g.kv_dtype})",
@@ -492,7 +496,7 @@ def run_block_copy(args, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle.allocator import block_copy as oracle_copy
         def host(t):
-            return t.cpu().numpy() if t.dtype == torch.int8 else t.view(torch.int16).cpu().numpy()
+            return t.view(torch.int16).cpu().numpy() if t.dtype == torch.bfloat16 else t.cpu().numpy()
         k_h, v_h = host(kc), host(vc)
         ks_h = ks.cpu().numpy() if ks is not None else None
         vs_h = vs.cpu().numpy() if vs is not None else None

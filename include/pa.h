@@ -44,7 +44,8 @@
  * Pool layout (the block layout [num_blocks, H, block_size, D] that [G] §7.1
  * gives for PagedAttention):
  *   k_cache, v_cache : [num_blocks][n_kv][block_size][d_h]  bf16 or int8 codes
- *   k_scale, v_scale : [num_blocks][n_kv][block_size]       fp32 (INT8 only)
+ *                      [num_blocks][n_kv][block_size][d_h/2] bytes for INT4
+ *   k_scale, v_scale : [num_blocks][n_kv][block_size]       fp32 (INT8, INT4)
  * so the 16 rows of one (block, kv head) pair are one contiguous tile.
  * Token j of a sequence lives in physical block block_table[j / block_size] at
  * offset j % block_size ([F] "逻辑块与物理块映射"); its slot is
@@ -88,7 +89,10 @@ typedef enum pa_status {
 /* Element type of the cached K/V. */
 typedef enum pa_kv_dtype {
     PA_KV_BF16 = 0, /* bf16 rows, stored as given */
-    PA_KV_INT8 = 1  /* int8 codes + one fp32 scale per (token, kv head), [G] §4.2 */
+    PA_KV_INT8 = 1, /* int8 codes + one fp32 scale per (token, kv head), [G] §4.2 */
+    PA_KV_INT4 = 2  /* int4 codes, two per byte (element 2i in the low nibble of
+                       byte i, two's complement), + one fp32 scale per (token,
+                       kv head), [G] §4.2 with num_bits = 4 */
 } pa_kv_dtype;
 
 /* Attention and pool geometry of one layer.
@@ -126,12 +130,15 @@ typedef struct pa_geom {
  *     code  = clamp(round_half_even(x / scale), -128, 127)
  * and scale is stored in k_scale/v_scale[s / bs][h][s % bs]. A row of zeros
  * stores scale 0 and zero codes.
+ * INT4 (PA_KV_INT4), the same with num_bits = 4:
+ *     scale = max_d |x_d| / 7,  code = clamp(round_half_even(x / scale), -8, 7)
+ * packed two per byte as the pa_kv_dtype comment says.
  *
  *   k, v          bf16 [num_tokens][n_kv][d_h]      new rows (read)
  *   slot_mapping  int64 [num_tokens]                 slot of each row; < 0 = skip
  *   num_tokens    >= 0 (0 enqueues nothing)
  *   k_cache, v_cache  pool (written), layout above
- *   k_scale, v_scale  fp32 scales (written); must be NULL for PA_KV_BF16
+ *   k_scale, v_scale  fp32 scales (written, INT8/INT4); must be NULL for PA_KV_BF16
  *   dev_status    optional int32 device word for PA_DEV_BAD_SLOT
  * Duplicate non-negative slots in one call leave the slot's content undefined.
  */
@@ -216,7 +223,7 @@ pa_status pa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
  *             attends positions [max(0, ctx_b - window), ctx_b). Block-table
  *             entries of logical blocks wholly before that start are never
  *             read (a windowed cache may have released them). 0 = attend all.
- *   n_sink    INT8 pools only, 0..16: attention-sink rows ([G] §4.3: the first
+ *   n_sink    INT8/INT4 pools only, 0..16: attention-sink rows ([G] §4.3: the first
  *             k tokens, typically 4, stay unquantised in an INT8 cache). An
  *             attended position j < n_sink takes its K and V from the bf16
  *             rows sink_k/sink_v[b][kv head][j][:] instead of the pool; the

@@ -25,6 +25,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "libpa.so")
 
 PA_KV_BF16 = 0
 PA_KV_INT8 = 1
+PA_KV_INT4 = 2
 
 PA_DEV_BAD_BLOCK = 0x1
 PA_DEV_BAD_SLOT = 0x2
@@ -175,7 +176,8 @@ def _need_cuda(name: str, t: torch.Tensor, dtype=None):
 
 
 def geometry(k_cache: torch.Tensor, n_h: int) -> pa_geom:
-    """pa_geom of a pool [num_blocks, n_kv, 16, d_h] (bf16 or int8) for n_h query heads."""
+    """pa_geom of a pool [num_blocks, n_kv, 16, d_h] (bf16 or int8; uint8 [.., d_h/2]
+    for INT4) for n_h query heads."""
     if k_cache.dim() != 4:
         raise ValueError("k_cache must be [num_blocks, n_kv, block_size, d_h]")
     nb, n_kv, bs, d = k_cache.shape
@@ -183,8 +185,11 @@ def geometry(k_cache: torch.Tensor, n_h: int) -> pa_geom:
         dt = PA_KV_BF16
     elif k_cache.dtype == torch.int8:
         dt = PA_KV_INT8
+    elif k_cache.dtype == torch.uint8:
+        dt = PA_KV_INT4  # two codes per byte
+        d = 2 * d
     else:
-        raise TypeError("k_cache must be bfloat16 or int8")
+        raise TypeError("k_cache must be bfloat16, int8 or uint8 (INT4)")
     return pa_geom(num_blocks=nb, n_h=n_h, n_kv=n_kv, d_h=d, block_size=bs, kv_dtype=dt, reserved=0)
 
 
@@ -201,10 +206,10 @@ def pa_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
     g = geometry(k_cache, n_h=k_cache.shape[1])
     if k.shape != (slot_mapping.shape[0], g.n_kv, g.d_h) or v.shape != k.shape:
         raise ValueError("k, v must be [num_tokens, n_kv, d_h] matching the pool and slot_mapping")
-    if g.kv_dtype == PA_KV_INT8:
+    if g.kv_dtype != PA_KV_BF16:
         for nm, s in (("k_scale", k_scale), ("v_scale", v_scale)):
             if s is None:
-                raise ValueError(f"{nm} is required for an int8 pool")
+                raise ValueError(f"{nm} is required for an int8/int4 pool")
             _need_cuda(nm, s, torch.float32)
             if tuple(s.shape) != tuple(k_cache.shape[:3]):
                 raise ValueError(f"{nm} must be [num_blocks, n_kv, block_size]")
@@ -287,10 +292,10 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     if d != g.d_h or block_tables.dim() != 2 or block_tables.shape[0] != B or \
             context_lens.shape != (B,):
         raise ValueError("q, block_tables, context_lens disagree on num_seqs or d_h")
-    if g.kv_dtype == PA_KV_INT8:
+    if g.kv_dtype != PA_KV_BF16:
         for nm, s in (("k_scale", k_scale), ("v_scale", v_scale)):
             if s is None:
-                raise ValueError(f"{nm} is required for an int8 pool")
+                raise ValueError(f"{nm} is required for an int8/int4 pool")
             _need_cuda(nm, s, torch.float32)
     if out is None:
         out = torch.empty_like(q)
@@ -380,9 +385,13 @@ def allocate_pool(num_blocks: int, n_kv: int, d_h: int, kv_dtype: str = "bf16",
         kc = torch.zeros(shape, dtype=torch.bfloat16, device=device)
         vc = torch.zeros(shape, dtype=torch.bfloat16, device=device)
         return kc, vc, None, None
-    if kv_dtype == "int8":
-        kc = torch.zeros(shape, dtype=torch.int8, device=device)
-        vc = torch.zeros(shape, dtype=torch.int8, device=device)
+    if kv_dtype in ("int8", "int4"):
+        if kv_dtype == "int8":
+            kc = torch.zeros(shape, dtype=torch.int8, device=device)
+            vc = torch.zeros(shape, dtype=torch.int8, device=device)
+        else:
+            kc = torch.zeros(shape[:3] + (d_h // 2,), dtype=torch.uint8, device=device)
+            vc = torch.zeros(shape[:3] + (d_h // 2,), dtype=torch.uint8, device=device)
         ks = torch.zeros(shape[:3], dtype=torch.float32, device=device)
         vs = torch.zeros(shape[:3], dtype=torch.float32, device=device)
         return kc, vc, ks, vs
@@ -402,10 +411,10 @@ def pa_block_copy(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs: torch.Ten
     if pairs.dim() != 2 or pairs.shape[1] != 2:
         raise ValueError("pairs must be [num_pairs, 2]")
     g = geometry(k_cache, n_h=k_cache.shape[1])
-    if g.kv_dtype == PA_KV_INT8:
+    if g.kv_dtype != PA_KV_BF16:
         for nm, s in (("k_scale", k_scale), ("v_scale", v_scale)):
             if s is None:
-                raise ValueError(f"{nm} is required for an int8 pool")
+                raise ValueError(f"{nm} is required for an int8/int4 pool")
             _need_cuda(nm, s, torch.float32)
             if tuple(s.shape) != tuple(k_cache.shape[:3]):
                 raise ValueError(f"{nm} must be [num_blocks, n_kv, block_size]")

@@ -26,7 +26,7 @@ pa_status check_geom(const pa_geom &g)
 {
     if (g.reserved != 0)
         return PA_ERR_SHAPE;
-    if (g.kv_dtype != PA_KV_BF16 && g.kv_dtype != PA_KV_INT8)
+    if (g.kv_dtype != PA_KV_BF16 && g.kv_dtype != PA_KV_INT8 && g.kv_dtype != PA_KV_INT4)
         return PA_ERR_DTYPE;
     if (g.n_h <= 0 || g.n_kv <= 0 || g.n_h % g.n_kv != 0 || g.num_blocks <= 0)
         return PA_ERR_SHAPE;
@@ -44,8 +44,9 @@ pa_status check_geom(const pa_geom &g)
 const DecodeKernel *kernel_for(const pa_geom &g)
 {
     const int gq = group_of(g);
-    return g.kv_dtype == PA_KV_INT8 ? pa::find_decode_kernel_int8(g.d_h, gq)
-                                    : pa::find_decode_kernel_bf16(g.d_h, gq);
+    return g.kv_dtype == PA_KV_INT8   ? pa::find_decode_kernel_int8(g.d_h, gq)
+           : g.kv_dtype == PA_KV_INT4 ? pa::find_decode_kernel_int4(g.d_h, gq)
+                                      : pa::find_decode_kernel_bf16(g.d_h, gq);
 }
 
 // --------------------------------------------------------------- device info
@@ -170,25 +171,28 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D view of a pool: rows of d_h elements, one row per (block, head, offset);
-// a box is one 16-row tile of at most 128 bytes per row, swizzled so that
-// ldmatrix/ld.shared of 8 consecutive rows hit distinct banks.
+// 2-D view of a pool: one row per (block, head, offset); a box is one 16-row
+// tile of at most 128 bytes per row. bf16 and INT8 tiles are swizzled so that
+// ldmatrix/ld.shared of 8 consecutive rows hit distinct banks; INT4 rows (64
+// or 32 bytes) are read as whole contiguous runs and stay unswizzled.
 pa_status encode_pool_uncached(CUtensorMap &m, const void *base, const pa_geom &g)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return PA_ERR_CUDA;
-    const bool i8 = g.kv_dtype == PA_KV_INT8;
-    const int esz = i8 ? 1 : 2;
-    const cuuint64_t dims[2] = {(cuuint64_t)g.d_h, (cuuint64_t)(g.num_blocks * g.n_kv * 16)};
-    const cuuint64_t strides[1] = {(cuuint64_t)g.d_h * esz};
-    const cuuint32_t box_x = (cuuint32_t)((g.d_h * esz > 128) ? 128 / esz : g.d_h);
+    const bool bf16 = g.kv_dtype == PA_KV_BF16, i4 = g.kv_dtype == PA_KV_INT4;
+    const int row_elems = i4 ? g.d_h / 2 : g.d_h; // bytes for INT8/INT4, elements for bf16
+    const int esz = bf16 ? 2 : 1;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)(g.num_blocks * g.n_kv * 16)};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_elems * esz};
+    const cuuint32_t box_x = (cuuint32_t)((row_elems * esz > 128) ? 128 / esz : row_elems);
     const cuuint32_t box[2] = {box_x, 16};
     const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapSwizzle sw =
-        (box_x * esz == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUtensorMapSwizzle sw = i4                     ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                  : (box_x * esz == 128) ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                         : CU_TENSOR_MAP_SWIZZLE_64B;
     const CUresult r =
-        fn(&m, i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+        fn(&m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
            const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
@@ -246,7 +250,7 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     if (o.window < 0 || o.n_sink < 0 || o.n_sink > 16 || o.reserved != 0)
         return PA_ERR_SHAPE;
     if (o.n_sink > 0) {
-        if (g.kv_dtype != PA_KV_INT8)
+        if (g.kv_dtype == PA_KV_BF16)
             return PA_ERR_SHAPE;
         if (!o.sink_k || !o.sink_v)
             return PA_ERR_NULL;
@@ -261,7 +265,7 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
         return PA_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
         return !workspace ? PA_ERR_WORKSPACE : PA_ERR_NULL;
-    const bool i8 = g.kv_dtype == PA_KV_INT8;
+    const bool i8 = g.kv_dtype != PA_KV_BF16; // INT8 or INT4: fp32 scales
     if (i8 && (!k_scale || !v_scale))
         return PA_ERR_NULL;
     if (!i8 && (k_scale || v_scale))
@@ -327,6 +331,15 @@ const DecodeKernel *find_decode_kernel_bf16(int d_h, int group)
                       : d_h == 64 ? find_decode_kernel_bf16_d64(group) : nullptr;
 }
 
+const DecodeKernel *find_decode_kernel_int4_d64(int group);
+const DecodeKernel *find_decode_kernel_int4_d128(int group);
+
+const DecodeKernel *find_decode_kernel_int4(int d_h, int group)
+{
+    return d_h == 128 ? find_decode_kernel_int4_d128(group)
+                      : d_h == 64 ? find_decode_kernel_int4_d64(group) : nullptr;
+}
+
 const DecodeKernel *find_decode_kernel_int8(int d_h, int group)
 {
     return d_h == 128 ? find_decode_kernel_int8_d128(group)
@@ -351,7 +364,7 @@ pa_status pa_cache_write(const void *k, const void *v, const int64_t *slot_mappi
         return PA_ERR_UNSUPPORTED;
     if (!k || !v || !slot_mapping || !k_cache || !v_cache)
         return PA_ERR_NULL;
-    const bool i8 = geom.kv_dtype == PA_KV_INT8;
+    const bool i8 = geom.kv_dtype != PA_KV_BF16; // INT8 or INT4: fp32 scales
     if (i8 && (!k_scale || !v_scale))
         return PA_ERR_NULL;
     if (!i8 && (k_scale || v_scale))
@@ -360,7 +373,8 @@ pa_status pa_cache_write(const void *k, const void *v, const int64_t *slot_mappi
         !aligned(slot_mapping, 8) || (i8 && (!aligned(k_scale, 4) || !aligned(v_scale, 4))))
         return PA_ERR_ALIGNMENT;
     const cudaError_t e = pa::launch_cache_write(
-        k, v, slot_mapping, num_tokens, geom.n_kv, geom.d_h, i8, geom.num_blocks * 16, k_cache,
+        k, v, slot_mapping, num_tokens, geom.n_kv, geom.d_h, geom.kv_dtype, geom.num_blocks * 16,
+        k_cache,
         v_cache, k_scale, v_scale, dev_status, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -378,7 +392,7 @@ pa_status pa_block_copy(void *k_cache, void *v_cache, float *k_scale, float *v_s
         return PA_OK;
     if (!k_cache || !v_cache || !pairs)
         return PA_ERR_NULL;
-    const bool i8 = geom.kv_dtype == PA_KV_INT8;
+    const bool i8 = geom.kv_dtype != PA_KV_BF16; // INT8 or INT4: fp32 scales
     if (i8 && (!k_scale || !v_scale))
         return PA_ERR_NULL;
     if (!i8 && (k_scale || v_scale))
@@ -388,7 +402,8 @@ pa_status pa_block_copy(void *k_cache, void *v_cache, float *k_scale, float *v_s
         return PA_ERR_ALIGNMENT;
     const cudaError_t e = pa::launch_block_copy(k_cache, v_cache, k_scale, v_scale, pairs,
                                                 num_pairs, geom.num_blocks, geom.n_kv, geom.d_h,
-                                                i8, dev_status, static_cast<cudaStream_t>(stream));
+                                                geom.kv_dtype, dev_status,
+                                                static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

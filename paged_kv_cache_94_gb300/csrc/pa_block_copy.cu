@@ -7,7 +7,7 @@
 //
 // One block of one tensor is n_kv * 16 * d_h elements, contiguous in the
 // [num_blocks][n_kv][16][d_h] pool (32 KiB for 8 bf16 heads of 128), plus
-// n_kv * 16 fp32 scales for INT8. CTA (x, z) copies chunk x % chunks of pair
+// n_kv * 16 fp32 scales for INT8 and INT4. CTA (x, z) copies chunk x % chunks of pair
 // x / chunks of tensor z (0 = K, 1 = V): 256 threads, four 16-byte loads in
 // flight each, then four stores. The copy is HBM-bound: read + write of the
 // block bytes, nothing else.
@@ -64,17 +64,18 @@ block_copy_kernel(uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_s
 
 cudaError_t launch_block_copy(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
                               const int32_t *pairs, int32_t num_pairs, int64_t num_blocks,
-                              int n_kv, int d_h, bool int8, int32_t *dev_status,
+                              int n_kv, int d_h, int kind, int32_t *dev_status,
                               cudaStream_t stream)
 {
-    const int64_t tile_bytes = (int64_t)n_kv * 16 * d_h * (int8 ? 1 : 2);
+    // bytes of one block of one tensor: bf16 2, INT8 1, INT4 1/2 per element
+    const int64_t tile_bytes = (int64_t)n_kv * 16 * d_h * (kind == 0 ? 4 : kind == 1 ? 2 : 1) / 2;
     const int chunks = (int)((tile_bytes + kChunkBytes - 1) / kChunkBytes);
     const int64_t gx = (int64_t)num_pairs * chunks;
     if (gx > INT32_MAX)
         return cudaErrorInvalidValue;
     block_copy_kernel<<<dim3((unsigned)gx, 1, 2), kThreads, 0, stream>>>(
         static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), k_scale, v_scale, pairs,
-        num_blocks, tile_bytes, chunks, int8 ? n_kv * 16 : 0, dev_status);
+        num_blocks, tile_bytes, chunks, kind ? n_kv * 16 : 0, dev_status);
     return cudaGetLastError();
 }
 

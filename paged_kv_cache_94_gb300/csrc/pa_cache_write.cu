@@ -9,6 +9,8 @@
 //     scale = max|x| / 127,  code = clamp(round_half_even(x / scale), -128, 127).
 // The divisions are correctly rounded (__fdiv_rn), rintf rounds half to even,
 // and a row of zeros stores scale 0 with zero codes.
+// INT4 (same page, num_bits 4): scale = max|x| / 7, code = clamp(round(x /
+// scale), -8, 7), two codes per byte: element 2i in the low nibble of byte i.
 //
 // One warp handles one (token, head) row: lane l owns d = l*E .. l*E+E-1.
 #include <cuda_bf16.h>
@@ -68,7 +70,40 @@ __device__ __forceinline__ void quantize_store(const float (&x)[E], int8_t *dst_
         *dst_scale = scale;
 }
 
-template <int D, bool INT8>
+// INT4 codes of a row: lane l packs its E codes into E/2 bytes.
+template <int E>
+__device__ __forceinline__ void quantize_store4(const float (&x)[E], uint8_t *dst_codes,
+                                                float *dst_scale)
+{
+    float a = 0.f;
+#pragma unroll
+    for (int i = 0; i < E; ++i)
+        a = fmaxf(a, fabsf(x[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const float scale = __fdiv_rn(a, 7.0f);
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+        float c = 0.f;
+        if (scale != 0.f) {
+            c = rintf(__fdiv_rn(x[i], scale));
+            c = fminf(fmaxf(c, -8.0f), 7.0f);
+        }
+        packed |= ((uint32_t)(int)c & 0xFu) << (4 * i);
+    }
+    const int lane = threadIdx.x & 31;
+    if constexpr (E == 4)
+        reinterpret_cast<uint16_t *>(dst_codes)[lane] = (uint16_t)packed;
+    else
+        dst_codes[lane] = (uint8_t)packed;
+    if (lane == 0)
+        *dst_scale = scale;
+}
+
+// KIND: 0 bf16, 1 INT8, 2 INT4
+template <int D, int KIND>
 __global__ void __launch_bounds__(256)
     cache_write_kernel(const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
                        const int64_t *__restrict__ slots, int64_t rows, int n_kv, int64_t num_slots,
@@ -95,7 +130,7 @@ __global__ void __launch_bounds__(256)
     uint32_t rk[E / 2], rv[E / 2];
     load_row<E>(k + row * D + lane * E, xk, rk);
     load_row<E>(v + row * D + lane * E, xv, rv);
-    if constexpr (!INT8) {
+    if constexpr (KIND == 0) {
         __nv_bfloat16 *kc = static_cast<__nv_bfloat16 *>(k_cache) + dst_row * D + lane * E;
         __nv_bfloat16 *vc = static_cast<__nv_bfloat16 *>(v_cache) + dst_row * D + lane * E;
         if constexpr (E == 4) {
@@ -105,9 +140,14 @@ __global__ void __launch_bounds__(256)
             *reinterpret_cast<uint32_t *>(kc) = rk[0];
             *reinterpret_cast<uint32_t *>(vc) = rv[0];
         }
-    } else {
+    } else if constexpr (KIND == 1) {
         quantize_store<E>(xk, static_cast<int8_t *>(k_cache) + dst_row * D, k_scale + dst_row);
         quantize_store<E>(xv, static_cast<int8_t *>(v_cache) + dst_row * D, v_scale + dst_row);
+    } else {
+        quantize_store4<E>(xk, static_cast<uint8_t *>(k_cache) + dst_row * (D / 2),
+                           k_scale + dst_row);
+        quantize_store4<E>(xv, static_cast<uint8_t *>(v_cache) + dst_row * (D / 2),
+                           v_scale + dst_row);
     }
 }
 
@@ -154,7 +194,7 @@ cudaError_t launch_sink_write(const void *k, const void *v, const int32_t *seq_r
 }
 
 cudaError_t launch_cache_write(const void *k, const void *v, const int64_t *slots, int64_t T,
-                               int n_kv, int d_h, bool int8, int64_t num_slots, void *k_cache,
+                               int n_kv, int d_h, int kind, int64_t num_slots, void *k_cache,
                                void *v_cache, float *k_scale, float *v_scale, int32_t *dev_status,
                                cudaStream_t stream)
 {
@@ -165,16 +205,25 @@ cudaError_t launch_cache_write(const void *k, const void *v, const int64_t *slot
     const dim3 grid((unsigned)blocks), block(256);
     const __nv_bfloat16 *kb = static_cast<const __nv_bfloat16 *>(k);
     const __nv_bfloat16 *vb = static_cast<const __nv_bfloat16 *>(v);
-    if (d_h == 128 && !int8)
-        cache_write_kernel<128, false><<<grid, block, 0, stream>>>(kb, vb, slots, rows, n_kv, num_slots, k_cache, v_cache, k_scale, v_scale, dev_status);
-    else if (d_h == 128 && int8)
-        cache_write_kernel<128, true><<<grid, block, 0, stream>>>(kb, vb, slots, rows, n_kv, num_slots, k_cache, v_cache, k_scale, v_scale, dev_status);
-    else if (d_h == 64 && !int8)
-        cache_write_kernel<64, false><<<grid, block, 0, stream>>>(kb, vb, slots, rows, n_kv, num_slots, k_cache, v_cache, k_scale, v_scale, dev_status);
-    else if (d_h == 64 && int8)
-        cache_write_kernel<64, true><<<grid, block, 0, stream>>>(kb, vb, slots, rows, n_kv, num_slots, k_cache, v_cache, k_scale, v_scale, dev_status);
+#define PA_CW(D, K)                                                                           \
+    cache_write_kernel<D, K><<<grid, block, 0, stream>>>(kb, vb, slots, rows, n_kv, num_slots,    \
+                                                         k_cache, v_cache, k_scale, v_scale,     \
+                                                         dev_status)
+    if (d_h == 128 && kind == 0)
+        PA_CW(128, 0);
+    else if (d_h == 128 && kind == 1)
+        PA_CW(128, 1);
+    else if (d_h == 128 && kind == 2)
+        PA_CW(128, 2);
+    else if (d_h == 64 && kind == 0)
+        PA_CW(64, 0);
+    else if (d_h == 64 && kind == 1)
+        PA_CW(64, 1);
+    else if (d_h == 64 && kind == 2)
+        PA_CW(64, 2);
     else
         return cudaErrorInvalidValue;
+#undef PA_CW
     return cudaGetLastError();
 }
 

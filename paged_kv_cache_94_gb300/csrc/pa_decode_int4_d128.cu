@@ -1,0 +1,51 @@
+// Compiled decode kernels: int4 K/V, head dim 128, group sizes 1..16.
+#include "pa_decode_kernel.cuh"
+
+// Warps per CTA and ring stages per warp (overridable when building for a
+// tuning sweep).
+#ifndef PA_INT4_D128_NW
+#define PA_INT4_D128_NW 4
+#endif
+#ifndef PA_INT4_D128_STAGES
+#define PA_INT4_D128_STAGES 6
+#endif
+
+namespace pa {
+namespace {
+
+template <class Pol>
+size_t smem_of(int num_seqs)
+{
+    return Pol::Layout::bytes(num_seqs);
+}
+
+template <class Pol>
+cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
+                      size_t smem, cudaStream_t stream)
+{
+    decode_kernel<Pol><<<grid, Pol::NW * 32, smem, stream>>>(tk, tv, p);
+    return cudaGetLastError();
+}
+
+template <int G>
+using Pol = QuantMmaPolicy<4, 128, G, PA_INT4_D128_NW, PA_INT4_D128_STAGES>;
+
+template <int G>
+const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G>>),
+                             Pol<G>::NW * 32, &smem_of<Pol<G>>, &launch_of<Pol<G>>};
+
+} // namespace
+
+const DecodeKernel *find_decode_kernel_int4_d128(int group)
+{
+    switch (group) {
+    case 1: return &kEntry<1>;
+    case 2: return &kEntry<2>;
+    case 4: return &kEntry<4>;
+    case 8: return &kEntry<8>;
+    case 16: return &kEntry<16>;
+    default: return nullptr;
+    }
+}
+
+} // namespace pa

@@ -28,7 +28,7 @@ cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const Decode
 }
 
 template <int G>
-using Pol = Int8MmaPolicy<128, G, PA_INT8_D128_NW, PA_INT8_D128_STAGES>;
+using Pol = QuantMmaPolicy<8, 128, G, PA_INT8_D128_NW, PA_INT8_D128_STAGES>;
 
 template <int G>
 const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G>>),

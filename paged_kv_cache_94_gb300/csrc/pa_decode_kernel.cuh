@@ -7,11 +7,12 @@
 //              Tokens sit on the M side, so the query group only pads N to 8;
 //              P^T is moved from the accumulator layout to the B-operand
 //              layout with movmatrix.
-//  Int8MmaPolicy (pa_decode_int8.cuh): K/V tiles as int8 codes plus an
-//              fp32 scale per row ("kv-cache-guide" (guijiagi.com) §4.2,
-//              dequantize_kv: x = code * scale); codes become exact fp16
-//              values and both contractions run as mma.sync f16. The K scale
-//              multiplies the score, the V scale the softmax weight.
+//  QuantMmaPolicy (pa_decode_quant.cuh): K/V tiles as INT8 or packed INT4
+//              codes plus an fp32 scale per row ("kv-cache-guide"
+//              (guijiagi.com) §4.2, dequantize_kv: x = code * scale); codes
+//              become exact fp16 values and both contractions run as mma.sync
+//              f16. The K scale multiplies the score, the V scale the softmax
+//              weight.
 #pragma once
 
 #include "pa_decode.cuh"
@@ -40,7 +41,6 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 template <int D_, int GQ_, int NW_, int S_>
 struct Bf16Policy {
     static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_;
-    static constexpr bool kInt8 = false;
     static constexpr int NT = (GQ + 7) / 8;           // 8-head n-tiles
     static constexpr int KS = D / 16;                 // k-steps / m-tiles over D
     static constexpr int HALVES = D / 64;             // 64-column TMA boxes per tile
@@ -267,7 +267,7 @@ struct Bf16Policy {
 
 } // namespace pa
 
-#include "pa_decode_int8.cuh"
+#include "pa_decode_quant.cuh"
 
 namespace pa {
 

@@ -27,9 +27,10 @@ struct DecodeKernel {
 // NULL when the combination is not compiled.
 const DecodeKernel *find_decode_kernel_bf16(int d_h, int group);
 const DecodeKernel *find_decode_kernel_int8(int d_h, int group);
+const DecodeKernel *find_decode_kernel_int4(int d_h, int group);
 
 cudaError_t launch_cache_write(const void *k, const void *v, const int64_t *slots, int64_t T,
-                               int n_kv, int d_h, bool int8, int64_t num_slots, void *k_cache,
+                               int n_kv, int d_h, int kind, int64_t num_slots, void *k_cache,
                                void *v_cache, float *k_scale, float *v_scale, int32_t *dev_status,
                                cudaStream_t stream);
 
@@ -39,7 +40,7 @@ cudaError_t launch_sink_write(const void *k, const void *v, const int32_t *seq_r
 
 cudaError_t launch_block_copy(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
                               const int32_t *pairs, int32_t num_pairs, int64_t num_blocks,
-                              int n_kv, int d_h, bool int8, int32_t *dev_status,
+                              int n_kv, int d_h, int kind, int32_t *dev_status,
                               cudaStream_t stream);
 
 } // namespace pa

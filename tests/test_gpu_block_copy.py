@@ -26,8 +26,13 @@ def random_pool(seed, nb, n_kv, d_h, kv_dtype):
         k = torch.randn(shape, generator=gen).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
         v = torch.randn(shape, generator=gen).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
         return k, v, None, None
-    k = torch.randint(-128, 128, shape, generator=gen, dtype=torch.int8).numpy()
-    v = torch.randint(-128, 128, shape, generator=gen, dtype=torch.int8).numpy()
+    if kv_dtype == "int4":  # two codes per byte
+        shape = shape[:3] + (d_h // 2,)
+        k = torch.randint(0, 256, shape, generator=gen, dtype=torch.uint8).numpy()
+        v = torch.randint(0, 256, shape, generator=gen, dtype=torch.uint8).numpy()
+    else:
+        k = torch.randint(-128, 128, shape, generator=gen, dtype=torch.int8).numpy()
+        v = torch.randint(-128, 128, shape, generator=gen, dtype=torch.int8).numpy()
     ks = torch.rand(shape[:3], generator=gen).numpy().astype(np.float32)
     vs = torch.rand(shape[:3], generator=gen).numpy().astype(np.float32)
     return k, v, ks, vs
@@ -47,6 +52,8 @@ def to_device(k, v, ks, vs):
     ("bf16", 2, 64, 40, 7),
     ("int8", 32, 128, 300, 100),   # LLaMA-2-7B MHA layer: 64 KiB codes + 2 KiB scales
     ("int8", 1, 64, 16, 3),        # one 1 KiB tile, a partial chunk
+    ("int4", 8, 128, 200, 50),     # 8 KiB of packed codes per block and tensor
+    ("int4", 1, 64, 16, 3),        # one 512-byte tile
 ])
 def test_block_copy_bit_exact(kv_dtype, n_kv, d_h, nb, npairs):
     k, v, ks, vs = random_pool(11, nb, n_kv, d_h, kv_dtype)
@@ -58,7 +65,7 @@ def test_block_copy_bit_exact(kv_dtype, n_kv, d_h, nb, npairs):
     assert int(status.item()) == 0
     oracle_block_copy(k, v, pairs.tolist(), ks, vs)
     assert np.array_equal(pool_bits(kd), k) and np.array_equal(pool_bits(vd), v)
-    if kv_dtype == "int8":
+    if kv_dtype != "bf16":
         assert np.array_equal(ksd.cpu().numpy().view(np.uint32), ks.view(np.uint32))
         assert np.array_equal(vsd.cpu().numpy().view(np.uint32), vs.view(np.uint32))
 
@@ -85,7 +92,7 @@ def test_block_copy_empty_is_a_no_op():
     assert not kd.any()
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "int8"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "int8", "int4"])
 def test_decode_step_with_prefix_cache_fork_and_copy_on_write(kv_dtype):
     n_h, n_kv, d_h, NB, CAP = 8, 2, 128, 64, 12
     vocab = np.random.default_rng(21)
@@ -165,7 +172,7 @@ def test_decode_step_with_prefix_cache_fork_and_copy_on_write(kv_dtype):
     used = sorted({int(b) for i in range(B) for b in tables[i, :nblk[i]]})
     assert np.array_equal(pool_bits(kc)[used], opool.k[used])
     assert np.array_equal(pool_bits(vc)[used], opool.v[used])
-    if kv_dtype == "int8":
+    if kv_dtype != "bf16":
         assert np.array_equal(ksc.cpu().numpy()[used], opool.k_scale[used])
     # the four branches now differ only in their last token
     assert len({int(tables[i, nblk[i] - 1]) for i in range(4)}) == 4

@@ -29,7 +29,7 @@ def _check_pool_bitexact(w, pool, opool):
     kc, vc, ks, vs = pool
     np.testing.assert_array_equal(pool_bits(kc), opool.k)
     np.testing.assert_array_equal(pool_bits(vc), opool.v)
-    if w.geom.kv_dtype == "int8":
+    if w.geom.kv_dtype in ("int8", "int4"):
         np.testing.assert_array_equal(ks.cpu().numpy().view(np.uint32), opool.k_scale.view(np.uint32))
         np.testing.assert_array_equal(vs.cpu().numpy().view(np.uint32), opool.v_scale.view(np.uint32))
 
@@ -47,6 +47,12 @@ SMALL = [
     (32, 32, 128, "int8", [16, 33, 777]),
     (8, 4, 64, "int8", [3, 64, 129]),
     (16, 1, 128, "int8", [40, 200]),
+    (32, 8, 128, "int4", [1, 17, 500, 1300]),
+    (32, 32, 128, "int4", [16, 33, 777]),
+    (8, 4, 64, "int4", [3, 64, 129]),
+    (16, 1, 128, "int4", [40, 200]),
+    (8, 8, 64, "int4", [1, 31, 250]),
+    (32, 2, 64, "int4", [7, 90]),
     (8, 4, 128, "bf16", [0, 40, 0, 16]),
 ]
 
@@ -76,7 +82,7 @@ def test_tiny_config(dev):
     assert_close(out.float().cpu().numpy(), ref, "tiny")
 
 
-@pytest.mark.parametrize("dt", ["bf16", "int8"])
+@pytest.mark.parametrize("dt", ["bf16", "int8", "int4"])
 def test_split_count_invariance(dev, dt):
     w = make_workload("split", Geometry(32, 8, 128, kv_dtype=dt), [3000, 17, 1500, 4096], seed=77)
     pool = gpu_pool(w, dev)
@@ -110,7 +116,7 @@ def test_block_permutation_is_bit_identical(dev):
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
 
 
-@pytest.mark.parametrize("dt", ["bf16", "int8"])
+@pytest.mark.parametrize("dt", ["bf16", "int8", "int4"])
 def test_poisoned_pool(dev, dt):
     # unused slots and unused blocks hold NaN: never read, never propagated
     w = make_workload("nan", Geometry(32, 8, 128, kv_dtype=dt), [5, 17, 31, 250], seed=9,

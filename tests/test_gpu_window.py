@@ -74,7 +74,8 @@ def poison_before_window(w, pool, window):
                 vs[blk, :, off] = float("nan")
 
 
-GEOMS = [("bf16", 128, 4), ("bf16", 64, 2), ("int8", 128, 1), ("int8", 64, 8)]
+GEOMS = [("bf16", 128, 4), ("bf16", 64, 2), ("int8", 128, 1), ("int8", 64, 8), ("int4", 128, 4),
+         ("int4", 64, 1)]
 
 
 @pytest.mark.parametrize("kv_dtype,d_h,g", GEOMS)
@@ -107,11 +108,12 @@ def test_window_never_reads_entries_before_it():
     assert st == 0 and np.array_equal(out, base)
 
 
-@pytest.mark.parametrize("d_h,g", [(128, 1), (128, 4), (64, 8)])
+@pytest.mark.parametrize("kv_dtype,d_h,g", [("int8", 128, 1), ("int8", 128, 4), ("int8", 64, 8),
+                                            ("int4", 128, 8), ("int4", 64, 2)])
 @pytest.mark.parametrize("n_sink,window", [(4, 0), (4, 3), (16, 0), (4, 50), (1, 0)])
-def test_sink_rows_match_oracle(d_h, g, n_sink, window):
+def test_sink_rows_match_oracle(kv_dtype, d_h, g, n_sink, window):
     n_kv = 2
-    w = make_workload("sink", Geometry(n_h=n_kv * g, n_kv=n_kv, d_h=d_h, kv_dtype="int8"),
+    w = make_workload("sink", Geometry(n_h=n_kv * g, n_kv=n_kv, d_h=d_h, kv_dtype=kv_dtype),
                       [1, 2, 4, 5, 16, 21, 40, 200], seed=23)
     pool = gpu_pool(w, DEV, fill_nan=True)
     opool = oracle.pool_for(w, fill_nan=True)
@@ -139,7 +141,8 @@ def test_sink_rows_match_oracle(d_h, g, n_sink, window):
     for num_ctas in (0, 1, 7, 64):
         out, dst = run(w, pool, window=window, sink=(sk, sv), num_ctas=num_ctas)
         assert dst == 0
-        assert_close(out, ref, f"sink {n_sink} window {window} d{d_h} g{g} ctas {num_ctas}")
+        assert_close(out, ref, f"{kv_dtype} sink {n_sink} window {window} d{d_h} g{g} "
+                               f"ctas {num_ctas}")
 
 
 def test_decode_opt_argument_errors():

@@ -281,7 +281,7 @@ def make_workload(name: str, geom: Geometry, context_lens, seed: int,
 
 CONFIG_NAMES = ["tiny", "llama3_8b", "llama3_70b", "llama2_7b_int8_prefix", "long_context"]
 # further workloads of the variants built beside the decode step
-EXTRA_NAMES = ["mistral_7b_window"]
+EXTRA_NAMES = ["mistral_7b_window", "llama3_8b_int4"]
 
 
 def named_workload(name: str) -> Workload:
@@ -322,6 +322,14 @@ def named_workload(name: str) -> Workload:
             name, Geometry(n_h=32, n_kv=8, d_h=128), ctx, seed, window=4096,
             description="Mistral-7B layer, sliding window 4096: B=16, ctx U[16384,32768], "
                         "n_h=32, n_kv=8, d_h=128, bf16")
+    if name == "llama3_8b_int4":
+        # the Llama-3-8B step with an INT4 cache ("kv-cache-guide" §4.2, num_bits 4)
+        rng = np.random.default_rng(seed)
+        ctx = rng.integers(512, 4096, size=64, endpoint=True)
+        return make_workload(
+            name, Geometry(n_h=32, n_kv=8, d_h=128, kv_dtype="int4"), ctx, seed,
+            description="Llama-3-8B layer, INT4 KV: B=64, ctx U[512,4096], n_h=32, n_kv=8, "
+                        "d_h=128")
     if name == "long_context":
         return make_workload(
             name, Geometry(n_h=32, n_kv=8, d_h=128), [131072, 98304, 65536, 32768], seed,
