@@ -293,6 +293,8 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
 
     DecodeParams p;
     p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
     p.block_tables = block_tables;

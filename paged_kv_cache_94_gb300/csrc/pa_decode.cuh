@@ -45,6 +45,8 @@ struct DecodeParams {
     const __nv_bfloat16 *q;      // [B][n_h][D]
     const float *k_scale;        // INT8: [NB][n_kv][16]
     const float *v_scale;
+    const void *k_cache;         // pools (for LSU-loaded tiles; TMA uses the tensor maps)
+    const void *v_cache;
     const int32_t *block_tables; // [B][max_blocks]
     const int32_t *context_lens; // [B]
     __nv_bfloat16 *out;          // [B][n_h][D]

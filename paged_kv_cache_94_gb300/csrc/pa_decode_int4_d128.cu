@@ -1,10 +1,13 @@
 // Compiled decode kernels: int4 K/V, head dim 128, group sizes 1..16.
 #include "pa_decode_kernel.cuh"
 
-// Warps per CTA and ring stages per warp (overridable when building for a
-// tuning sweep).
+// Warps per CTA, ring stages per warp and the resident CTAs per SM the
+// register budget targets (overridable when building for a tuning sweep).
 #ifndef PA_INT4_D128_NW
 #define PA_INT4_D128_NW 4
+#endif
+#ifndef PA_INT4_D128_MINB
+#define PA_INT4_D128_MINB 1
 #endif
 #ifndef PA_INT4_D128_STAGES
 #define PA_INT4_D128_STAGES 6
@@ -28,7 +31,8 @@ cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const Decode
 }
 
 template <int G>
-using Pol = QuantMmaPolicy<4, 128, G, PA_INT4_D128_NW, PA_INT4_D128_STAGES>;
+using Pol = QuantMmaPolicy<4, 128, G, PA_INT4_D128_NW, PA_INT4_D128_STAGES,
+                           (G >= 16 ? 1 : PA_INT4_D128_MINB)>; // g = 16 needs its registers
 
 template <int G>
 const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G>>),

@@ -41,6 +41,9 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 template <int D_, int GQ_, int NW_, int S_>
 struct Bf16Policy {
     static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_;
+    static constexpr int kMinBlocks = 1;
+    static constexpr bool kLsuLoad = false;           // tiles arrive by TMA (lane 0 issues)
+    static constexpr uint32_t kArrivals = 1;
     static constexpr int NT = (GQ + 7) / 8;           // 8-head n-tiles
     static constexpr int KS = D / 16;                 // k-steps / m-tiles over D
     static constexpr int HALVES = D / 64;             // 64-column TMA boxes per tile
@@ -56,6 +59,11 @@ struct Bf16Policy {
         float m[NT][2], l[NT][2];
         float acc[NT][KS][4];   // O^T accumulators: rows d, cols heads
     };
+
+    __device__ static void issue_lanes(uint32_t, uint32_t, int32_t, const DecodeParams &,
+                                       const void *, const void *, uint64_t, int)
+    {
+    }
 
     __device__ static void issue(uint32_t dst, uint32_t /*extra*/, int32_t row, uint32_t bar,
                                  const CUtensorMap *tk, const CUtensorMap *tv,
@@ -275,7 +283,7 @@ namespace pa {
 // The kernel: split, ring, segments, merge.
 // ---------------------------------------------------------------------------
 template <class Pol>
-__global__ void __launch_bounds__(Pol::NW * 32)
+__global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p)
 {
@@ -314,7 +322,7 @@ __global__ void __launch_bounds__(Pol::NW * 32)
 
     if (lane == 0)
         for (int s = 0; s < S; ++s)
-            mbar_init(smem_u32(&bars[warp * S + s]), 1);
+            mbar_init(smem_u32(&bars[warp * S + s]), Pol::kArrivals);
     fence_barrier_init();
     __syncthreads();
 
@@ -348,7 +356,25 @@ __global__ void __launch_bounds__(Pol::NW * 32)
         }
         const int32_t phys = __shfl_sync(0xffffffffu, r.phys_cur, (int)(k & 31));
         const int32_t kvh = __shfl_sync(0xffffffffu, r.kvh_cur, (int)(k & 31));
-        if (lane == 0) {
+        if constexpr (Pol::kLsuLoad) {
+            // every lane copies its share and arrives when its copies land
+            const uint32_t bar = bar_base + 8u * istage;
+            const bool bad = phys < 0 || (int64_t)phys >= p.num_blocks;
+            const int32_t row = bad ? -1 : phys * p.n_kv + kvh;
+            if (lane == 0) {
+                wmeta[istage] = row;
+                if (bad)
+                    flag_error(p.dev_status, PA_DEV_BAD_BLOCK_BIT);
+            }
+            if (bad) {
+                mbar_arrive(bar); // the phase completes with no data: the item is skipped
+            } else {
+                Pol::issue_lanes(ring_base + (uint32_t)(istage * Pol::STAGE),
+                                 extra_base + (uint32_t)(istage * Pol::EXTRA), row, p, p.k_cache,
+                                 p.v_cache, pol, lane);
+                cp_async_mbar_arrive_noinc(bar);
+            }
+        } else if (lane == 0) {
             const uint32_t bar = bar_base + 8u * istage;
             const bool bad = phys < 0 || (int64_t)phys >= p.num_blocks;
             const int32_t row = bad ? -1 : phys * p.n_kv + kvh;
@@ -433,9 +459,12 @@ __global__ void __launch_bounds__(Pol::NW * 32)
 
     // After a timeout, give the copies still in flight a bounded chance to
     // land before the CTA's shared memory is released.
-    if (dead && lane == 0)
+    if constexpr (Pol::kLsuLoad) {
+        cp_async_wait_all(); // this thread's own copies: ends when they land
+    } else if (dead && lane == 0) {
         for (int64_t kk = fail_k; kk < r.issued; ++kk)
             mbar_wait(bar_base + 8u * (uint32_t)(kk % S), (uint32_t)((kk / S) & 1));
+    }
 }
 
 } // namespace pa

@@ -6,17 +6,21 @@
 // [-128, 127], 4-bit codes in [-8, 7] packed two per byte, low nibble first).
 // Every code is exact in fp16. A code c becomes fp16 by writing its
 // offset-binary form (c + 128, or c + 8) into the mantissa of 1024
-// (exponent bits 0x64): that half is 1024 + offset + c, and one subtraction
-// of 1024 + offset leaves c. Both contractions then run as mma.sync
-// m16n8k16 with fp16 inputs and fp32 accumulation:
+// (exponent bits 0x64): that half is B + c with B = 1152 (INT8) or 1032
+// (INT4). The bias is not subtracted per element: sum_d (B + c_d) q_d =
+// sum_d c_d q_d + B * sum_d q_d, so one correction per score with the
+// per-head sum of the fp16 query values removes it, and likewise
+// B * sum_tok w_tok per head for the weighted V sum (every product of two
+// fp16 values is exact in the fp32 accumulators). Both contractions run as
+// mma.sync m16n8k16 with fp16 inputs and fp32 accumulation:
 //   S^T[16 tok][8 heads] = Kcode[16 tok][D] . Q'^T[D][8 heads]
 //       (tokens on M; the k index is permuted so each thread's A fragments
 //        for all k-steps come from one 16-byte (or 8-byte) load of a row)
 //   s = S^T * 2^e * k_scale[tok] * scale * log2(e)
-//   O[16 heads][D] += W[16 heads][16 tok] . Vcode[16 tok][D]
-//       (heads on M; output columns are permuted so each thread's B
-//        fragments for all D/8 column tiles come from one load of each of
-//        its four token rows)
+//   O^T[D][8 heads] += Vcode^T[D][16 tok] . W^T[16 tok][8 heads]
+//       (d on M, so the query group only pads N to 8; the rows of O^T are
+//        permuted so each thread's A fragments for all D/16 row tiles come
+//        from one load of each of its four token rows)
 // Q' = q * 2^-e with e >= 0 chosen per (sequence, kv head) so that
 // max|Q'| < 2^15: the bf16 -> fp16 conversion is then exact for every
 // normal value. W = p * v_scale[tok] / s_base, where s_base is a running
@@ -30,15 +34,14 @@
 
 namespace pa {
 
-// Two int8 bytes (b0 low, b1 high, already XORed with 0x80) at byte positions
-// selected by SEL of `w` -> fp16x2 {code0, code1}.
+// Two int8 codes (bytes of `w` already XORed with 0x80, picked by SEL) ->
+// fp16x2 {1152 + code0, 1152 + code1}: the codes with a constant bias, which
+// the policy subtracts from the contraction's result instead of from every
+// element.
 template <uint32_t SEL>
 __device__ __forceinline__ uint32_t bytes_to_h2(uint32_t w)
 {
-    uint32_t h = __byte_perm(w, 0x64646464u, SEL);
-    uint32_t r;
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
-    return r;
+    return __byte_perm(w, 0x64646464u, SEL);
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
@@ -81,14 +84,20 @@ __device__ __forceinline__ float lds_f32(uint32_t addr)
     return v;
 }
 
-// Two 4-bit codes (offset form, nibbles j and j+4 of `w`) -> fp16x2 {code_j, code_j+4}.
+// Two 4-bit codes (offset form, nibbles j and j+4 of `w`) -> fp16x2
+// {1032 + code_j, 1032 + code_j+4} (biased as bytes_to_h2).
 template <int J>
 __device__ __forceinline__ uint32_t nibs_to_h2(uint32_t w)
 {
-    const uint32_t h = ((w >> (4 * J)) & 0x000F000Fu) | 0x64006400u;
-    uint32_t r;
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64086408u));
-    return r;
+    return ((w >> (4 * J)) & 0x000F000Fu) | 0x64006400u;
+}
+
+// fp32 values of the two halves of an fp16x2.
+__device__ __forceinline__ void h2_to_f2(uint32_t x, float &lo, float &hi)
+{
+    asm("{.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(x));
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr)
@@ -99,14 +108,14 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 }
 
 // ---------------------------------------------------------------------------
-template <int BITS, int D_, int GQ_, int NW_, int S_>
+template <int BITS, int D_, int GQ_, int NW_, int S_, int MINB_ = 1>
 struct QuantMmaPolicy {
     static_assert(BITS == 8 || BITS == 4, "INT8 or INT4 codes");
     static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_;
+    static constexpr int kMinBlocks = MINB_;       // resident CTAs per SM the registers allow
     static constexpr int NT = (GQ + 7) / 8;        // 8-head tiles of S^T
     static constexpr int KS = D / 16;              // k-steps of Q.K
-    static constexpr int VT = D / 8;               // column tiles of O
-    static constexpr int CW = D / 8;               // O columns per thread (see to_merge)
+    static constexpr int CW = D / 8;               // d values of O^T per thread (see to_merge)
     static constexpr int ROWB = D * BITS / 8;      // bytes per code row: 128/64 (8), 64/32 (4)
     static constexpr int TILE = kBlockTokens * ROWB; // bytes of a K (or V) code tile
     static constexpr int STAGE = 2 * TILE;
@@ -114,25 +123,59 @@ struct QuantMmaPolicy {
     static constexpr int QBYTES = 0;
     static constexpr uint32_t TX = STAGE + EXTRA;
     static constexpr float kScaleRatio = 64.f;     // V-scale base moves beyond this
+    static constexpr float kBias = BITS == 8 ? 1152.f : 1032.f; // fp16 value of code 0
     using Layout = SmemLayout<D, GQ, NW, S, STAGE, EXTRA, QBYTES>;
 
     struct State {
         uint32_t qf[NT][KS][2]; // Q'^T B-fragments (fp16, k permuted)
         float qexp;             // 2^e: Q' = q * 2^-e
         float m[NT][2], l[NT][2];
-        float acc[VT][4];       // O accumulators: rows heads gid / gid+8, cols permuted d
+        float acc[NT][KS][4];   // O^T accumulators: rows permuted d, cols heads
         float sbase;            // V-scale base of acc (0 until a nonzero scale is seen)
+        float sinv;             // 1 / sbase (0 while sbase is 0)
+        float qsum[NT][2];      // sum_d of the fp16 Q' values of head 2t4 + e
+        float wpart[NT][2];     // this lane's sum of the fp16 weights of head 2t4 + e
     };
 
-    __device__ static void issue(uint32_t dst, uint32_t extra, int32_t row, uint32_t bar,
-                                 const CUtensorMap *tk, const CUtensorMap *tv,
-                                 const DecodeParams &p, uint64_t pol)
+    // Tiles of 1-2 KiB move faster as 16-byte cp.async copies spread over the
+    // warp's lanes than as TMA boxes: every lane issues its share of the K
+    // and V tiles (and lanes 0-7 the 128 bytes of scales), then arrives on the
+    // stage barrier once its copies land (the barrier expects 32 arrivals).
+    static constexpr bool kLsuLoad = true;
+    static constexpr uint32_t kArrivals = 32;
+    static constexpr int CHUNKS = TILE / 16;       // 16-byte chunks per tile
+
+    // Shared-memory offset of chunk c of a tile: 16-byte chunk c % (ROWB/16)
+    // of row c / (ROWB/16), swizzled as the K/V readers expect.
+    __device__ static uint32_t chunk_off(int c)
     {
-        const int32_t y = row * kBlockTokens;
-        tma_load_2d(dst, tk, 0, y, bar, pol);
-        tma_load_2d(dst + TILE, tv, 0, y, bar, pol);
-        bulk_load_1d(extra, p.k_scale + (size_t)row * kBlockTokens, 64, bar, pol);
-        bulk_load_1d(extra + 64, p.v_scale + (size_t)row * kBlockTokens, 64, bar, pol);
+        constexpr int CPR = ROWB / 16;
+        if constexpr (BITS == 8)
+            return swz<ROWB>(c / CPR, c % CPR);
+        else
+            return (uint32_t)(c * 16);
+    }
+
+    __device__ static void issue_lanes(uint32_t dst, uint32_t extra, int32_t row,
+                                       const DecodeParams &p, const void *kc, const void *vc,
+                                       uint64_t pol, int lane)
+    {
+        const uint8_t *ks = static_cast<const uint8_t *>(kc) + (size_t)row * TILE;
+        const uint8_t *vs = static_cast<const uint8_t *>(vc) + (size_t)row * TILE;
+#pragma unroll
+        for (int c = lane; c < CHUNKS; c += 32) {
+            cp_async_16(dst + chunk_off(c), ks + 16 * c, pol);
+            cp_async_16(dst + TILE + chunk_off(c), vs + 16 * c, pol);
+        }
+        if (lane < 8) {
+            const float *sc = (lane < 4 ? p.k_scale : p.v_scale) + (size_t)row * kBlockTokens;
+            cp_async_16(extra + 16 * lane, sc + 4 * (lane & 3), pol);
+        }
+    }
+
+    __device__ static void issue(uint32_t, uint32_t, int32_t, uint32_t, const CUtensorMap *,
+                                 const CUtensorMap *, const DecodeParams &, uint64_t)
+    {
     }
 
     // Physical d of the k values thread t holds in k-step kk; the A and B
@@ -204,12 +247,26 @@ struct QuantMmaPolicy {
         st.qexp = __uint_as_float((uint32_t)(127 + e) << 23);
         const float down = __uint_as_float((uint32_t)(127 - e) << 23);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt) {
+            float part = 0.f; // sum of this thread's fp16 values of head nt*8 + gid
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
                 st.qf[nt][kk][0] = pack_f16x2(qv[nt][kk][0] * down, qv[nt][kk][1] * down);
                 st.qf[nt][kk][1] = pack_f16x2(qv[nt][kk][2] * down, qv[nt][kk][3] * down);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    float lo, hi;
+                    h2_to_f2(st.qf[nt][kk][r], lo, hi);
+                    part += lo + hi;
+                }
             }
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            // score columns are heads 2t4 + e: their sums sit in lanes 4 (2t4 + e)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                st.qsum[nt][e] = __shfl_sync(0xffffffffu, part, 4 * (2 * t4 + e));
+        }
     }
 
     __device__ static void reset(State &st)
@@ -222,11 +279,19 @@ struct QuantMmaPolicy {
                 st.l[nt][e] = 0.f;
             }
 #pragma unroll
-        for (int vt = 0; vt < VT; ++vt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                st.acc[vt][e] = 0.f;
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    st.acc[nt][mt][e] = 0.f;
         st.sbase = 0.f;
+        st.sinv = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                st.wpart[nt][e] = 0.f;
     }
 
     // One 16-token block: K codes at kt, V codes at kt + TILE, scales at extra
@@ -297,90 +362,105 @@ struct QuantMmaPolicy {
         const float f_lo = st.qexp * lds_f32(extra + 4 * gid) * scale_log2;
         const float f_hi = st.qexp * lds_f32(extra + 4 * (gid + 8)) * scale_log2;
         float pr[NT][4];
-        float alpha[NT][2];
-        bool need = false;
+        bool need = false; // some lane's score exceeds its column's base by 2^kRescaleLog2
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            pr[nt][0] = lo_ok ? (s0[nt][0] + s1[nt][0]) * f_lo : -INFINITY;
-            pr[nt][1] = lo_ok ? (s0[nt][1] + s1[nt][1]) * f_lo : -INFINITY;
-            pr[nt][2] = hi_ok ? (s0[nt][2] + s1[nt][2]) * f_hi : -INFINITY;
-            pr[nt][3] = hi_ok ? (s0[nt][3] + s1[nt][3]) * f_hi : -INFINITY;
-            // lazy rescale of the softmax base (as in the bf16 policy)
+            // S^T element c: token row gid (c < 2) or gid+8, head column 2t4 + (c & 1)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                float mx = fmaxf(pr[nt][e], pr[nt][e + 2]);
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const bool up = mx > st.m[nt][e] + kRescaleLog2;
-                const float mnew = up ? mx : st.m[nt][e];
-                alpha[nt][e] = up ? fast_exp2(st.m[nt][e] - mnew) : 1.f;
-                need |= up;
-                st.m[nt][e] = mnew;
-                const float base = (mnew == -INFINITY) ? 0.f : mnew;
-                pr[nt][e] = fast_exp2(pr[nt][e] - base);
-                pr[nt][e + 2] = fast_exp2(pr[nt][e + 2] - base);
+            for (int c = 0; c < 4; ++c) {
+                const float sb = s0[nt][c] + s1[nt][c];
+                const float sc = fmaf(-kBias, st.qsum[nt][c & 1], sb) * ((c & 2) ? f_hi : f_lo);
+                pr[nt][c] = ((c & 2) ? hi_ok : lo_ok) ? sc : -INFINITY;
             }
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                need |= fmaxf(pr[nt][e], pr[nt][e + 2]) > st.m[nt][e] + kRescaleLog2;
         }
+        // Lazy rescale (as in the bf16 policy), and the column maxima are only
+        // reduced across the lanes when some lane exceeds its base.
         if (__any_sync(0xffffffffu, need)) {
-            // O rows are heads gid and gid+8; head h's factor lives in lane
-            // (h & 7) >> 1 of S^T tile h >> 3, slot h & 1
-            const float a00 = __shfl_sync(0xffffffffu, alpha[0][0], gid >> 1);
-            const float a01 = __shfl_sync(0xffffffffu, alpha[0][1], gid >> 1);
-            const float al_lo = (gid & 1) ? a01 : a00;
-            float al_hi = 1.f;
-            if constexpr (NT > 1) {
-                const float a10 = __shfl_sync(0xffffffffu, alpha[1][0], gid >> 1);
-                const float a11 = __shfl_sync(0xffffffffu, alpha[1][1], gid >> 1);
-                al_hi = (gid & 1) ? a11 : a10;
-            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int e = 0; e < 2; ++e)
-                    st.l[nt][e] *= alpha[nt][e];
+                for (int e = 0; e < 2; ++e) {
+                    float mx = fmaxf(pr[nt][e], pr[nt][e + 2]);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    if (mx > st.m[nt][e] + kRescaleLog2) { // same in every lane of the column
+                        const float alpha = fast_exp2(st.m[nt][e] - mx);
+                        st.m[nt][e] = mx;
+                        st.l[nt][e] *= alpha;
+                        st.wpart[nt][e] *= alpha;
 #pragma unroll
-            for (int v = 0; v < VT; ++v) {
-                st.acc[v][0] *= al_lo;
-                st.acc[v][1] *= al_lo;
-                st.acc[v][2] *= al_hi;
-                st.acc[v][3] *= al_hi;
-            }
+                        for (int mt = 0; mt < KS; ++mt) {
+                            st.acc[nt][mt][e] *= alpha;
+                            st.acc[nt][mt][e + 2] *= alpha;
+                        }
+                    }
+                }
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
+            for (int e = 0; e < 2; ++e) {
+                const float base = (st.m[nt][e] == -INFINITY) ? 0.f : st.m[nt][e];
+                pr[nt][e] = fast_exp2(pr[nt][e] - base);
+                pr[nt][e + 2] = fast_exp2(pr[nt][e + 2] - base);
                 st.l[nt][e] += pr[nt][e] + pr[nt][e + 2];
+            }
 
-        // ---- V scales: fold sv / s_base into the weights
+        // ---- V scales: fold sv / s_base into the weights; the base moves only
+        // when some row's scale exceeds it kScaleRatio-fold (then to the max)
         const float sv_lo = lo_ok ? lds_f32(extra + 64 + 4 * gid) : 0.f;
         const float sv_hi = hi_ok ? lds_f32(extra + 64 + 4 * (gid + 8)) : 0.f;
-        float svm = fmaxf(sv_lo, sv_hi);
-        svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, 4));
-        svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, 8));
-        svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, 16));
-        if (svm > st.sbase * kScaleRatio) { // warp-uniform: svm is the same in all lanes
+        if (__any_sync(0xffffffffu, fmaxf(sv_lo, sv_hi) > st.sbase * kScaleRatio)) {
+            float svm = fmaxf(sv_lo, sv_hi);
+            svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, 4));
+            svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, 8));
+            svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, 16));
+            svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, 1));
+            svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, 2));
             const float f = st.sbase / svm;
 #pragma unroll
-            for (int v = 0; v < VT; ++v)
+            for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    st.acc[v][e] *= f;
+                for (int e = 0; e < 2; ++e)
+                    st.wpart[nt][e] *= f;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        st.acc[nt][mt][e] *= f;
+            }
             st.sbase = svm;
+            st.sinv = 1.f / svm;
         }
-        const float inv = st.sbase > 0.f ? 1.f / st.sbase : 0.f;
-        const float r_lo = sv_lo * inv, r_hi = sv_hi * inv;
-        uint32_t pa[NT][2];
+        const float r_lo = sv_lo * st.sinv, r_hi = sv_hi * st.sinv;
+        // W^T as B fragments (tokens x heads): transpose of the score layout.
+        // The lane's weights, as rounded to fp16, join its bias sums.
+        uint32_t pb0[NT], pb1[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            pa[nt][0] = movmatrix_trans(pack_f16x2(pr[nt][0] * r_lo, pr[nt][1] * r_lo));
-            pa[nt][1] = movmatrix_trans(pack_f16x2(pr[nt][2] * r_hi, pr[nt][3] * r_hi));
+            const uint32_t w0 = pack_f16x2(pr[nt][0] * r_lo, pr[nt][1] * r_lo);
+            const uint32_t w1 = pack_f16x2(pr[nt][2] * r_hi, pr[nt][3] * r_hi);
+            float a, b, c, d;
+            h2_to_f2(w0, a, b);
+            h2_to_f2(w1, c, d);
+            st.wpart[nt][0] += a + c;
+            st.wpart[nt][1] += b + d;
+            pb0[nt] = movmatrix_trans(w0);
+            pb1[nt] = movmatrix_trans(w1);
         }
-        const uint32_t a0 = pa[0][0], a2 = pa[0][1];
-        const uint32_t a1 = NT > 1 ? pa[NT - 1][0] : 0u, a3 = NT > 1 ? pa[NT - 1][1] : 0u;
+        auto pv = [&](int mt, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma_f16_16816(st.acc[nt][mt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+        };
 
-        // ---- O += W . Vcode; thread rows 2t, 2t+1, 2t+8, 2t+9, columns CW*gid + nt
+        // ---- O^T += Vcode^T . W^T. Thread rows (tokens) 2t, 2t+1, 2t+8, 2t+9;
+        // its d values are CW*gid + 2*mt + r for row tile mt, r = 0 (A rows
+        // gid) or 1 (A rows gid+8): CW contiguous codes of each token row.
         if constexpr (BITS == 8) {
             constexpr int WPR = D / 32; // 32-bit words per thread per row
             uint32_t ra[WPR], rb[WPR], rc[WPR], rd[WPR];
@@ -406,21 +486,19 @@ struct QuantMmaPolicy {
             }
 #pragma unroll
             for (int i = 0; i < WPR; ++i) {
+                // word i holds d values 4i..4i+3: row tiles 2i (bytes 0, 1), 2i+1 (bytes 2, 3)
                 const uint32_t A = ra[i] ^ 0x80808080u, B = rb[i] ^ 0x80808080u;
                 const uint32_t C = rc[i] ^ 0x80808080u, E = rd[i] ^ 0x80808080u;
                 const uint32_t ab_lo = __byte_perm(A, B, 0x5140), ab_hi = __byte_perm(A, B, 0x7362);
                 const uint32_t ce_lo = __byte_perm(C, E, 0x5140), ce_hi = __byte_perm(C, E, 0x7362);
-                mma_f16_16816(st.acc[4 * i + 0], a0, a1, a2, a3, bytes_to_h2<0x4140>(ab_lo),
-                              bytes_to_h2<0x4140>(ce_lo));
-                mma_f16_16816(st.acc[4 * i + 1], a0, a1, a2, a3, bytes_to_h2<0x4342>(ab_lo),
-                              bytes_to_h2<0x4342>(ce_lo));
-                mma_f16_16816(st.acc[4 * i + 2], a0, a1, a2, a3, bytes_to_h2<0x4140>(ab_hi),
-                              bytes_to_h2<0x4140>(ce_hi));
-                mma_f16_16816(st.acc[4 * i + 3], a0, a1, a2, a3, bytes_to_h2<0x4342>(ab_hi),
-                              bytes_to_h2<0x4342>(ce_hi));
+                pv(2 * i, bytes_to_h2<0x4140>(ab_lo), bytes_to_h2<0x4342>(ab_lo),
+                   bytes_to_h2<0x4140>(ce_lo), bytes_to_h2<0x4342>(ce_lo));
+                pv(2 * i + 1, bytes_to_h2<0x4140>(ab_hi), bytes_to_h2<0x4342>(ab_hi),
+                   bytes_to_h2<0x4140>(ce_hi), bytes_to_h2<0x4342>(ce_hi));
             }
         } else {
-            // CW/2 bytes per row: byte k of word wi holds columns 8wi+2k (low nibble), +1
+            // CW/2 bytes per row; byte k of word i holds d values 8i+2k (low
+            // nibble) and 8i+2k+1 (high nibble): row tile 4i+k
             constexpr int WPR = CW / 8;
             uint32_t ra[WPR], rb[WPR], rc[WPR], rd[WPR];
             if constexpr (D == 128) {
@@ -444,13 +522,11 @@ struct QuantMmaPolicy {
                 const uint32_t C = rc[i] ^ 0x88888888u, E = rd[i] ^ 0x88888888u;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    // bytes {A_k, A_k, B_k, B_k}: nibble pairs (row 2t, row 2t+1) of one column
+                    // bytes {A_k, A_k, B_k, B_k}: nibble pairs (row 2t, row 2t+1) of one d
                     const uint32_t sel = k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12);
                     const uint32_t Y = __byte_perm(A, B, sel), Z = __byte_perm(C, E, sel);
-                    mma_f16_16816(st.acc[8 * i + 2 * k], a0, a1, a2, a3, nibs_to_h2<0>(Y),
-                                  nibs_to_h2<0>(Z));
-                    mma_f16_16816(st.acc[8 * i + 2 * k + 1], a0, a1, a2, a3, nibs_to_h2<1>(Y),
-                                  nibs_to_h2<1>(Z));
+                    pv(4 * i + k, nibs_to_h2<0>(Y), nibs_to_h2<1>(Y), nibs_to_h2<0>(Z),
+                       nibs_to_h2<1>(Z));
                 }
             }
         }
@@ -476,18 +552,28 @@ struct QuantMmaPolicy {
                     mb[1] = l;
                 }
             }
+        // acc[nt][mt][e]: row gid (e < 2) or gid+8 (e >= 2) of row tile mt is
+        // d = CW*gid + 2*mt + (e >> 1); column 2t4 + (e & 1) is the head. The
+        // codes' bias contributed kBias * (sum of the head's weights) to every d.
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int h = gid + 8 * half;
-            if (h < GQ) {
-                float *mb = merge + (warp * GQ + h) * (D + 2) + 2;
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int v = 0; v < VT; ++v) {
-                    mb[CW * (2 * t4) + v] = st.acc[v][2 * half] * st.sbase;
-                    mb[CW * (2 * t4 + 1) + v] = st.acc[v][2 * half + 1] * st.sbase;
+            for (int c = 0; c < 2; ++c) {
+                float ws = st.wpart[nt][c];
+                ws += __shfl_xor_sync(0xffffffffu, ws, 4);
+                ws += __shfl_xor_sync(0xffffffffu, ws, 8);
+                ws += __shfl_xor_sync(0xffffffffu, ws, 16);
+                const float bias = kBias * ws;
+                const int h = nt * 8 + 2 * t4 + c;
+                if (h < GQ) {
+                    float *mb = merge + (warp * GQ + h) * (D + 2) + 2 + CW * gid;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        mb[2 * mt] = (st.acc[nt][mt][c] - bias) * st.sbase;
+                        mb[2 * mt + 1] = (st.acc[nt][mt][c + 2] - bias) * st.sbase;
+                    }
                 }
             }
-        }
     }
 };
 

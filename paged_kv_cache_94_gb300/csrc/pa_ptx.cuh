@@ -102,6 +102,27 @@ __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint
                  : "memory");
 }
 
+// ------------------------------------------------------------- cp.async (LSU)
+// 16-byte global -> shared copy through the load/store path (L1 bypassed).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint64_t policy)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst),
+                 "l"(src), "l"(policy)
+                 : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (counts as one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
