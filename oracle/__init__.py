@@ -72,6 +72,9 @@ def _load():
         lib.oracle_decode.restype = ctypes.c_int
         lib.oracle_decode.argtypes = [P, P, P, P, P, i32, P, i32, P, i32, i32, i32, i32, i32, i64,
                                       dbl, P]
+        lib.oracle_decode_mq.restype = ctypes.c_int
+        lib.oracle_decode_mq.argtypes = [P, P, P, P, P, i32, P, i32, P, i32, i32, i32, i32, i32,
+                                         i32, i64, dbl, P]
         lib.oracle_decode_window.restype = ctypes.c_int
         lib.oracle_decode_window.argtypes = [P, P, P, P, P, i32, P, i32, P, i32, i32, i32, i32,
                                              i32, i64, dbl, i32, i32, P, P, P]
@@ -208,6 +211,24 @@ def decode_window(q_bits: np.ndarray, pool: Pool, block_tables: np.ndarray,
                                   _ptr(bt), bt.shape[1], _ptr(ctx), B, n_h, pool.n_kv, pool.d_h,
                                   pool.block_size, pool.num_blocks, float(scale), int(window),
                                   int(n_sink), _ptr(sink_k_bits), _ptr(sink_v_bits), _ptr(out))
+    return out, st
+
+
+def decode_mq(q_bits: np.ndarray, pool: Pool, block_tables: np.ndarray,
+              context_lens: np.ndarray, n_h: int, scale: float) -> tuple[np.ndarray, int]:
+    """Multi-query decode: q [B, n_q, n_h, d_h] (bf16 bits), the last n_q
+    positions of each sequence attending causally. float64 [B, n_q, n_h, d_h]."""
+    lib = _load()
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, n_q = q_bits.shape[:2]
+    assert q_bits.shape == (B, n_q, n_h, pool.d_h) and ctx.shape == (B,)
+    out = np.zeros(q_bits.shape, dtype=np.float64)
+    st = lib.oracle_decode_mq(_ptr(q_bits), _ptr(pool.k), _ptr(pool.v), _ptr(pool.k_scale),
+                              _ptr(pool.v_scale), KV_KIND[pool.kv_dtype], _ptr(bt), bt.shape[1],
+                              _ptr(ctx), B, n_q, n_h, pool.n_kv, pool.d_h, pool.block_size,
+                              pool.num_blocks, float(scale), _ptr(out))
     return out, st
 
 

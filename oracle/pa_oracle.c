@@ -13,6 +13,7 @@
  *  [G] "kv-cache-guide" (guijiagi.com)
  *  [T] "KV Cache 显存管理全景：内存碎片拟合推导、vLLM PagedAttention 虚拟内存与
  *      Prefix Caching" (talentme.airsota.com)
+ *  [E] "LLM 推理引擎设计：KV Cache、PagedAttention 与连续批处理" (hx.sn.cn)
  *
  * Floating point: attention runs in double precision. The INT8 quantiser runs
  * in IEEE single precision (the scales it produces are fp32 numbers, so the
@@ -432,6 +433,88 @@ int oracle_decode_window(const uint16_t *q, const void *k_cache, const void *v_c
                 } else {
                     int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + j / block_size];
                     int64_t row = (blk * n_kv + kvh) * block_size + j % block_size;
+                    for (int d = 0; d < d_h; ++d)
+                        o[d] += w * cached_elem(v_cache, v_scale, kv_kind, row, d, d_h);
+                }
+            }
+        }
+    }
+    free(scores);
+    return status;
+}
+
+/* ------------------------------------------------------------------------
+ * Multi-query decode: n_q new tokens per sequence attend at once, as in
+ * speculative verification (a draft of k tokens checked in one step, [E]
+ * §6 "投机解码") or a chunk of a chunked prefill ([F] "Chunked Prefill"). The
+ * n_q new tokens of sequence b are its last n_q positions ctx_b - n_q ..
+ * ctx_b - 1 (their K/V already appended); query i (0-based) attends causally
+ * to positions [0, ctx_b - n_q + i], i.e. every earlier token and itself.
+ * A query whose range is empty (ctx_b < n_q - i) gets a zero output.
+ *   q   [B][n_q][n_h][d_h] bf16 bits,  out [B][n_q][n_h][d_h] double.
+ * Per query the arithmetic is oracle_decode's: scores, max-subtracted
+ * softmax, weighted V sum, in double precision.
+ * ---------------------------------------------------------------------- */
+int oracle_decode_mq(const uint16_t *q, const void *k_cache, const void *v_cache,
+                     const float *k_scale, const float *v_scale, int kv_kind,
+                     const int32_t *block_tables, int max_blocks_per_seq,
+                     const int32_t *context_lens, int B, int n_q, int n_h, int n_kv, int d_h,
+                     int block_size, int64_t num_blocks, double scale, double *out)
+{
+    int status = 0;
+    int g = n_h / n_kv;
+    double *scores = NULL;
+    int64_t cap = 0;
+    for (int b = 0; b < B; ++b) {
+        int64_t ctx = context_lens[b];
+        int bad = 0;
+        if (ctx < 0 || ctx > (int64_t)max_blocks_per_seq * block_size) {
+            status |= ORC_BAD_CTX;
+            bad = 1;
+        }
+        for (int64_t i = 0; !bad && i * block_size < ctx; ++i) {
+            int32_t blk = block_tables[(int64_t)b * max_blocks_per_seq + i];
+            if (blk < 0 || blk >= num_blocks) {
+                status |= ORC_BAD_BLOCK;
+                bad = 1;
+            }
+        }
+        if (ctx > cap) {
+            free(scores);
+            cap = ctx;
+            scores = (double *)malloc(sizeof(double) * (size_t)cap);
+        }
+        for (int i = 0; i < n_q; ++i) {
+            int64_t n = bad ? 0 : ctx - n_q + i + 1; /* attended positions 0 .. n-1 */
+            for (int h = 0; h < n_h; ++h) {
+                double *o = out + (((int64_t)b * n_q + i) * n_h + h) * d_h;
+                for (int d = 0; d < d_h; ++d)
+                    o[d] = 0.0;
+                if (n <= 0)
+                    continue;
+                int kvh = h / g;
+                const uint16_t *qh = q + (((int64_t)b * n_q + i) * n_h + h) * d_h;
+                double m = -INFINITY;
+                for (int64_t j = 0; j < n; ++j) {
+                    int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + j / block_size];
+                    int64_t row = (blk * n_kv + kvh) * block_size + j % block_size;
+                    double dot = 0.0;
+                    for (int d = 0; d < d_h; ++d)
+                        dot += (double)bf16_bits_to_float(qh[d]) *
+                               cached_elem(k_cache, k_scale, kv_kind, row, d, d_h);
+                    scores[j] = dot * scale;
+                    if (scores[j] > m)
+                        m = scores[j];
+                }
+                double denom = 0.0;
+                for (int64_t j = 0; j < n; ++j) {
+                    scores[j] = exp(scores[j] - m);
+                    denom += scores[j];
+                }
+                for (int64_t j = 0; j < n; ++j) {
+                    int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + j / block_size];
+                    int64_t row = (blk * n_kv + kvh) * block_size + j % block_size;
+                    double w = scores[j] / denom;
                     for (int d = 0; d < d_h; ++d)
                         o[d] += w * cached_elem(v_cache, v_scale, kv_kind, row, d, d_h);
                 }
