@@ -103,16 +103,16 @@ def decode_bytes(w, unique_blocks: bool = True) -> dict:
     else:
         tok = tok_logical
     blocks = sum(len(span(b)[2]) for b in range(w.B))
-    other = 4 * blocks + 4 * w.B + 2 * 2 * w.B * g.n_h * g.d_h
+    other = 4 * blocks + 4 * w.B + 2 * 2 * w.B * w.n_q * g.n_h * g.d_h
     return {"bytes": tok * per_token + other, "logical_bytes": tok_logical * per_token + other,
-            "flops": 4 * g.n_h * g.d_h * tok_logical}
+            "flops": 4 * g.n_h * g.d_h * tok_logical * w.n_q}
 
 
 def cache_write_bytes(w) -> int:
     """Bytes of one pa_cache_write of B new tokens: read k, v and slots, write rows."""
     g = w.geom
-    rows = w.B * g.n_kv
-    read = 2 * rows * g.d_h * 2 + 8 * w.B
+    rows = w.B * w.n_q * g.n_kv
+    read = 2 * rows * g.d_h * 2 + 8 * w.B * w.n_q
     write = 2 * rows * g.d_h * kv_bits_per_elem(w) // 8 + 2 * rows * scale_bytes_per_row(w)
     return read + write
 
@@ -227,14 +227,17 @@ def oracle_sample(w, gen_device, seconds: float):
         pool.write(oracle.bf16_bits(k), oracle.bf16_bits(v), np.arange(ctx))
         table = np.arange(nblk, dtype=np.int32)[None]
         t0 = time.perf_counter()
-        if w.window:
+        if w.n_q > 1:
+            oracle.decode_mq(q_all[b:b + 1], pool, table, np.array([ctx], np.int32), g.n_h,
+                             w.scale)
+        elif w.window:
             oracle.decode_window(q_all[b:b + 1], pool, table, np.array([ctx], np.int32), g.n_h,
                                  w.scale, window=w.window)
         else:
             oracle.decode(q_all[b:b + 1], pool, table, np.array([ctx], np.int32), g.n_h, w.scale)
         spent += time.perf_counter() - t0
         lo = max(0, ctx - w.window) if w.window else 0
-        done_bytes += (ctx - lo) * per_token + 4 * (nblk - lo // 16) + 4 + 4 * g.n_h * g.d_h
+        done_bytes += (ctx - lo) * per_token + 4 * (nblk - lo // 16) + 4 + 4 * w.n_q * g.n_h * g.d_h
         seqs.append(b)
         if spent >= seconds:
             break
@@ -267,14 +270,22 @@ def run_native(args, rank, world, local_rank):
     cl = torch.from_numpy(w.context_lens).to(dev)
     out = torch.empty_like(q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws = pa.decode_workspace(pa.geometry(kc, g.n_h), w.B, dev, args.num_ctas)
+    ws = pa.decode_workspace(pa.geometry(kc, g.n_h), w.B, dev, args.num_ctas, n_q=w.n_q)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize(dev)
 
+    def attend(q_, bt_, cl_):
+        if w.n_q > 1:  # multi-query step: the n_q new tokens of each sequence at once
+            pa.pa_decode_mq(q_, kc, vc, bt_, cl_, w.scale, out=out, workspace=ws,
+                            dev_status=status)
+        else:
+            pa.pa_decode(q_, kc, vc, bt_, cl_, w.scale, out=out, k_scale=ks, v_scale=vs,
+                         workspace=ws, dev_status=status, num_ctas=args.num_ctas,
+                         window=w.window)
+
     def step():
         pa.pa_cache_write(kn, vn, slots_new, kc, vc, ks, vs, dev_status=status)
-        pa.pa_decode(q, kc, vc, bt, cl, w.scale, out=out, k_scale=ks, v_scale=vs, workspace=ws,
-                     dev_status=status, num_ctas=args.num_ctas, window=w.window)
+        attend(q, bt, cl)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -294,8 +305,7 @@ def run_native(args, rank, world, local_rank):
         ev[i][0].record(stream)
         pa.pa_cache_write(kn, vn, slots_new, kc, vc, ks, vs, dev_status=status)
         ev[i][1].record(stream)
-        pa.pa_decode(q, kc, vc, bt, cl, w.scale, out=out, k_scale=ks, v_scale=vs, workspace=ws,
-                     dev_status=status, num_ctas=args.num_ctas, window=w.window)
+        attend(q, bt, cl)
         ev[i][2].record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
@@ -361,8 +371,7 @@ def run_native(args, rank, world, local_rank):
             for d, h in ((dq, hq), (dk, hk), (dv, hv), (ds, hs), (dbt, hbt), (dcl, hcl)):
                 d.copy_(h, non_blocking=True)
             pa.pa_cache_write(dk, dv, ds, kc, vc, ks, vs, dev_status=status)
-            pa.pa_decode(dq, kc, vc, dbt, dcl, w.scale, out=out, k_scale=ks, v_scale=vs,
-                         workspace=ws, dev_status=status, window=w.window)
+            attend(dq, dbt, dcl)
             hout.copy_(out, non_blocking=True)
 
         for _ in range(args.warmup):

@@ -15,6 +15,7 @@
  *  [G] "kv-cache-guide" (guijiagi.com)
  *  [T] "KV Cache 显存管理全景：内存碎片拟合推导、vLLM PagedAttention 虚拟内存与
  *      Prefix Caching" (talentme.airsota.com)
+ *  [E] "LLM 推理引擎设计：KV Cache、PagedAttention 与连续批处理" (hx.sn.cn)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -253,6 +254,34 @@ pa_status pa_decode_opt(const void *q, const void *k_cache, const void *v_cache,
                         int32_t num_seqs, float scale, void *out, void *workspace,
                         size_t workspace_bytes, pa_geom geom, const pa_decode_opts *opts,
                         int32_t *dev_status, void *stream);
+
+/*
+ * pa_decode_mq -- multi-query decode: n_q new tokens per sequence attend in
+ * one pass, as when a target model verifies a k-token draft ([E] §6
+ * "投机解码": the large model checks the draft tokens in one parallel
+ * forward) or processes one chunk of a chunked prefill ([F] "Chunked
+ * Prefill"). The n_q tokens of sequence b are its last n_q positions
+ * ctx_b - n_q .. ctx_b - 1 (their K/V already written with pa_cache_write);
+ * new token i attends causally to positions 0 .. ctx_b - n_q + i. A token
+ * whose range is empty (ctx_b < n_q - i) gets a zero output.
+ *
+ *   q    bf16 [num_seqs][n_q][n_h][d_h]; out the same shape
+ *   n_q  1 (pa_decode), or 2, 4, 8 with g * n_q <= 16; bf16 pools only
+ *        (PA_ERR_UNSUPPORTED otherwise)
+ * Every other argument is pa_decode's. All n_q * g query rows of a kv head
+ * read each K/V tile once: the bytes moved are those of one decode step.
+ * The workspace is pa_decode_mq_workspace_size(geom, num_seqs, n_q, 0).
+ */
+pa_status pa_decode_mq(const void *q, const void *k_cache, const void *v_cache,
+                       const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                       int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                       int32_t n_q, float scale, void *out, void *workspace,
+                       size_t workspace_bytes, pa_geom geom, int32_t *dev_status, void *stream);
+
+/* Workspace bytes pa_decode_mq needs (num_ctas 0: the default grid); 0 when
+ * the geometry or n_q is not supported. */
+size_t pa_decode_mq_workspace_size(pa_geom geom, int32_t num_seqs, int32_t n_q,
+                                   int32_t num_ctas);
 
 /*
  * pa_sink_write -- store bf16 attention-sink rows of new tokens.

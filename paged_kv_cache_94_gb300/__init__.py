@@ -44,6 +44,7 @@ PA_ERR_STATE = -13
 EXPORTED = ["pa_cache_write", "pa_decode_workspace_size", "pa_decode_workspace_init",
             "pa_decode", "pa_decode_ex", "pa_decode_noalloc", "pa_decode_default_ctas",
             "pa_plan_owner", "pa_block_copy", "pa_decode_opt", "pa_sink_write",
+            "pa_decode_mq", "pa_decode_mq_workspace_size",
             "pa_status_string", "pa_status_from_device", "pa_version",
             # host block manager (include/pa_alloc.h)
             "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate_prompt",
@@ -114,6 +115,11 @@ def _lib():
         lib.pa_status_from_device.argtypes = [i32]
         lib.pa_version.restype = i32
         lib.pa_version.argtypes = []
+        lib.pa_decode_mq.restype = ctypes.c_int
+        lib.pa_decode_mq.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, f32, P, P, sz, pa_geom,
+                                     P, P]
+        lib.pa_decode_mq_workspace_size.restype = sz
+        lib.pa_decode_mq_workspace_size.argtypes = [pa_geom, i32, i32, i32]
         lib.pa_decode_opt.restype = ctypes.c_int
         lib.pa_decode_opt.argtypes = dec[:14] + [P] + dec[14:]
         lib.pa_sink_write.restype = ctypes.c_int
@@ -231,7 +237,7 @@ def _counter_bytes(g: pa_geom, num_seqs: int) -> int:
 
 
 def decode_workspace(g: pa_geom, num_seqs: int, device: torch.device, num_ctas: int = 0,
-                     stream=None) -> torch.Tensor:
+                     stream=None, n_q: int = 1) -> torch.Tensor:
     """A workspace for pa_decode, cached per device.
 
     Its leading counter area must be zero on entry; pa_decode leaves it zero,
@@ -239,12 +245,15 @@ def decode_workspace(g: pa_geom, num_seqs: int, device: torch.device, num_ctas: 
     than the buffer has had zeroed so far.
     """
     key = device.index if device.index is not None else torch.cuda.current_device()
-    size_key = (key, g.num_blocks, g.n_h, g.n_kv, g.d_h, g.kv_dtype, num_seqs, num_ctas)
+    size_key = (key, g.num_blocks, g.n_h, g.n_kv, g.d_h, g.kv_dtype, num_seqs, num_ctas, n_q)
     nbytes = _WS_SIZES.get(size_key)
     if nbytes is None:
-        nbytes = _lib().pa_decode_workspace_size(g, num_seqs, num_ctas)
+        if n_q == 1:
+            nbytes = _lib().pa_decode_workspace_size(g, num_seqs, num_ctas)
+        else:
+            nbytes = _lib().pa_decode_mq_workspace_size(g, num_seqs, n_q, num_ctas)
         if nbytes == 0:
-            raise PAError(-2, "pa_decode_workspace_size")
+            raise PAError(-4 if n_q > 1 else -2, "pa_decode_workspace_size")
         _WS_SIZES[size_key] = nbytes
     need_zero = _counter_bytes(g, num_seqs)
     with _WS_LOCK:
@@ -330,6 +339,45 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     else:
         st = lib.pa_decode(*args)
     _check(st, "pa_decode")
+    return out
+
+
+def pa_decode_mq(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                 out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                 dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Multi-query decode: q [B, n_q, n_h, d_h] bf16 (the last n_q tokens of each
+    sequence, attending causally) over a bf16 pool -> out of q's shape."""
+    _need_cuda("q", q, torch.bfloat16)
+    _need_cuda("k_cache", k_cache, torch.bfloat16)
+    _need_cuda("v_cache", v_cache, torch.bfloat16)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    if q.dim() != 4:
+        raise ValueError("q must be [num_seqs, n_q, n_h, d_h]")
+    B, n_q, n_h, d = q.shape
+    g = geometry(k_cache, n_h)
+    if d != g.d_h or block_tables.dim() != 2 or block_tables.shape[0] != B or \
+            context_lens.shape != (B,):
+        raise ValueError("q, block_tables, context_lens disagree on num_seqs or d_h")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, torch.bfloat16)
+        if out.shape != q.shape:
+            raise ValueError("out must have the shape of q")
+    if workspace is None:
+        workspace = decode_workspace(g, B, q.device, 0, stream, n_q=n_q)
+    else:
+        _need_cuda("workspace", workspace)
+    if dev_status is not None:
+        _need_cuda("dev_status", dev_status, torch.int32)
+    st = _lib().pa_decode_mq(_ptr(q), _ptr(k_cache), _ptr(v_cache), None, None,
+                             _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B,
+                             n_q, float(scale), _ptr(out), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), g, _ptr(dev_status),
+                             _stream_ptr(stream))
+    _check(st, "pa_decode_mq")
     return out
 
 

@@ -41,9 +41,11 @@ pa_status check_geom(const pa_geom &g)
     return PA_OK;
 }
 
-const DecodeKernel *kernel_for(const pa_geom &g)
+const DecodeKernel *kernel_for(const pa_geom &g, int nq = 1)
 {
     const int gq = group_of(g);
+    if (nq != 1)
+        return g.kv_dtype == PA_KV_BF16 ? pa::find_decode_kernel_bf16_mq(g.d_h, gq, nq) : nullptr;
     return g.kv_dtype == PA_KV_INT8   ? pa::find_decode_kernel_int8(g.d_h, gq)
            : g.kv_dtype == PA_KV_INT4 ? pa::find_decode_kernel_int4(g.d_h, gq)
                                       : pa::find_decode_kernel_bf16(g.d_h, gq);
@@ -125,9 +127,9 @@ pa_status ctas_per_sm(const DecodeKernel *kd, size_t smem, int &n)
     return PA_OK;
 }
 
-pa_status default_ctas(const pa_geom &g, int num_seqs, int &grid)
+pa_status default_ctas(const pa_geom &g, int num_seqs, int &grid, int nq = 1)
 {
-    const DecodeKernel *kd = kernel_for(g);
+    const DecodeKernel *kd = kernel_for(g, nq);
     if (!kd)
         return PA_ERR_UNSUPPORTED;
     int dev, sms, per;
@@ -143,10 +145,10 @@ pa_status default_ctas(const pa_geom &g, int num_seqs, int &grid)
 
 size_t counters_bytes(int64_t units) { return (size_t)((units * 4 + 255) / 256 * 256); }
 
-size_t workspace_bytes_for(const pa_geom &g, int num_seqs, int grid)
+size_t workspace_bytes_for(const pa_geom &g, int num_seqs, int grid, int nq = 1)
 {
     const int64_t units = (int64_t)num_seqs * g.n_kv;
-    const int64_t rec = (int64_t)group_of(g) * (g.d_h + 2) * 4;
+    const int64_t rec = (int64_t)group_of(g) * nq * (g.d_h + 2) * 4;
     return counters_bytes(units) + (size_t)((grid + units) * rec);
 }
 
@@ -240,7 +242,8 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
                       const float *v_scale, const int32_t *block_tables, int32_t max_blocks,
                       const int32_t *context_lens, int32_t num_seqs, float scale, void *out,
                       void *workspace, size_t workspace_bytes, pa_geom g, int32_t *dev_status,
-                      void *stream, int32_t num_ctas, const pa_decode_opts *opts = nullptr)
+                      void *stream, int32_t num_ctas, const pa_decode_opts *opts = nullptr,
+                      int nq = 1)
 {
     pa_status st = check_geom(g);
     if (st != PA_OK)
@@ -274,7 +277,7 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
         !aligned(workspace, 256) || (i8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16))))
         return PA_ERR_ALIGNMENT;
 
-    const DecodeKernel *kd = kernel_for(g);
+    const DecodeKernel *kd = kernel_for(g, nq);
     if (!kd)
         return PA_ERR_UNSUPPORTED;
     int dev, sms, per;
@@ -284,7 +287,7 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     if ((st = ctas_per_sm(kd, smem, per)) != PA_OK)
         return st;
     const int grid = num_ctas > 0 ? num_ctas : sms * per;
-    if (workspace_bytes < workspace_bytes_for(g, num_seqs, grid))
+    if (workspace_bytes < workspace_bytes_for(g, num_seqs, grid, nq))
         return PA_ERR_WORKSPACE;
 
     CUtensorMap tk, tv;
@@ -463,6 +466,31 @@ pa_status pa_decode_opt(const void *q, const void *k_cache, const void *v_cache,
     return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
                        context_lens, num_seqs, scale, out, workspace, workspace_bytes, geom,
                        dev_status, stream, opts ? opts->num_ctas : 0, opts);
+}
+
+size_t pa_decode_mq_workspace_size(pa_geom geom, int32_t num_seqs, int32_t n_q,
+                                   int32_t num_ctas)
+{
+    if (check_geom(geom) != PA_OK || num_seqs < 0 || num_seqs > kMaxSeqs || num_ctas < 0 ||
+        n_q < 1 || !kernel_for(geom, n_q))
+        return 0;
+    int grid = num_ctas;
+    if (grid == 0 && default_ctas(geom, num_seqs, grid, n_q) != PA_OK)
+        return 0;
+    return workspace_bytes_for(geom, num_seqs, grid, n_q);
+}
+
+pa_status pa_decode_mq(const void *q, const void *k_cache, const void *v_cache,
+                       const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                       int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                       int32_t n_q, float scale, void *out, void *workspace,
+                       size_t workspace_bytes, pa_geom geom, int32_t *dev_status, void *stream)
+{
+    if (n_q < 1)
+        return PA_ERR_SHAPE;
+    return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, scale, out, workspace, workspace_bytes, geom,
+                       dev_status, stream, 0, nullptr, n_q);
 }
 
 pa_status pa_sink_write(const void *k, const void *v, const int32_t *seq_rows,

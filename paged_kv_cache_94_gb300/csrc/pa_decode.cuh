@@ -65,6 +65,18 @@ struct DecodeParams {
     const __nv_bfloat16 *sink_v;
 };
 
+// Row of query row v of (sequence b, kv head kvh) in q and out, laid out
+// [B][NQ][n_h][D]: the GQ = G * NQ query rows of a kv head are its G query
+// heads for each of the NQ new tokens (v = i * G + h). NQ = 1 is the plain
+// single-token decode, [B][n_h][D].
+template <int GQ, int NQ>
+__device__ __forceinline__ size_t qo_row(const DecodeParams &p, int b, int kvh, int v)
+{
+    constexpr int G = GQ / NQ;
+    const int i = v / G, h = v - i * G;
+    return ((size_t)(b * NQ + i) * p.n_kv + kvh) * G + h;
+}
+
 // First position a sequence attends: max(0, ctx - window) under a window.
 __device__ __forceinline__ int32_t window_start(const DecodeParams &p, int32_t ctx)
 {
@@ -178,16 +190,17 @@ __device__ __forceinline__ void locate_item(int64_t x, const int32_t *P, int num
     i = (int)(r - (int64_t)kvh * nb);
 }
 
-// Zero the output rows of sequences with no blocks (ctx == 0 or invalid).
-template <int D>
+// Zero the output rows of sequences with no blocks (ctx == 0 or invalid);
+// each sequence has NQ * n_h rows.
+template <int D, int NQ>
 __device__ __forceinline__ void zero_empty_sequences(const DecodeParams &p, const int32_t *P,
                                                      int n_h)
 {
-    const int rows16 = n_h * D * 2 / 16; // 16-byte chunks per sequence
+    const int rows16 = NQ * n_h * D * 2 / 16; // 16-byte chunks per sequence
     for (int b = blockIdx.x; b < p.num_seqs; b += p.num_ctas) {
         if (P[b + 1] != P[b])
             continue;
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (size_t)b * n_h * D);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (size_t)b * NQ * n_h * D);
         for (int i = threadIdx.x; i < rows16; i += blockDim.x)
             dst[i] = make_uint4(0, 0, 0, 0);
     }
@@ -216,20 +229,20 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t *addr, int v)
 // Scores (log2 domain) of the bf16 sink rows [s_lo, s_hi) of (b, kvh) for
 // the GQ heads: sc[h * 16 + j - s_lo]. One warp per (head, row) pair, lanes
 // over d. Called by all threads; ends with a CTA barrier.
-template <int D, int GQ, int NW>
+template <int D, int GQ, int NW, int NQ>
 __device__ __forceinline__ void sink_scores(const DecodeParams &p, int b, int kvh, int s_lo,
                                             int s_hi, float *sc)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ns = s_hi - s_lo;
-    const __nv_bfloat16 *q = p.q + ((size_t)b * p.n_kv * GQ + (size_t)kvh * GQ) * D;
     const __nv_bfloat16 *k = p.sink_k + ((size_t)b * p.n_kv + kvh) * p.n_sink * D;
     for (int t = warp; t < GQ * ns; t += NW) {
         const int h = t / ns, j = s_lo + t % ns;
+        const __nv_bfloat16 *q = p.q + qo_row<GQ, NQ>(p, b, kvh, h) * D;
         float a = 0.f;
 #pragma unroll
         for (int d = lane; d < D; d += 32)
-            a = fmaf(__bfloat162float(q[h * D + d]), __bfloat162float(k[j * D + d]), a);
+            a = fmaf(__bfloat162float(q[d]), __bfloat162float(k[j * D + d]), a);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             a += __shfl_xor_sync(0xffffffffu, a, o);
@@ -239,7 +252,7 @@ __device__ __forceinline__ void sink_scores(const DecodeParams &p, int b, int kv
     __syncthreads();
 }
 
-template <int D, int GQ, int NW>
+template <int D, int GQ, int NW, int NQ>
 __device__ __forceinline__ void finish_segment(const DecodeParams &p, const float *merge,
                                                int32_t *misc, float *sink_sc, int b, int kvh,
                                                int64_t unit_start, int nb, int64_t W, int64_t G,
@@ -247,15 +260,13 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const floa
 {
     constexpr int NT = NW * 32;
     constexpr int REC = D + 2;
-    const int n_h = p.n_kv * GQ;
     const int u = b * p.n_kv + kvh;
-    __nv_bfloat16 *out = p.out + ((size_t)b * n_h + (size_t)kvh * GQ) * D;
     float *rec = p.partials + ((size_t)blockIdx.x + u) * (GQ * REC);
     // Sink rows [s_lo, s_hi) join this segment's merge as one more partial
     // state (the segment that holds the sequence's first block has them).
     const int ns = s_hi - s_lo;
     if (ns > 0)
-        sink_scores<D, GQ, NW>(p, b, kvh, s_lo, s_hi, sink_sc);
+        sink_scores<D, GQ, NW, NQ>(p, b, kvh, s_lo, s_hi, sink_sc);
     const __nv_bfloat16 *sv = p.sink_v + ((size_t)b * p.n_kv + kvh) * p.n_sink * D;
 
 #pragma unroll 1
@@ -285,7 +296,7 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const floa
             }
         }
         if (whole) {
-            out[h * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+            p.out[qo_row<GQ, NQ>(p, b, kvh, h) * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
         } else {
             if (d == 0) {
                 rec[h * REC] = M;
@@ -345,7 +356,7 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const floa
                 }
             }
         }
-        out[h * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+        p.out[qo_row<GQ, NQ>(p, b, kvh, h) * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
     }
 }
 

@@ -30,6 +30,25 @@ namespace pa {
 // than this (log2 units): softmax weights stay <= 2^8 between rescales.
 constexpr float kRescaleLog2 = 8.0f;
 
+// Multi-query causal mask on one 16x8 score tile (rows: tokens gid, gid+8 of
+// the block; columns: query rows nt*8 + 2*t4 + e). Query row v belongs to new
+// token i = v / (GQ/NQ), which sees the block's first rem - (NQ-1-i) tokens,
+// rem = ctx - (the block's first position), not clamped to the block.
+template <int GQ, int NQ>
+__device__ __forceinline__ void causal_mask(float (&sc)[4], int nt, int gid, int t4, int rem)
+{
+    constexpr int G = GQ / NQ;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int i = (nt * 8 + 2 * t4 + e) / G;
+        const int vis = rem - (NQ - 1 - i);
+        if (gid >= vis)
+            sc[e] = -INFINITY;
+        if (gid + 8 >= vis)
+            sc[e + 2] = -INFINITY;
+    }
+}
+
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -38,9 +57,11 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 // ---------------------------------------------------------------------------
 // bf16 K/V, tensor-core contractions.
 // ---------------------------------------------------------------------------
-template <int D_, int GQ_, int NW_, int S_>
+// GQ query rows share each K/V tile: the g query heads of a kv head for each
+// of NQ new tokens (NQ > 1: multi-query decode, each token masked causally).
+template <int D_, int GQ_, int NW_, int S_, int NQ_ = 1>
 struct Bf16Policy {
-    static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_;
+    static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_, NQ = NQ_;
     static constexpr int kMinBlocks = 1;
     static constexpr bool kLsuLoad = false;           // tiles arrive by TMA (lane 0 issues)
     static constexpr uint32_t kArrivals = 1;
@@ -82,13 +103,12 @@ struct Bf16Policy {
                                   float * /*qsm*/)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
-        const int n_h = p.n_kv * GQ;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int hl = nt * 8 + gid;
             const bool ok = hl < GQ;
             const uint32_t *row = reinterpret_cast<const uint32_t *>(
-                p.q + ((size_t)b * n_h + (size_t)kvh * GQ + (ok ? hl : 0)) * D);
+                p.q + qo_row<GQ, NQ>(p, b, kvh, ok ? hl : 0) * D);
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
                 st.qf[nt][kk][0] = ok ? __ldg(row + kk * 8 + t4) : 0u;
@@ -115,9 +135,10 @@ struct Bf16Policy {
     }
 
     // One 16-token block: K tile at kt, V tile at kt + TILE (shared addresses).
-    // Rows [lo, valid) of the block are attended; the others are masked.
+    // Rows [lo, valid) of the block are attended; the others are masked. rem =
+    // ctx - the block's first position (the multi-query causal limit).
     __device__ static void compute(State &st, uint32_t kt, uint32_t /*extra*/, int lo, int valid,
-                                   float scale_log2)
+                                   int rem, float scale_log2)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
         const int mi = lane >> 3, rr = lane & 7;
@@ -164,6 +185,8 @@ struct Bf16Policy {
                 sc[2] = -INFINITY;
                 sc[3] = -INFINITY;
             }
+            if constexpr (NQ > 1)
+                causal_mask<GQ, NQ>(sc, nt, gid, t4, rem);
             // Lazy rescale: the running base m only moves when a tile's max
             // exceeds it by more than 2^kRescaleLog2; otherwise weights up to
             // 2^kRescaleLog2 are accumulated against the old base (exact: acc
@@ -301,7 +324,7 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     int32_t *P = reinterpret_cast<int32_t *>(smem + L::kOffPrefix);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n_h = p.n_kv * GQ;
+    const int n_h = p.n_kv * (GQ / Pol::NQ); // query heads per token
 
     if (tid == 0) {
         prefetch_tensormap(&tmK);
@@ -309,7 +332,7 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     }
     prefix_blocks<NW * 32>(p, P, misc + 8);
     __syncthreads();
-    zero_empty_sequences<D>(p, P, n_h);
+    zero_empty_sequences<D, Pol::NQ>(p, P, n_h);
     const int64_t W = (int64_t)p.n_kv * P[p.num_seqs];
     // At most one CTA per item: then every CTA owns at least one item, and the
     // CTAs owning a (sequence, kv head) are exactly plan_owner(first) ..
@@ -434,9 +457,10 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
             if (ok && wmeta[cstage] >= 0) {
                 const int32_t t0 = (fb + (int32_t)(x - unit_start)) * kBlockTokens;
                 const int lo = pool_from > t0 ? (int)min(pool_from - t0, kBlockTokens) : 0;
-                const int valid = (int)min(ctx - t0, kBlockTokens);
+                const int rem = (int)min(ctx - t0, 2 * kBlockTokens); // >= 16 + NQ - 1
+                const int valid = (int)min(rem, kBlockTokens);
                 Pol::compute(st, ring_base + (uint32_t)(cstage * Pol::STAGE),
-                             extra_base + (uint32_t)(cstage * Pol::EXTRA), lo, valid,
+                             extra_base + (uint32_t)(cstage * Pol::EXTRA), lo, valid, rem,
                              p.scale_log2);
             }
             __syncwarp();
@@ -452,8 +476,8 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         Pol::to_merge(st, merge);
         __syncthreads();
         const int32_t s_hi = (i0 == 0 && p.n_sink > ws) ? min(p.n_sink, ctx) : 0;
-        finish_segment<D, GQ, NW>(p, merge, misc, sink_sc, b, kvh, unit_start, nb, W, G, whole,
-                                  ws, s_hi > ws ? s_hi : ws);
+        finish_segment<D, GQ, NW, Pol::NQ>(p, merge, misc, sink_sc, b, kvh, unit_start, nb, W, G,
+                                           whole, ws, s_hi > ws ? s_hi : ws);
         seg_lo = seg_hi;
     }
 

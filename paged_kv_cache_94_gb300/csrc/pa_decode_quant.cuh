@@ -111,7 +111,7 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 template <int BITS, int D_, int GQ_, int NW_, int S_, int MINB_ = 1>
 struct QuantMmaPolicy {
     static_assert(BITS == 8 || BITS == 4, "INT8 or INT4 codes");
-    static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_;
+    static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_, NQ = 1;
     static constexpr int kMinBlocks = MINB_;       // resident CTAs per SM the registers allow
     static constexpr int NT = (GQ + 7) / 8;        // 8-head tiles of S^T
     static constexpr int KS = D / 16;              // k-steps of Q.K
@@ -190,15 +190,13 @@ struct QuantMmaPolicy {
                                   float * /*qsm*/)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
-        const int n_h = p.n_kv * GQ;
         float qv[NT][KS][4]; // per k-step: register 0 (lo, hi), register 1 (lo, hi)
         float mx = 0.f;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int hl = nt * 8 + gid;
             const bool ok = hl < GQ;
-            const __nv_bfloat16 *row =
-                p.q + ((size_t)b * n_h + (size_t)kvh * GQ + (ok ? hl : 0)) * D;
+            const __nv_bfloat16 *row = p.q + qo_row<GQ, NQ>(p, b, kvh, ok ? hl : 0) * D;
             if constexpr (BITS == 8) {
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
@@ -297,7 +295,7 @@ struct QuantMmaPolicy {
     // One 16-token block: K codes at kt, V codes at kt + TILE, scales at extra
     // (16 K scales, then 16 V scales). Rows [lo, valid) are attended.
     __device__ static void compute(State &st, uint32_t kt, uint32_t extra, int lo, int valid,
-                                   float scale_log2)
+                                   int /*rem*/, float scale_log2)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
         const uint32_t vt = kt + TILE;

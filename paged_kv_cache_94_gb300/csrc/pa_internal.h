@@ -28,6 +28,8 @@ struct DecodeKernel {
 const DecodeKernel *find_decode_kernel_bf16(int d_h, int group);
 const DecodeKernel *find_decode_kernel_int8(int d_h, int group);
 const DecodeKernel *find_decode_kernel_int4(int d_h, int group);
+// Multi-query (nq new tokens per sequence) bf16 kernels; NULL when not compiled.
+const DecodeKernel *find_decode_kernel_bf16_mq(int d_h, int group, int nq);
 
 cudaError_t launch_cache_write(const void *k, const void *v, const int64_t *slots, int64_t T,
                                int n_kv, int d_h, int kind, int64_t num_slots, void *k_cache,

@@ -70,6 +70,7 @@ class Workload:
     group: np.ndarray                 # int32 [B]: shared-prefix group id (-1 = none)
     description: str = ""
     window: int = 0                   # > 0: the step attends the last `window` tokens only
+    n_q: int = 1                      # new tokens per sequence (> 1: multi-query step)
     # streams are generated lazily; cache of (stream id) -> (k, v) on a device
     _cache: dict = field(default_factory=dict, repr=False)
 
@@ -119,10 +120,14 @@ class Workload:
         return torch.cat(ks, 0), torch.cat(vs, 0)
 
     def q(self, device="cpu") -> torch.Tensor:
-        """Query rows of the step: bf16 [B, n_h, d_h]."""
+        """Query rows of the step: bf16 [B, n_h, d_h], or [B, n_q, n_h, d_h]
+        for a multi-query step."""
         gen = torch.Generator(device=device)
         gen.manual_seed(self._stream_seed(2_000_000))
-        x = torch.randn((self.B, self.geom.n_h, self.geom.d_h), generator=gen, device=device)
+        shape = (self.B, self.geom.n_h, self.geom.d_h)
+        if self.n_q > 1:
+            shape = (self.B, self.n_q) + shape[1:]
+        x = torch.randn(shape, generator=gen, device=device)
         return x.to(torch.bfloat16)
 
     # ------------------------------------------------------------------ slots
@@ -137,29 +142,31 @@ class Workload:
         return self.block_tables[b, pos // bs].astype(np.int64) * bs + pos % bs
 
     def new_token_slots(self) -> np.ndarray:
-        """int64 [B]: slot of each sequence's new token (position ctx-1); -1 for an
-        empty sequence (a padding row the append skips)."""
-        return np.array([self.slot_of(b, np.array([self.context_lens[b] - 1]))[0]
-                         if self.context_lens[b] > 0 else -1
-                         for b in range(self.B)], dtype=np.int64)
+        """int64 [B * n_q]: slots of each sequence's new tokens (positions
+        ctx-n_q .. ctx-1, sequence-major); -1 for a position < 0 (a padding row
+        the append skips)."""
+        out = []
+        for b in range(self.B):
+            ctx = int(self.context_lens[b])
+            for pos in range(ctx - self.n_q, ctx):
+                out.append(self.slot_of(b, np.array([pos]))[0] if pos >= 0 else -1)
+        return np.array(out, dtype=np.int64)
 
     def new_kv(self, device="cpu") -> tuple[torch.Tensor, torch.Tensor]:
-        """K/V rows of the new token of every sequence: bf16 [B, n_kv, d_h]
-        (zeros for an empty sequence)."""
+        """K/V rows of the new tokens of every sequence: bf16 [B * n_q, n_kv, d_h]
+        (zeros where the position is < 0)."""
         ks, vs = [], []
+        z = torch.zeros((self.geom.n_kv, self.geom.d_h), dtype=torch.bfloat16, device=device)
         for b in range(self.B):
             ctx = int(self.context_lens[b])
             p = int(self.prefix_len[b])
-            if ctx == 0:
-                z = torch.zeros((self.geom.n_kv, self.geom.d_h), dtype=torch.bfloat16,
-                                device=device)
-                ks.append(z)
-                vs.append(z)
-                continue
-            assert ctx - 1 >= p, "new token must be private to its sequence"
-            ko, vo = self._gen_rows(b, ctx - p, device)
-            ks.append(ko[-1])
-            vs.append(vo[-1])
+            ko = vo = None
+            if ctx > 0:
+                assert max(ctx - self.n_q, 0) >= p, "new tokens must be private to their sequence"
+                ko, vo = self._gen_rows(b, ctx - p, device)
+            for pos in range(ctx - self.n_q, ctx):
+                ks.append(ko[pos - p] if pos >= 0 else z)
+                vs.append(vo[pos - p] if pos >= 0 else z)
         return torch.stack(ks), torch.stack(vs)
 
     def history_chunks(self, device="cpu", max_rows: int = 1 << 20,
@@ -167,7 +174,7 @@ class Workload:
                        ) -> Iterator[tuple[torch.Tensor, torch.Tensor, np.ndarray]]:
         """Yield (k, v, slots) covering every history position exactly once.
 
-        History = positions 0..ctx-2 of each sequence. A shared prefix is
+        History = positions 0..ctx-1-n_q of each sequence. A shared prefix is
         yielded once, by the first sequence of its group. ``seqs`` restricts the
         output to those sequences (their shared prefix included).
         """
@@ -181,11 +188,11 @@ class Workload:
                 done_groups.add(grp)
                 k, v = self._gen_rows(self._prefix_stream(grp), p, device)
                 yield from self._chunk(k, v, self.slot_of(b, np.arange(p)), max_rows)
-            n_priv = ctx - 1 - p
+            n_priv = ctx - self.n_q - p
             if n_priv > 0:
                 k, v = self._gen_rows(b, ctx - p, device)
                 yield from self._chunk(k[:n_priv], v[:n_priv],
-                                       self.slot_of(b, np.arange(p, ctx - 1)), max_rows)
+                                       self.slot_of(b, np.arange(p, ctx - self.n_q)), max_rows)
 
     @staticmethod
     def _chunk(k, v, slots, max_rows):
@@ -240,7 +247,7 @@ def make_workload(name: str, geom: Geometry, context_lens, seed: int,
                   pool_factor: float = 1.1, num_blocks: Optional[int] = None,
                   prefix_len=None, group=None, scale: Optional[float] = None,
                   extra_table_cols: int = 0, description: str = "",
-                  window: int = 0) -> Workload:
+                  window: int = 0, n_q: int = 1) -> Workload:
     """Build a workload from explicit context lengths.
 
     pool_factor: the physical pool holds ceil(pool_factor * blocks needed) blocks
@@ -272,7 +279,7 @@ def make_workload(name: str, geom: Geometry, context_lens, seed: int,
         scale = 1.0 / math.sqrt(geom.d_h)
     return Workload(name=name, geom=geom, seed=seed, context_lens=ctx, block_tables=tables,
                     num_blocks=int(num_blocks), scale=float(scale), prefix_len=pl, group=gr,
-                    description=description, window=int(window))
+                    description=description, window=int(window), n_q=int(n_q))
 
 
 # ---------------------------------------------------------------------------
@@ -281,7 +288,7 @@ def make_workload(name: str, geom: Geometry, context_lens, seed: int,
 
 CONFIG_NAMES = ["tiny", "llama3_8b", "llama3_70b", "llama2_7b_int8_prefix", "long_context"]
 # further workloads of the variants built beside the decode step
-EXTRA_NAMES = ["mistral_7b_window", "llama3_8b_int4"]
+EXTRA_NAMES = ["mistral_7b_window", "llama3_8b_int4", "llama3_8b_spec4"]
 
 
 def named_workload(name: str) -> Workload:
@@ -330,6 +337,15 @@ def named_workload(name: str) -> Workload:
             name, Geometry(n_h=32, n_kv=8, d_h=128, kv_dtype="int4"), ctx, seed,
             description="Llama-3-8B layer, INT4 KV: B=64, ctx U[512,4096], n_h=32, n_kv=8, "
                         "d_h=128")
+    if name == "llama3_8b_spec4":
+        # speculative verification ("LLM 推理引擎设计" §6): the Llama-3-8B batch
+        # checks a 4-token draft per sequence in one multi-query step
+        rng = np.random.default_rng(seed)
+        ctx = rng.integers(512, 4096, size=64, endpoint=True)
+        return make_workload(
+            name, Geometry(n_h=32, n_kv=8, d_h=128), ctx, seed, n_q=4,
+            description="Llama-3-8B layer, 4-token speculative verify: B=64, ctx U[512,4096], "
+                        "n_q=4, n_h=32, n_kv=8, d_h=128, bf16")
     if name == "long_context":
         return make_workload(
             name, Geometry(n_h=32, n_kv=8, d_h=128), [131072, 98304, 65536, 32768], seed,
