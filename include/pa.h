@@ -15,7 +15,7 @@
  *  [G] "kv-cache-guide" (guijiagi.com)
  *  [T] "KV Cache 显存管理全景：内存碎片拟合推导、vLLM PagedAttention 虚拟内存与
  *      Prefix Caching" (talentme.airsota.com)
- *  [E] "LLM 推理引擎设计：KV Cache、PagedAttention 与连续批处理" (hx.sn.cn)
+ *  [H] "LLM 推理引擎设计：KV Cache、PagedAttention 与连续批处理" (hx.sn.cn)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -257,7 +257,7 @@ pa_status pa_decode_opt(const void *q, const void *k_cache, const void *v_cache,
 
 /*
  * pa_decode_mq -- multi-query decode: n_q new tokens per sequence attend in
- * one pass, as when a target model verifies a k-token draft ([E] §6
+ * one pass, as when a target model verifies a k-token draft ([H] §6
  * "投机解码": the large model checks the draft tokens in one parallel
  * forward) or processes one chunk of a chunked prefill ([F] "Chunked
  * Prefill"). The n_q tokens of sequence b are its last n_q positions

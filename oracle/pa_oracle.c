@@ -13,7 +13,7 @@
  *  [G] "kv-cache-guide" (guijiagi.com)
  *  [T] "KV Cache 显存管理全景：内存碎片拟合推导、vLLM PagedAttention 虚拟内存与
  *      Prefix Caching" (talentme.airsota.com)
- *  [E] "LLM 推理引擎设计：KV Cache、PagedAttention 与连续批处理" (hx.sn.cn)
+ *  [H] "LLM 推理引擎设计：KV Cache、PagedAttention 与连续批处理" (hx.sn.cn)
  *
  * Floating point: attention runs in double precision. The INT8 quantiser runs
  * in IEEE single precision (the scales it produces are fp32 numbers, so the
@@ -445,7 +445,7 @@ int oracle_decode_window(const uint16_t *q, const void *k_cache, const void *v_c
 
 /* ------------------------------------------------------------------------
  * Multi-query decode: n_q new tokens per sequence attend at once, as in
- * speculative verification (a draft of k tokens checked in one step, [E]
+ * speculative verification (a draft of k tokens checked in one step, [H]
  * §6 "投机解码") or a chunk of a chunked prefill ([F] "Chunked Prefill"). The
  * n_q new tokens of sequence b are its last n_q positions ctx_b - n_q ..
  * ctx_b - 1 (their K/V already appended); query i (0-based) attends causally
