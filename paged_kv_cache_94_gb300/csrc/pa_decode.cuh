@@ -10,10 +10,13 @@
 // How the work is split.
 //   An "item" is one (sequence, kv head, 16-token block). Items are laid out
 //   sequence-major, then kv head, then block, so the W items of the whole
-//   batch form one line. CTA c of G takes items [c*W/G, (c+1)*W/G): every CTA
-//   gets the same number of K/V bytes whatever the mix of context lengths, and
-//   long contexts are split across CTAs ("split-context" decode). A CTA's
-//   range is cut at (sequence, kv head) boundaries into segments.
+//   batch form one line. The split is by cost: each (sequence, kv head) also
+//   counts kSegCost items for the merge that ends each of its segments (see
+//   virt_first), and CTA c of G takes the items in [c/G, (c+1)/G) of that
+//   weighted line. Every CTA gets about the same work whatever the mix of
+//   context lengths, and long contexts are split across CTAs
+//   ("split-context" decode). A CTA's range is cut at (sequence, kv head)
+//   boundaries into segments.
 //   The g query heads of one KV head are processed together, so each K/V tile
 //   is read from HBM once for all g heads.
 // Inside a CTA.
@@ -170,6 +173,54 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Cost-weighted split. Besides its blocks, every (sequence, kv head) unit
+// costs a fixed merge at the end of each segment that covers it. The split
+// runs on a "virtual" line where unit (b, kvh) is kSegCost + nb_b long: the
+// first kSegCost positions stand for the merge, the rest for its blocks in
+// order. CTA c of G owns virtual [plan_lo(c, Wv, G), plan_lo(c+1, Wv, G)),
+// i.e. the contiguous real items whose virtual positions fall there, so a CTA
+// covering many short units gets fewer blocks. Every sequence (even an empty
+// one) carries n_kv * kSegCost, so the virtual prefix is P[b] + kSegCost * b.
+// ---------------------------------------------------------------------------
+constexpr int kSegCost = 8;
+
+// Virtual position of the first block of unit (b, kvh) (nb = blocks of b).
+__device__ __forceinline__ int64_t virt_first(const DecodeParams &p, const int32_t *P, int b,
+                                              int kvh, int nb)
+{
+    return (int64_t)p.n_kv * (P[b] + (int64_t)kSegCost * b) + (int64_t)kvh * (nb + kSegCost) +
+           kSegCost;
+}
+
+// Total virtual length.
+__device__ __forceinline__ int64_t virt_total(const DecodeParams &p, const int32_t *P)
+{
+    return (int64_t)p.n_kv * (P[p.num_seqs] + (int64_t)kSegCost * p.num_seqs);
+}
+
+// First real item whose virtual position is >= y (W for y >= the total).
+__device__ __forceinline__ int64_t real_at_virtual(const DecodeParams &p, const int32_t *P,
+                                                   int64_t y)
+{
+    if (y >= virt_total(p, P))
+        return (int64_t)p.n_kv * P[p.num_seqs];
+    int lo = 0, hi = p.num_seqs;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)p.n_kv * (P[mid] + (int64_t)kSegCost * mid) <= y)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const int b = lo;
+    const int64_t nb = P[b + 1] - P[b], v = nb + kSegCost;
+    const int64_t r = y - (int64_t)p.n_kv * (P[b] + (int64_t)kSegCost * b);
+    const int64_t kvh = r / v, off = r - kvh * v;
+    const int64_t base = (int64_t)p.n_kv * P[b] + kvh * nb;
+    return off < kSegCost ? base : base + (off - kSegCost);
+}
+
 // Item x -> (sequence b, kv head, block index i within the sequence, blocks
 // of the sequence). Largest b with n_kv*P[b] <= x; such a b has blocks.
 __device__ __forceinline__ void locate_item(int64_t x, const int32_t *P, int num_seqs, int n_kv,
@@ -253,9 +304,9 @@ __device__ __forceinline__ void sink_scores(const DecodeParams &p, int b, int kv
 }
 
 template <int D, int GQ, int NW, int NQ>
-__device__ __forceinline__ void finish_segment(const DecodeParams &p, const float *merge,
-                                               int32_t *misc, float *sink_sc, int b, int kvh,
-                                               int64_t unit_start, int nb, int64_t W, int64_t G,
+__device__ __forceinline__ void finish_segment(const DecodeParams &p, const int32_t *P,
+                                               const float *merge, int32_t *misc, float *sink_sc,
+                                               int b, int kvh, int nb, int64_t Wv, int64_t G,
                                                bool whole, int s_lo, int s_hi)
 {
     constexpr int NT = NW * 32;
@@ -308,8 +359,10 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const floa
     __syncthreads(); // also: every record store of this CTA is done (CTA scope)
     if (whole)
         return;
-    const int64_t c_first = plan_owner(unit_start, W, G);
-    const int nseg = (int)(plan_owner(unit_start + nb - 1, W, G) - c_first + 1);
+    // the CTAs that own the unit's blocks: owners of its first and last block
+    const int64_t v0 = virt_first(p, P, b, kvh, nb);
+    const int64_t c_first = plan_owner(v0, Wv, G);
+    const int nseg = (int)(plan_owner(v0 + nb - 1, Wv, G) - c_first + 1);
     if (threadIdx.x == 0) {
         const int old = atomic_add_acq_rel_gpu(&p.counters[u], 1);
         const int last = (old == nseg - 1);

@@ -99,8 +99,9 @@ struct Bf16Policy {
             tma_load_2d(dst + TILE + h * (TILE / HALVES), tv, h * 64, y, bar, pol);
     }
 
-    __device__ static void load_q(State &st, const DecodeParams &p, int b, int kvh,
-                                  float * /*qsm*/)
+    // Issue the loads of a segment's q fragments (they land while the
+    // previous segment merges); finish_q completes them at segment start.
+    __device__ static void prefetch_q(State &st, const DecodeParams &p, int b, int kvh)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
 #pragma unroll
@@ -116,6 +117,8 @@ struct Bf16Policy {
             }
         }
     }
+
+    __device__ static void finish_q(State &) {}
 
     __device__ static void reset(State &st)
     {
@@ -333,15 +336,16 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     prefix_blocks<NW * 32>(p, P, misc + 8);
     __syncthreads();
     zero_empty_sequences<D, Pol::NQ>(p, P, n_h);
-    const int64_t W = (int64_t)p.n_kv * P[p.num_seqs];
-    // At most one CTA per item: then every CTA owns at least one item, and the
-    // CTAs owning a (sequence, kv head) are exactly plan_owner(first) ..
-    // plan_owner(last), which the split merge counts on.
-    const int64_t G = plan_ctas(p.num_ctas, W);
+    // Cost-weighted split on the virtual line (see virt_first). A CTA whose
+    // virtual range holds no block does nothing; the CTAs owning a (sequence,
+    // kv head) are exactly the owners of its first through last block, which
+    // the split merge counts on.
+    const int64_t Wv = virt_total(p, P);
+    const int64_t G = plan_ctas(p.num_ctas, Wv);
     if ((int64_t)blockIdx.x >= G)
         return;
-    const int64_t lo = plan_lo(blockIdx.x, W, G);
-    const int64_t hi = plan_lo(blockIdx.x + 1, W, G);
+    const int64_t lo = real_at_virtual(p, P, plan_lo(blockIdx.x, Wv, G));
+    const int64_t hi = real_at_virtual(p, P, plan_lo(blockIdx.x + 1, Wv, G));
 
     if (lane == 0)
         for (int s = 0; s < S; ++s)
@@ -427,9 +431,13 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     int cstage = 0;       // ring stage of item k
     uint32_t cphase = 0;  // barrier phase parity of item k
     int64_t seg_lo = lo;
-    while (seg_lo < hi) {
-        int b, kvh, i0, nb;
+    int b, kvh, i0, nb;
+    if (seg_lo < hi) {
         locate_item(seg_lo, P, p.num_seqs, p.n_kv, b, kvh, i0, nb);
+        Pol::prefetch_q(st, p, b, kvh);
+    }
+    while (seg_lo < hi) {
+        const int i0_cur = i0;
         const int64_t unit_start = seg_lo - i0;
         const int64_t unit_end = unit_start + nb;
         const int64_t seg_hi = unit_end < hi ? unit_end : hi;
@@ -441,7 +449,7 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         const int32_t pool_from = ws > p.n_sink ? ws : p.n_sink;
         const int32_t fb = ws / kBlockTokens;
 
-        Pol::load_q(st, p, b, kvh, qsm);
+        Pol::finish_q(st);
         Pol::reset(st);
         int64_t x = lo + warp + k * NW;
         while (k < r.n_items && x < seg_hi) {
@@ -473,11 +481,18 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
                 cphase ^= 1u;
             }
         }
+        // the next segment's q loads overlap this segment's merge
+        const int b_cur = b, kvh_cur = kvh;
+        const int64_t nb_cur = nb;
+        if (seg_hi < hi) {
+            locate_item(seg_hi, P, p.num_seqs, p.n_kv, b, kvh, i0, nb);
+            Pol::prefetch_q(st, p, b, kvh);
+        }
         Pol::to_merge(st, merge);
         __syncthreads();
-        const int32_t s_hi = (i0 == 0 && p.n_sink > ws) ? min(p.n_sink, ctx) : 0;
-        finish_segment<D, GQ, NW, Pol::NQ>(p, merge, misc, sink_sc, b, kvh, unit_start, nb, W, G,
-                                           whole, ws, s_hi > ws ? s_hi : ws);
+        const int32_t s_hi = (i0_cur == 0 && p.n_sink > ws) ? min(p.n_sink, ctx) : 0;
+        finish_segment<D, GQ, NW, Pol::NQ>(p, P, merge, misc, sink_sc, b_cur, kvh_cur,
+                                           (int)nb_cur, Wv, G, whole, ws, s_hi > ws ? s_hi : ws);
         seg_lo = seg_hi;
     }
 

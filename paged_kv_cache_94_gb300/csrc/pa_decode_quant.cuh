@@ -186,12 +186,11 @@ struct QuantMmaPolicy {
     //         (nibbles j, j+4 of one 32-bit word of the thread's slice).
     __device__ static int kperm_d0(int kk, int t) { return 64 * (kk >> 2) + 16 * t + 4 * (kk & 3); }
 
-    __device__ static void load_q(State &st, const DecodeParams &p, int b, int kvh,
-                                  float * /*qsm*/)
+    // Issue the loads of a segment's raw bf16 q words into st.qf (they land
+    // while the previous segment merges); finish_q converts them in place.
+    __device__ static void prefetch_q(State &st, const DecodeParams &p, int b, int kvh)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
-        float qv[NT][KS][4]; // per k-step: register 0 (lo, hi), register 1 (lo, hi)
-        float mx = 0.f;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int hl = nt * 8 + gid;
@@ -202,20 +201,47 @@ struct QuantMmaPolicy {
                 for (int kk = 0; kk < KS; ++kk) {
                     const uint2 w = ok ? __ldg(reinterpret_cast<const uint2 *>(row + kperm_d0(kk, t4)))
                                        : make_uint2(0u, 0u);
-                    qv[nt][kk][0] = __uint_as_float(w.x << 16);
-                    qv[nt][kk][1] = __uint_as_float(w.x & 0xffff0000u);
-                    qv[nt][kk][2] = __uint_as_float(w.y << 16);
-                    qv[nt][kk][3] = __uint_as_float(w.y & 0xffff0000u);
+                    st.qf[nt][kk][0] = w.x;
+                    st.qf[nt][kk][1] = w.y;
+                }
+            } else {
+#pragma unroll
+                for (int wi = 0; wi < KS / 2; ++wi) {
+                    const uint4 w = ok ? __ldg(reinterpret_cast<const uint4 *>(
+                                             row + (D / 4) * t4 + 8 * wi))
+                                       : make_uint4(0u, 0u, 0u, 0u);
+                    st.qf[nt][2 * wi][0] = w.x;
+                    st.qf[nt][2 * wi][1] = w.y;
+                    st.qf[nt][2 * wi + 1][0] = w.z;
+                    st.qf[nt][2 * wi + 1][1] = w.w;
+                }
+            }
+        }
+    }
+
+    __device__ static void finish_q(State &st)
+    {
+        const int lane = threadIdx.x & 31, t4 = lane & 3;
+        float qv[NT][KS][4]; // per k-step: register 0 (lo, hi), register 1 (lo, hi)
+        float mx = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            if constexpr (BITS == 8) {
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    const uint32_t wx = st.qf[nt][kk][0], wy = st.qf[nt][kk][1];
+                    qv[nt][kk][0] = __uint_as_float(wx << 16);
+                    qv[nt][kk][1] = __uint_as_float(wx & 0xffff0000u);
+                    qv[nt][kk][2] = __uint_as_float(wy << 16);
+                    qv[nt][kk][3] = __uint_as_float(wy & 0xffff0000u);
                 }
             } else {
 #pragma unroll
                 for (int wi = 0; wi < KS / 2; ++wi) {
                     // d values D/4*t4 + 8*wi + 0..7
-                    const uint4 w = ok ? __ldg(reinterpret_cast<const uint4 *>(
-                                             row + (D / 4) * t4 + 8 * wi))
-                                       : make_uint4(0u, 0u, 0u, 0u);
                     float x[8];
-                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                    const uint32_t ww[4] = {st.qf[nt][2 * wi][0], st.qf[nt][2 * wi][1],
+                                            st.qf[nt][2 * wi + 1][0], st.qf[nt][2 * wi + 1][1]};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         x[2 * i] = __uint_as_float(ww[i] << 16);

@@ -1,7 +1,7 @@
-// Work split of the decode kernels, shared by host and device code.
-//
-// W items (sequence, kv head, block) on one line; CTA c of G = min(grid, W)
-// owns [floor(c*W/G), floor((c+1)*W/G)); CTAs c >= G do no work.
+// Equal split of a line of W positions over G = min(grid, W) parts, shared
+// by host and device code: part c owns [floor(c*W/G), floor((c+1)*W/G)).
+// The decode kernels apply it to a cost-weighted line of their items (blocks
+// plus a fixed charge per (sequence, kv head), pa_decode.cuh).
 #pragma once
 
 #include <stdint.h>
