@@ -59,6 +59,8 @@ def parse_args():
                     help="step: the decode step (default); block_copy: pa_block_copy; "
                          "allocator: the host block manager")
     ap.add_argument("--pairs", type=int, default=4096, help="block pairs per pa_block_copy")
+    ap.add_argument("--no-share", action="store_true",
+                    help="decode shared-prefix workloads without the shared-prefix passes")
     return ap.parse_args()
 
 
@@ -270,7 +272,10 @@ def run_native(args, rank, world, local_rank):
     cl = torch.from_numpy(w.context_lens).to(dev)
     out = torch.empty_like(q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws = pa.decode_workspace(pa.geometry(kc, g.n_h), w.B, dev, args.num_ctas, n_q=w.n_q)
+    # sequences sharing prefix blocks (prefix caching): attend those blocks once per group
+    share = bool((w.group >= 0).any()) and not args.no_share
+    ws = pa.decode_workspace(pa.geometry(kc, g.n_h), w.B, dev, args.num_ctas, n_q=w.n_q,
+                             share_prefix=share)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize(dev)
 
@@ -281,7 +286,7 @@ def run_native(args, rank, world, local_rank):
         else:
             pa.pa_decode(q_, kc, vc, bt_, cl_, w.scale, out=out, k_scale=ks, v_scale=vs,
                          workspace=ws, dev_status=status, num_ctas=args.num_ctas,
-                         window=w.window)
+                         window=w.window, share_prefix=share)
 
     def step():
         pa.pa_cache_write(kn, vn, slots_new, kc, vc, ks, vs, dev_status=status)
@@ -342,16 +347,19 @@ def run_native(args, rank, world, local_rank):
                    "context_tokens": int(w.context_lens.sum()),
                    "l2": "flushed between timed steps (512 MiB write); KV working set "
                          f"{db['bytes'] / 1e6:.0f} MB > 129 MB L2",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "shared_prefix_passes": share},
         "seqs_per_s": round(world * w.B / (ms_per_step * 1e-3), 1),
         "decode_ms": round(dec_avg, 5), "cache_write_ms": round(statistics.mean(write_ms), 5),
         "bytes_per_step": step_bytes, "logical_kv_bytes": db["logical_bytes"],
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                      "traffic": recorded_traffic(args.workload),
-                     "kernel": "pa::decode_kernel", "peak_source": pk["source"],
+                     "kernel": ("pa::share_detect_kernel + pa::decode_kernel (prefix pass, "
+                                "decode pass)" if share else "pa::decode_kernel"),
+                     "peak_source": pk["source"],
                      "algorithmic_bytes_per_launch": db["bytes"]},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (4 if share else 2) * args.steps,
         "clocks": clocks,
     }
 
@@ -395,7 +403,7 @@ def run_native(args, rank, world, local_rank):
         result["e2e"] = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2),
                          "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-        result["gpu_launches"] += 2 * args.steps
+        result["gpu_launches"] += (4 if share else 2) * args.steps
 
     # ---- the oracle on the host cores (rank 0 only, N=1 only)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -233,6 +233,18 @@ pa_status pa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
  *             2-byte aligned), required when n_sink > 0, else NULL.
  *             pa_sink_write fills them.
  *   num_ctas  > 0: the CTA count as in pa_decode_ex; 0: the default.
+ *   share_prefix  1: sequences whose block tables start with the same
+ *             physical blocks (prefix caching, [F] "Prefix Caching 与
+ *             Copy-on-Write") have those blocks attended once per group: a
+ *             first kernel finds runs of adjacent sequences sharing >= 8
+ *             leading full blocks (groups of at most 8 sequences for g <= 2,
+ *             16/g otherwise), a prefix pass attends the shared blocks with
+ *             all the group's query rows at once and keeps their softmax
+ *             states, and the decode of each sequence's remaining blocks
+ *             merges them (log-sum-exp). The result equals pa_decode's up to
+ *             rounding. Sharers must be adjacent in the batch. Not with a
+ *             window or sink rows; g <= 8. The workspace is
+ *             pa_decode_opt_workspace_size(geom, num_seqs, opts).
  */
 typedef struct pa_decode_opts {
     int32_t window;
@@ -240,8 +252,12 @@ typedef struct pa_decode_opts {
     const void *sink_k;
     const void *sink_v;
     int32_t num_ctas;
-    int32_t reserved; /* must be 0 */
+    int32_t share_prefix; /* 1: attend shared prefixes once per group (below) */
+    int32_t reserved;     /* must be 0 */
 } pa_decode_opts;
+
+/* Workspace bytes pa_decode_opt needs for these options (0 if invalid). */
+size_t pa_decode_opt_workspace_size(pa_geom geom, int32_t num_seqs, const pa_decode_opts *opts);
 
 /* pa_decode with options (opts may be NULL: plain pa_decode). Extra
  * errors: PA_ERR_SHAPE for window < 0, n_sink outside 0..16, n_sink > 0 on

@@ -44,7 +44,7 @@ PA_ERR_STATE = -13
 EXPORTED = ["pa_cache_write", "pa_decode_workspace_size", "pa_decode_workspace_init",
             "pa_decode", "pa_decode_ex", "pa_decode_noalloc", "pa_decode_default_ctas",
             "pa_plan_owner", "pa_block_copy", "pa_decode_opt", "pa_sink_write",
-            "pa_decode_mq", "pa_decode_mq_workspace_size",
+            "pa_decode_mq", "pa_decode_mq_workspace_size", "pa_decode_opt_workspace_size",
             "pa_status_string", "pa_status_from_device", "pa_version",
             # host block manager (include/pa_alloc.h)
             "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate_prompt",
@@ -70,7 +70,8 @@ class pa_geom(ctypes.Structure):
 class pa_decode_opts(ctypes.Structure):
     _fields_ = [("window", ctypes.c_int32), ("n_sink", ctypes.c_int32),
                 ("sink_k", ctypes.c_void_p), ("sink_v", ctypes.c_void_p),
-                ("num_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("num_ctas", ctypes.c_int32), ("share_prefix", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _LIB = None
@@ -120,6 +121,8 @@ def _lib():
                                      P, P]
         lib.pa_decode_mq_workspace_size.restype = sz
         lib.pa_decode_mq_workspace_size.argtypes = [pa_geom, i32, i32, i32]
+        lib.pa_decode_opt_workspace_size.restype = sz
+        lib.pa_decode_opt_workspace_size.argtypes = [pa_geom, i32, P]
         lib.pa_decode_opt.restype = ctypes.c_int
         lib.pa_decode_opt.argtypes = dec[:14] + [P] + dec[14:]
         lib.pa_sink_write.restype = ctypes.c_int
@@ -237,7 +240,7 @@ def _counter_bytes(g: pa_geom, num_seqs: int) -> int:
 
 
 def decode_workspace(g: pa_geom, num_seqs: int, device: torch.device, num_ctas: int = 0,
-                     stream=None, n_q: int = 1) -> torch.Tensor:
+                     stream=None, n_q: int = 1, share_prefix: bool = False) -> torch.Tensor:
     """A workspace for pa_decode, cached per device.
 
     Its leading counter area must be zero on entry; pa_decode leaves it zero,
@@ -245,10 +248,14 @@ def decode_workspace(g: pa_geom, num_seqs: int, device: torch.device, num_ctas: 
     than the buffer has had zeroed so far.
     """
     key = device.index if device.index is not None else torch.cuda.current_device()
-    size_key = (key, g.num_blocks, g.n_h, g.n_kv, g.d_h, g.kv_dtype, num_seqs, num_ctas, n_q)
+    size_key = (key, g.num_blocks, g.n_h, g.n_kv, g.d_h, g.kv_dtype, num_seqs, num_ctas, n_q,
+                share_prefix)
     nbytes = _WS_SIZES.get(size_key)
     if nbytes is None:
-        if n_q == 1:
+        if share_prefix:
+            o = pa_decode_opts(num_ctas=int(num_ctas), share_prefix=1)
+            nbytes = _lib().pa_decode_opt_workspace_size(g, num_seqs, ctypes.byref(o))
+        elif n_q == 1:
             nbytes = _lib().pa_decode_workspace_size(g, num_seqs, num_ctas)
         else:
             nbytes = _lib().pa_decode_mq_workspace_size(g, num_seqs, n_q, num_ctas)
@@ -280,14 +287,15 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
               v_scale: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
               dev_status: Optional[torch.Tensor] = None, stream=None, num_ctas: int = 0,
               window: int = 0, sink_k: Optional[torch.Tensor] = None,
-              sink_v: Optional[torch.Tensor] = None) -> torch.Tensor:
+              sink_v: Optional[torch.Tensor] = None, share_prefix: bool = False) -> torch.Tensor:
     """Decode attention: q [B, n_h, d_h] bf16 over the paged pool -> out [B, n_h, d_h] bf16.
 
     block_tables [B, max_blocks] int32 and context_lens [B] int32 live on the device.
     num_ctas > 0 forces the number of CTAs the work is split over (pa_decode_ex).
     window > 0 attends the last `window` tokens of each sequence; sink_k/sink_v
     (bf16 [B, n_kv, n_sink, d_h], INT8 pools) hold the unquantised rows of the
-    first n_sink positions (pa_decode_opt).
+    first n_sink positions (pa_decode_opt). share_prefix attends blocks that
+    adjacent sequences share once per group (pa_decode_opt, share_prefix).
     """
     _need_cuda("q", q, torch.bfloat16)
     _need_cuda("k_cache", k_cache)
@@ -313,7 +321,8 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         if out.shape != q.shape:
             raise ValueError("out must have the shape of q")
     if workspace is None:
-        workspace = decode_workspace(g, B, q.device, num_ctas, stream)
+        workspace = decode_workspace(g, B, q.device, num_ctas, stream,
+                                     share_prefix=bool(share_prefix))
     else:
         _need_cuda("workspace", workspace)
     if dev_status is not None:
@@ -323,7 +332,7 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
             _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, float(scale),
             _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), g,
             _ptr(dev_status), _stream_ptr(stream)]
-    if window or sink_k is not None or sink_v is not None:
+    if window or sink_k is not None or sink_v is not None or share_prefix:
         n_sink = 0
         if sink_k is not None or sink_v is not None:
             _need_cuda("sink_k", sink_k, torch.bfloat16)
@@ -332,7 +341,8 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
             if sink_k.shape != (B, g.n_kv, n_sink, g.d_h) or sink_v.shape != sink_k.shape:
                 raise ValueError("sink_k, sink_v must be [num_seqs, n_kv, n_sink, d_h]")
         opts = pa_decode_opts(window=int(window), n_sink=n_sink, sink_k=_ptr(sink_k),
-                              sink_v=_ptr(sink_v), num_ctas=int(num_ctas), reserved=0)
+                              sink_v=_ptr(sink_v), num_ctas=int(num_ctas),
+                              share_prefix=1 if share_prefix else 0, reserved=0)
         st = lib.pa_decode_opt(*args[:14], ctypes.byref(opts), *args[14:])
     elif num_ctas > 0:
         st = lib.pa_decode_ex(*args, int(num_ctas))

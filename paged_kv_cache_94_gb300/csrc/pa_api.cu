@@ -152,6 +152,34 @@ size_t workspace_bytes_for(const pa_geom &g, int num_seqs, int grid, int nq = 1)
     return counters_bytes(units) + (size_t)((grid + units) * rec);
 }
 
+// CTAs per SM of the prefix pass: at most its occupancy (its units are few
+// and long, so fewer, fuller CTAs split them less).
+#ifndef PA_PREFIX_CTAS_PER_SM
+#define PA_PREFIX_CTAS_PER_SM 2
+#endif
+
+// Shared-prefix decode: after the counters and records (sized for the larger
+// of the two passes) come skip[B], groups[3B] and the prefix states
+// pre[B][n_h][d_h + 2].
+struct ShareLayout {
+    size_t records_end, skip, groups, pre, end;
+};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+ShareLayout share_layout(const pa_geom &g, int num_seqs, int grid_dec, int grid_pre)
+{
+    ShareLayout L;
+    const size_t dec = workspace_bytes_for(g, num_seqs, grid_dec);
+    const size_t pre = workspace_bytes_for(g, num_seqs, grid_pre, pa::kShareMembers(group_of(g)));
+    L.records_end = round256(dec > pre ? dec : pre);
+    L.skip = L.records_end;
+    L.groups = L.skip + round256(4 * (size_t)num_seqs);
+    L.pre = L.groups + round256(12 * (size_t)num_seqs);
+    L.end = L.pre + (size_t)num_seqs * g.n_h * (g.d_h + 2) * 4;
+    return L;
+}
+
 // ---------------------------------------------------------------- tensor maps
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -248,10 +276,14 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     pa_status st = check_geom(g);
     if (st != PA_OK)
         return st;
-    const pa_decode_opts none = {0, 0, nullptr, nullptr, 0, 0};
+    const pa_decode_opts none = {0, 0, nullptr, nullptr, 0, 0, 0};
     const pa_decode_opts &o = opts ? *opts : none;
-    if (o.window < 0 || o.n_sink < 0 || o.n_sink > 16 || o.reserved != 0)
+    if (o.window < 0 || o.n_sink < 0 || o.n_sink > 16 || o.reserved != 0 ||
+        (o.share_prefix != 0 && o.share_prefix != 1))
         return PA_ERR_SHAPE;
+    const bool share = o.share_prefix == 1;
+    if (share && (nq != 1 || o.window != 0 || o.n_sink != 0 || group_of(g) > 8))
+        return PA_ERR_UNSUPPORTED;
     if (o.n_sink > 0) {
         if (g.kv_dtype == PA_KV_BF16)
             return PA_ERR_SHAPE;
@@ -287,7 +319,20 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     if ((st = ctas_per_sm(kd, smem, per)) != PA_OK)
         return st;
     const int grid = num_ctas > 0 ? num_ctas : sms * per;
-    if (workspace_bytes < workspace_bytes_for(g, num_seqs, grid, nq))
+    const DecodeKernel *kp = share ? pa::find_prefix_kernel(g.kv_dtype, g.d_h, group_of(g)) : nullptr;
+    if (share && !kp)
+        return PA_ERR_UNSUPPORTED;
+    size_t smem_pre = 0;
+    int grid_pre = 0;
+    if (share) {
+        smem_pre = kp->smem_bytes(num_seqs);
+        int per_pre;
+        if ((st = ctas_per_sm(kp, smem_pre, per_pre)) != PA_OK)
+            return st;
+        grid_pre = sms * (per_pre < PA_PREFIX_CTAS_PER_SM ? per_pre : PA_PREFIX_CTAS_PER_SM);
+    }
+    const ShareLayout SL = share ? share_layout(g, num_seqs, grid, grid_pre) : ShareLayout{};
+    if (workspace_bytes < (share ? SL.end : workspace_bytes_for(g, num_seqs, grid, nq)))
         return PA_ERR_WORKSPACE;
 
     CUtensorMap tk, tv;
@@ -317,8 +362,35 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     p.n_sink = o.n_sink;
     p.sink_k = static_cast<const __nv_bfloat16 *>(o.n_sink > 0 ? o.sink_k : nullptr);
     p.sink_v = static_cast<const __nv_bfloat16 *>(o.n_sink > 0 ? o.sink_v : nullptr);
-    const cudaError_t e =
-        kd->launch(tk, tv, p, grid, smem, static_cast<cudaStream_t>(stream));
+    p.g = group_of(g);
+    p.seg_cost = pa::kSegCost;
+    p.skip = nullptr;
+    p.pre = nullptr;
+    p.groups = nullptr;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (share) {
+        // 1) groups of sequences sharing leading blocks, 2) the prefix pass
+        //    over them, 3) the decode of the rest, merging the prefix states
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        int32_t *skip = reinterpret_cast<int32_t *>(ws + SL.skip);
+        int32_t *groups = reinterpret_cast<int32_t *>(ws + SL.groups);
+        float *pre = reinterpret_cast<float *>(ws + SL.pre);
+        cudaError_t e = pa::launch_share_detect(block_tables, max_blocks, context_lens, num_seqs,
+                                                pa::kShareMembers(p.g), pa::kShareMinBlocks, skip,
+                                                groups, cs);
+        if (e != cudaSuccess)
+            return PA_ERR_CUDA;
+        DecodeParams pp = p;
+        pp.num_ctas = grid_pre;
+        pp.seg_cost = 0;
+        pp.groups = groups;
+        pp.pre = pre;
+        if ((e = kp->launch(tk, tv, pp, grid_pre, smem_pre, cs)) != cudaSuccess)
+            return PA_ERR_CUDA;
+        p.skip = skip;
+        p.pre = pre;
+    }
+    const cudaError_t e = kd->launch(tk, tv, p, grid, smem, cs);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -338,6 +410,25 @@ const DecodeKernel *find_decode_kernel_bf16(int d_h, int group)
 
 const DecodeKernel *find_decode_kernel_int4_d64(int group);
 const DecodeKernel *find_decode_kernel_int4_d128(int group);
+const DecodeKernel *find_prefix_kernel_bf16_d128(int group);
+const DecodeKernel *find_prefix_kernel_bf16_d64(int group);
+const DecodeKernel *find_prefix_kernel_int8_d128(int group);
+const DecodeKernel *find_prefix_kernel_int8_d64(int group);
+const DecodeKernel *find_prefix_kernel_int4_d128(int group);
+const DecodeKernel *find_prefix_kernel_int4_d64(int group);
+
+const DecodeKernel *find_prefix_kernel(int kv_dtype, int d_h, int group)
+{
+    if (d_h != 128 && d_h != 64)
+        return nullptr;
+    const bool big = d_h == 128;
+    switch (kv_dtype) {
+    case PA_KV_BF16: return big ? find_prefix_kernel_bf16_d128(group) : find_prefix_kernel_bf16_d64(group);
+    case PA_KV_INT8: return big ? find_prefix_kernel_int8_d128(group) : find_prefix_kernel_int8_d64(group);
+    case PA_KV_INT4: return big ? find_prefix_kernel_int4_d128(group) : find_prefix_kernel_int4_d64(group);
+    default: return nullptr;
+    }
+}
 
 const DecodeKernel *find_decode_kernel_int4(int d_h, int group)
 {
@@ -454,6 +545,27 @@ pa_status pa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
     return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
                        context_lens, num_seqs, scale, out, workspace, workspace_bytes, geom,
                        dev_status, stream, num_ctas);
+}
+
+size_t pa_decode_opt_workspace_size(pa_geom geom, int32_t num_seqs, const pa_decode_opts *opts)
+{
+    if (check_geom(geom) != PA_OK || num_seqs < 0 || num_seqs > kMaxSeqs)
+        return 0;
+    const int num_ctas = opts ? opts->num_ctas : 0;
+    if (num_ctas < 0)
+        return 0;
+    int grid = num_ctas;
+    if (grid == 0 && default_ctas(geom, num_seqs, grid) != PA_OK)
+        return 0;
+    if (!opts || opts->share_prefix == 0)
+        return workspace_bytes_for(geom, num_seqs, grid);
+    const DecodeKernel *kp = pa::find_prefix_kernel(geom.kv_dtype, geom.d_h, group_of(geom));
+    int dev, sms, per;
+    if (!kp || current_device(dev, sms) != PA_OK ||
+        ctas_per_sm(kp, kp->smem_bytes(num_seqs), per) != PA_OK)
+        return 0;
+    const int per_pre = per < PA_PREFIX_CTAS_PER_SM ? per : PA_PREFIX_CTAS_PER_SM;
+    return share_layout(geom, num_seqs, grid, sms * per_pre).end;
 }
 
 pa_status pa_decode_opt(const void *q, const void *k_cache, const void *v_cache,

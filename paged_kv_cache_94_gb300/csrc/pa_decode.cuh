@@ -66,7 +66,29 @@ struct DecodeParams {
     int32_t n_sink;              // INT8: positions < n_sink read the bf16 sink rows
     const __nv_bfloat16 *sink_k; // [B][n_kv][n_sink][D]
     const __nv_bfloat16 *sink_v;
+    int32_t g;                   // query heads per kv head
+    int32_t seg_cost;            // virtual items charged per (sequence, kv head) unit
+    // Shared prefixes (see pa_share.cu). Decode pass: skip[b] leading blocks of
+    // sequence b were attended by the prefix pass, whose partial state for
+    // each query head is pre[b][h] = (m, l, acc[D]) (skip NULL: none).
+    // Prefix pass: "sequence" s is the group groups[3s..3s+2] = (first
+    // member, members, shared blocks); its query rows are the g heads of each
+    // member and its results go to pre.
+    const int32_t *skip;
+    float *pre;
+    const int32_t *groups;
 };
+
+// Pass 0: decode of each sequence; pass 1: the prefix pass over groups.
+// First block, block count and block-table row of "sequence" s.
+template <int PASS>
+__device__ __forceinline__ int32_t seq_table_row(const DecodeParams &p, int s)
+{
+    if constexpr (PASS == 1)
+        return __ldg(p.groups + 3 * s);
+    else
+        return s;
+}
 
 // Row of query row v of (sequence b, kv head kvh) in q and out, laid out
 // [B][NQ][n_h][D]: the GQ = G * NQ query rows of a kv head are its G query
@@ -84,6 +106,15 @@ __device__ __forceinline__ size_t qo_row(const DecodeParams &p, int b, int kvh, 
 __device__ __forceinline__ int32_t window_start(const DecodeParams &p, int32_t ctx)
 {
     return (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
+}
+
+// First block a decode-pass sequence reads: the window's first block, or the
+// first block after the prefix the prefix pass attended.
+__device__ __forceinline__ int32_t seq_first_block(const DecodeParams &p, int b, int32_t ctx)
+{
+    if (p.skip)
+        return __ldg(p.skip + b);
+    return window_start(p, ctx) / kBlockTokens;
 }
 
 __device__ __forceinline__ void flag_error(int32_t *dev_status, int32_t bit)
@@ -122,7 +153,7 @@ struct SmemLayout {
 // context length outside [0, max_blocks*16] counts as 0 blocks (and is
 // reported).
 // ---------------------------------------------------------------------------
-template <int NT>
+template <int NT, int PASS>
 __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P, int32_t *wsum)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -134,13 +165,17 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
         const int b = base + tid;
         int32_t v = 0;
         if (b < p.num_seqs) {
-            const int32_t ctx = p.context_lens[b];
-            if (ctx < 0 || (int64_t)ctx > (int64_t)p.max_blocks * kBlockTokens) {
-                if (blockIdx.x == 0)
-                    flag_error(p.dev_status, PA_DEV_BAD_CONTEXT_BIT);
+            if constexpr (PASS == 1) {
+                v = __ldg(p.groups + 3 * b + 2); // the group's shared blocks (0: unused entry)
             } else {
-                // blocks from the one holding the window's first position
-                v = (ctx + kBlockTokens - 1) / kBlockTokens - window_start(p, ctx) / kBlockTokens;
+                const int32_t ctx = p.context_lens[b];
+                if (ctx < 0 || (int64_t)ctx > (int64_t)p.max_blocks * kBlockTokens) {
+                    if (blockIdx.x == 0)
+                        flag_error(p.dev_status, PA_DEV_BAD_CONTEXT_BIT);
+                } else {
+                    // blocks from the first one the sequence reads (window / shared prefix)
+                    v = (ctx + kBlockTokens - 1) / kBlockTokens - seq_first_block(p, b, ctx);
+                }
             }
         }
         int32_t x = v;
@@ -182,6 +217,7 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
 // i.e. the contiguous real items whose virtual positions fall there, so a CTA
 // covering many short units gets fewer blocks. Every sequence (even an empty
 // one) carries n_kv * kSegCost, so the virtual prefix is P[b] + kSegCost * b.
+// The prefix pass charges nothing (p.seg_cost = 0): its few units are long.
 // ---------------------------------------------------------------------------
 constexpr int kSegCost = 8;
 
@@ -189,14 +225,14 @@ constexpr int kSegCost = 8;
 __device__ __forceinline__ int64_t virt_first(const DecodeParams &p, const int32_t *P, int b,
                                               int kvh, int nb)
 {
-    return (int64_t)p.n_kv * (P[b] + (int64_t)kSegCost * b) + (int64_t)kvh * (nb + kSegCost) +
-           kSegCost;
+    return (int64_t)p.n_kv * (P[b] + (int64_t)p.seg_cost * b) + (int64_t)kvh * (nb + p.seg_cost) +
+           p.seg_cost;
 }
 
 // Total virtual length.
 __device__ __forceinline__ int64_t virt_total(const DecodeParams &p, const int32_t *P)
 {
-    return (int64_t)p.n_kv * (P[p.num_seqs] + (int64_t)kSegCost * p.num_seqs);
+    return (int64_t)p.n_kv * (P[p.num_seqs] + (int64_t)p.seg_cost * p.num_seqs);
 }
 
 // First real item whose virtual position is >= y (W for y >= the total).
@@ -206,19 +242,22 @@ __device__ __forceinline__ int64_t real_at_virtual(const DecodeParams &p, const 
     if (y >= virt_total(p, P))
         return (int64_t)p.n_kv * P[p.num_seqs];
     int lo = 0, hi = p.num_seqs;
+    const int64_t C = p.seg_cost;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if ((int64_t)p.n_kv * (P[mid] + (int64_t)kSegCost * mid) <= y)
+        if ((int64_t)p.n_kv * (P[mid] + C * mid) <= y)
             lo = mid;
         else
             hi = mid;
     }
+    // b has a nonzero virtual length (C > 0, or blocks: an empty b would not
+    // be the largest b with a start <= y)
     const int b = lo;
-    const int64_t nb = P[b + 1] - P[b], v = nb + kSegCost;
-    const int64_t r = y - (int64_t)p.n_kv * (P[b] + (int64_t)kSegCost * b);
+    const int64_t nb = P[b + 1] - P[b], v = nb + C;
+    const int64_t r = y - (int64_t)p.n_kv * (P[b] + C * b);
     const int64_t kvh = r / v, off = r - kvh * v;
     const int64_t base = (int64_t)p.n_kv * P[b] + kvh * nb;
-    return off < kSegCost ? base : base + (off - kSegCost);
+    return off < C ? base : base + (off - C);
 }
 
 // Item x -> (sequence b, kv head, block index i within the sequence, blocks
@@ -303,11 +342,49 @@ __device__ __forceinline__ void sink_scores(const DecodeParams &p, int b, int kv
     __syncthreads();
 }
 
-template <int D, int GQ, int NW, int NQ>
+// Row of query row v of unit (s, kvh) in q, out and pre, or -1 for a padding
+// row. Pass 0: qo_row. Pass 1 (s a group): member j = v / g of the group,
+// query head kvh * g + v % g of that sequence.
+template <int GQ, int NQ, int PASS>
+__device__ __forceinline__ int64_t unit_row(const DecodeParams &p, int s, int kvh, int v)
+{
+    if constexpr (PASS == 1) {
+        const int j = v / p.g, h = v - j * p.g;
+        if (j >= __ldg(p.groups + 3 * s + 1))
+            return -1;
+        const int b = __ldg(p.groups + 3 * s) + j;
+        return ((int64_t)b * p.n_kv + kvh) * p.g + h;
+    } else {
+        return (int64_t)qo_row<GQ, NQ>(p, s, kvh, v);
+    }
+}
+
+// Final (M, L, O) of query row h, column d: the bf16 output (pass 0) or the
+// unnormalised partial state in pre (pass 1).
+template <int D, int GQ, int NQ, int PASS>
+__device__ __forceinline__ void emit(const DecodeParams &p, int s, int kvh, int h, int d, float M,
+                                     float L, float O)
+{
+    const int64_t row = unit_row<GQ, NQ, PASS>(p, s, kvh, h);
+    if constexpr (PASS == 1) {
+        if (row < 0)
+            return;
+        float *r = p.pre + row * (D + 2);
+        if (d == 0) {
+            r[0] = M;
+            r[1] = L;
+        }
+        r[2 + d] = O;
+    } else {
+        p.out[row * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    }
+}
+
+template <int D, int GQ, int NW, int NQ, int PASS>
 __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int32_t *P,
                                                const float *merge, int32_t *misc, float *sink_sc,
                                                int b, int kvh, int nb, int64_t Wv, int64_t G,
-                                               bool whole, int s_lo, int s_hi)
+                                               bool whole, int s_lo, int s_hi, bool pre_merge)
 {
     constexpr int NT = NW * 32;
     constexpr int REC = D + 2;
@@ -332,6 +409,15 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
         }
         for (int j = 0; j < ns; ++j)
             M = fmaxf(M, sink_sc[h * 16 + j]);
+        // the prefix pass's state of this query row joins as one more partial
+        float pm = -INFINITY, pl = 0.f, po = 0.f;
+        if (pre_merge) {
+            const float *pr = p.pre + unit_row<GQ, NQ, PASS>(p, b, kvh, h) * REC;
+            pm = pr[0];
+            pl = pr[1];
+            po = pr[2 + d];
+            M = fmaxf(M, pm);
+        }
         float O = 0.f, L = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
@@ -340,6 +426,11 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
                 L = fmaf(sc, merge[(w * GQ + h) * REC + 1], L);
                 O = fmaf(sc, merge[(w * GQ + h) * REC + 2 + d], O);
             }
+            if (pm != -INFINITY) {
+                const float sc = fast_exp2(pm - M);
+                L = fmaf(sc, pl, L);
+                O = fmaf(sc, po, O);
+            }
             for (int j = 0; j < ns; ++j) {
                 const float e = fast_exp2(sink_sc[h * 16 + j] - M);
                 L += e;
@@ -347,7 +438,7 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
             }
         }
         if (whole) {
-            p.out[qo_row<GQ, NQ>(p, b, kvh, h) * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+            emit<D, GQ, NQ, PASS>(p, b, kvh, h, d, M, L, O);
         } else {
             if (d == 0) {
                 rec[h * REC] = M;
@@ -409,7 +500,7 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
                 }
             }
         }
-        p.out[qo_row<GQ, NQ>(p, b, kvh, h) * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+        emit<D, GQ, NQ, PASS>(p, b, kvh, h, d, M, L, O);
     }
 }
 
@@ -442,7 +533,7 @@ struct WarpRing {
 // Block-table entry and kv head of this warp's item k. The loaded value is
 // not used here, so the load's latency overlaps other work; the entry is
 // checked when the item is issued.
-template <int NW>
+template <int NW, int PASS>
 __device__ __forceinline__ void load_item(const DecodeParams &p, const int32_t *P,
                                           const WarpRing &r, int64_t k, int32_t &phys,
                                           int32_t &kvh)
@@ -455,9 +546,11 @@ __device__ __forceinline__ void load_item(const DecodeParams &p, const int32_t *
     const int64_t x = r.lo + r.warp + k * NW;
     int b, i, nb;
     locate_item(x, P, p.num_seqs, p.n_kv, b, kvh, i, nb);
-    if (p.window > 0)
-        i += window_start(p, __ldg(p.context_lens + b)) / kBlockTokens;
-    phys = __ldg(p.block_tables + (size_t)b * p.max_blocks + i);
+    if constexpr (PASS == 0) {
+        if (p.window > 0 || p.skip)
+            i += seq_first_block(p, b, __ldg(p.context_lens + b));
+    }
+    phys = __ldg(p.block_tables + (size_t)seq_table_row<PASS>(p, b) * p.max_blocks + i);
 }
 
 } // namespace pa

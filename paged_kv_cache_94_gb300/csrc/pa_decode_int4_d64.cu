@@ -22,11 +22,11 @@ size_t smem_of(int num_seqs)
     return Pol::Layout::bytes(num_seqs);
 }
 
-template <class Pol>
+template <class Pol, int PASS = 0>
 cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
                       size_t smem, cudaStream_t stream)
 {
-    decode_kernel<Pol><<<grid, Pol::NW * 32, smem, stream>>>(tk, tv, p);
+    decode_kernel<Pol, PASS><<<grid, Pol::NW * 32, smem, stream>>>(tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -38,7 +38,26 @@ template <int G>
 const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G>>),
                              Pol<G>::NW * 32, &smem_of<Pol<G>>, &launch_of<Pol<G>>};
 
+// Prefix pass of a shared-prefix decode: the query rows of up to kShareMembers(G)
+// sequences of a group (G heads each) share every K/V tile.
+template <int G>
+const DecodeKernel kPrefix = {
+    reinterpret_cast<const void *>(&decode_kernel<Pol<G * kShareMembers(G)>, 1>),
+    Pol<G * kShareMembers(G)>::NW * 32, &smem_of<Pol<G * kShareMembers(G)>>,
+    &launch_of<Pol<G * kShareMembers(G)>, 1>};
+
 } // namespace
+
+const DecodeKernel *find_prefix_kernel_int4_d64(int group)
+{
+    switch (group) {
+    case 1: return &kPrefix<1>;
+    case 2: return &kPrefix<2>;
+    case 4: return &kPrefix<4>;
+    case 8: return &kPrefix<8>;
+    default: return nullptr;
+    }
+}
 
 const DecodeKernel *find_decode_kernel_int4_d64(int group)
 {

@@ -101,15 +101,17 @@ struct Bf16Policy {
 
     // Issue the loads of a segment's q fragments (they land while the
     // previous segment merges); finish_q completes them at segment start.
-    __device__ static void prefetch_q(State &st, const DecodeParams &p, int b, int kvh)
+    // row_of(v): the q row of query row v, or -1 for a padding row.
+    template <class RowFn>
+    __device__ static void prefetch_q(State &st, const DecodeParams &p, RowFn row_of)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int hl = nt * 8 + gid;
-            const bool ok = hl < GQ;
-            const uint32_t *row = reinterpret_cast<const uint32_t *>(
-                p.q + qo_row<GQ, NQ>(p, b, kvh, ok ? hl : 0) * D);
+            const int64_t qr = hl < GQ ? row_of(hl) : -1;
+            const bool ok = qr >= 0;
+            const uint32_t *row = reinterpret_cast<const uint32_t *>(p.q + (ok ? qr : 0) * D);
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
                 st.qf[nt][kk][0] = ok ? __ldg(row + kk * 8 + t4) : 0u;
@@ -308,7 +310,9 @@ namespace pa {
 // ---------------------------------------------------------------------------
 // The kernel: split, ring, segments, merge.
 // ---------------------------------------------------------------------------
-template <class Pol>
+// PASS 0: decode (optionally skipping shared prefixes done by pass 1 and
+// merging their states); PASS 1: the prefix pass over groups of sequences.
+template <class Pol, int PASS = 0>
 __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p)
@@ -333,9 +337,10 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
-    prefix_blocks<NW * 32>(p, P, misc + 8);
+    prefix_blocks<NW * 32, PASS>(p, P, misc + 8);
     __syncthreads();
-    zero_empty_sequences<D, Pol::NQ>(p, P, n_h);
+    if constexpr (PASS == 0)
+        zero_empty_sequences<D, Pol::NQ>(p, P, n_h);
     // Cost-weighted split on the virtual line (see virt_first). A CTA whose
     // virtual range holds no block does nothing; the CTAs owning a (sequence,
     // kv head) are exactly the owners of its first through last block, which
@@ -360,8 +365,8 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     r.n_items = (hi - lo > warp) ? (hi - lo - warp + NW - 1) / NW : 0;
     r.issued = 0;
     r.batch = 0;
-    load_item<NW>(p, P, r, lane, r.phys_cur, r.kvh_cur);
-    load_item<NW>(p, P, r, 32 + lane, r.phys_next, r.kvh_next);
+    load_item<NW, PASS>(p, P, r, lane, r.phys_cur, r.kvh_cur);
+    load_item<NW, PASS>(p, P, r, 32 + lane, r.phys_next, r.kvh_next);
     const uint64_t pol = PA_KV_EVICT_FIRST ? l2_policy_evict_first() : l2_policy_evict_normal();
     const uint32_t ring_base = smem_u32(smem) + (uint32_t)(warp * S * Pol::STAGE);
     const uint32_t extra_base = smem_u32(smem + L::kOffExtra) + (uint32_t)(warp * S * Pol::EXTRA);
@@ -379,7 +384,7 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
             r.phys_cur = r.phys_next;
             r.kvh_cur = r.kvh_next;
             r.batch = bt;
-            load_item<NW>(p, P, r, (bt + 1) * 32 + lane, r.phys_next, r.kvh_next);
+            load_item<NW, PASS>(p, P, r, (bt + 1) * 32 + lane, r.phys_next, r.kvh_next);
         }
         const int32_t phys = __shfl_sync(0xffffffffu, r.phys_cur, (int)(k & 31));
         const int32_t kvh = __shfl_sync(0xffffffffu, r.kvh_cur, (int)(k & 31));
@@ -432,9 +437,12 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     uint32_t cphase = 0;  // barrier phase parity of item k
     int64_t seg_lo = lo;
     int b, kvh, i0, nb;
+    auto rows = [&](int s, int kh) {
+        return [&p, s, kh](int v) { return unit_row<GQ, Pol::NQ, PASS>(p, s, kh, v); };
+    };
     if (seg_lo < hi) {
         locate_item(seg_lo, P, p.num_seqs, p.n_kv, b, kvh, i0, nb);
-        Pol::prefetch_q(st, p, b, kvh);
+        Pol::prefetch_q(st, p, rows(b, kvh));
     }
     while (seg_lo < hi) {
         const int i0_cur = i0;
@@ -444,10 +452,18 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         const bool whole = (i0 == 0) && (unit_end <= hi);
         // Attended positions: [ws, ctx); the pool serves [max(ws, n_sink), ctx)
         // from logical block fb on, the sink rows serve [ws, min(n_sink, ctx)).
-        const int32_t ctx = __ldg(p.context_lens + b);
-        const int32_t ws = window_start(p, ctx);
-        const int32_t pool_from = ws > p.n_sink ? ws : p.n_sink;
-        const int32_t fb = ws / kBlockTokens;
+        // A shared prefix done by the prefix pass starts the pool at block fb.
+        // Pass 1: a group's shared blocks, all full.
+        int32_t ctx, ws, pool_from, fb;
+        if constexpr (PASS == 1) {
+            ctx = nb * kBlockTokens;
+            ws = pool_from = fb = 0;
+        } else {
+            ctx = __ldg(p.context_lens + b);
+            ws = window_start(p, ctx);
+            pool_from = ws > p.n_sink ? ws : p.n_sink;
+            fb = seq_first_block(p, b, ctx);
+        }
 
         Pol::finish_q(st);
         Pol::reset(st);
@@ -486,13 +502,15 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         const int64_t nb_cur = nb;
         if (seg_hi < hi) {
             locate_item(seg_hi, P, p.num_seqs, p.n_kv, b, kvh, i0, nb);
-            Pol::prefetch_q(st, p, b, kvh);
+            Pol::prefetch_q(st, p, rows(b, kvh));
         }
         Pol::to_merge(st, merge);
         __syncthreads();
-        const int32_t s_hi = (i0_cur == 0 && p.n_sink > ws) ? min(p.n_sink, ctx) : 0;
-        finish_segment<D, GQ, NW, Pol::NQ>(p, P, merge, misc, sink_sc, b_cur, kvh_cur,
-                                           (int)nb_cur, Wv, G, whole, ws, s_hi > ws ? s_hi : ws);
+        const int32_t s_hi = (PASS == 0 && i0_cur == 0 && p.n_sink > ws) ? min(p.n_sink, ctx) : 0;
+        const bool pre_merge = PASS == 0 && i0_cur == 0 && fb > 0 && p.skip != nullptr;
+        finish_segment<D, GQ, NW, Pol::NQ, PASS>(p, P, merge, misc, sink_sc, b_cur, kvh_cur,
+                                                 (int)nb_cur, Wv, G, whole, ws,
+                                                 s_hi > ws ? s_hi : ws, pre_merge);
         seg_lo = seg_hi;
     }
 

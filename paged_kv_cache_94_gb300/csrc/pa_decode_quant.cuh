@@ -188,14 +188,16 @@ struct QuantMmaPolicy {
 
     // Issue the loads of a segment's raw bf16 q words into st.qf (they land
     // while the previous segment merges); finish_q converts them in place.
-    __device__ static void prefetch_q(State &st, const DecodeParams &p, int b, int kvh)
+    template <class RowFn>
+    __device__ static void prefetch_q(State &st, const DecodeParams &p, RowFn row_of)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int hl = nt * 8 + gid;
-            const bool ok = hl < GQ;
-            const __nv_bfloat16 *row = p.q + qo_row<GQ, NQ>(p, b, kvh, ok ? hl : 0) * D;
+            const int64_t qr = hl < GQ ? row_of(hl) : -1;
+            const bool ok = qr >= 0;
+            const __nv_bfloat16 *row = p.q + (ok ? qr : 0) * D;
             if constexpr (BITS == 8) {
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {

@@ -28,6 +28,16 @@ struct DecodeKernel {
 const DecodeKernel *find_decode_kernel_bf16(int d_h, int group);
 const DecodeKernel *find_decode_kernel_int8(int d_h, int group);
 const DecodeKernel *find_decode_kernel_int4(int d_h, int group);
+// Shared-prefix decode: members per group of the prefix pass for group size
+// g (g * members <= 16 query rows per kv head), its kernels, and the group
+// detection kernel (pa_share.cu).
+constexpr int kShareMembers(int g) { return g <= 2 ? 8 : 16 / g; }
+constexpr int kShareMinBlocks = 8;
+const DecodeKernel *find_prefix_kernel(int kv_dtype, int d_h, int group);
+cudaError_t launch_share_detect(const int32_t *block_tables, int max_blocks,
+                                const int32_t *context_lens, int B, int gm, int min_blocks,
+                                int32_t *skip, int32_t *groups, cudaStream_t stream);
+
 // Multi-query (nq new tokens per sequence) bf16 kernels; NULL when not compiled.
 const DecodeKernel *find_decode_kernel_bf16_mq(int d_h, int group, int nq);
 

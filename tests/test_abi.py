@@ -160,7 +160,7 @@ def test_decode_opt_argument_checks(lib):
 
     def call(g, **kw):
         o = pa.pa_decode_opts(**{**dict(window=0, n_sink=0, sink_k=None, sink_v=None,
-                                        num_ctas=0, reserved=0), **kw})
+                                        num_ctas=0, share_prefix=0, reserved=0), **kw})
         return lib.pa_decode_opt(*dec, g, ctypes.byref(o), None, None)
 
     g = _geom()
@@ -171,3 +171,6 @@ def test_decode_opt_argument_checks(lib):
     assert call(gi, n_sink=17, sink_k=256, sink_v=256) == -2
     assert call(gi, n_sink=4, sink_k=None, sink_v=256) == -1
     assert call(gi, n_sink=4, sink_k=257, sink_v=256) == -11
+    assert call(g, share_prefix=2) == -2
+    assert call(g, share_prefix=1, window=64) == -4                 # not with a window
+    assert call(_geom(n_h=128, n_kv=8), share_prefix=1) == -4      # g = 16

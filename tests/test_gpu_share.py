@@ -1,0 +1,79 @@
+"""GPU parity of the shared-prefix decode (pa_decode_opt with share_prefix):
+blocks that adjacent sequences share ("LLM 推理底层", "Prefix Caching 与
+Copy-on-Write") are attended once per group, and the result must still equal
+the oracle's plain decode of every sequence."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_94_gb300 as pa
+from tests.gpu_helpers import assert_close, gpu_decode, gpu_pool, oracle_full, oracle_one_sequence
+from workloads import Geometry, make_workload, named_workload
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def run(w, pool, share=True, num_ctas=0, gen_device="cpu"):
+    kc, vc, ks, vs = pool
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = pa.pa_decode(w.q(gen_device).to(DEV), kc, vc, torch.from_numpy(w.block_tables).to(DEV),
+                       torch.from_numpy(w.context_lens).to(DEV), w.scale, k_scale=ks, v_scale=vs,
+                       dev_status=status, num_ctas=num_ctas, share_prefix=share)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), int(status.item())
+
+
+def grouped(kv_dtype, d_h, g, groups, prefix, suffix, seed):
+    """groups: group id per sequence (-1: none), adjacent members; prefix[i]:
+    shared tokens of sequence i's group; suffix[i]: its private tokens."""
+    ctx = [p + s for p, s in zip(prefix, suffix)]
+    return make_workload("share", Geometry(n_h=2 * g, n_kv=2, d_h=d_h, kv_dtype=kv_dtype), ctx,
+                         seed, prefix_len=prefix, group=groups)
+
+
+CASES = [
+    # (dtype, d_h, g, groups, prefix tokens, suffix tokens)
+    ("bf16", 128, 4, [0, 0, 0, 1, 1, -1, 2, 2], [256] * 3 + [160] * 2 + [0] + [512] * 2,
+     [5, 40, 300, 17, 1, 90, 16, 33]),
+    ("int8", 128, 1, [0] * 12, [400] * 12, [3, 17, 50, 9, 100, 1, 64, 31, 7, 260, 44, 2]),
+    ("int4", 64, 2, [0, 0, -1, 1, 1, 1], [320, 320, 0, 256, 256, 256], [48, 1, 200, 16, 15, 100]),
+    ("bf16", 64, 8, [0, 0, 0, -1, 1, 1], [144] * 3 + [0] + [208] * 2, [20, 16, 1, 77, 3, 400]),
+    ("int8", 64, 2, [-1, 0, 0, -1, 1, 1, -1], [0, 128, 128, 0, 512, 512, 0], [30, 2, 19, 0, 60, 8, 5]),
+]
+
+
+@pytest.mark.parametrize("kv_dtype,d_h,g,groups,prefix,suffix", CASES)
+def test_shared_prefix_matches_oracle(kv_dtype, d_h, g, groups, prefix, suffix):
+    w = grouped(kv_dtype, d_h, g, groups, prefix, suffix, seed=61 + g + d_h)
+    pool = gpu_pool(w, DEV, fill_nan=True)
+    ref, _ = oracle_full(w)
+    plain, st0 = run(w, pool, share=False)
+    assert st0 == 0
+    for num_ctas in (0, 1, 5, 200):
+        out, st = run(w, pool, share=True, num_ctas=num_ctas)
+        assert st == 0
+        assert_close(out, ref, f"{kv_dtype} d{d_h} g{g} ctas {num_ctas}")
+    assert np.abs(out - plain).max() < 2e-2
+
+
+def test_no_sharing_equals_plain_decode():
+    w = make_workload("ns", Geometry(n_h=8, n_kv=2, d_h=128), [300, 17, 1000, 64, 0, 5], seed=71)
+    pool = gpu_pool(w, DEV)
+    a, _ = run(w, pool, share=False)
+    b, st = run(w, pool, share=True)
+    assert st == 0 and np.array_equal(a, b)
+
+
+def test_shared_prefix_full_size_int8_workload():
+    # the LLaMA-2-7B INT8 workload: 4 groups of 8 sequences sharing 2048 tokens
+    w = named_workload("llama2_7b_int8_prefix")
+    pool = gpu_pool(w, DEV, gen_device=DEV)
+    out, st = run(w, pool, share=True, gen_device=DEV)
+    assert st == 0 and np.isfinite(out).all()
+    plain, _ = run(w, pool, share=False, gen_device=DEV)
+    assert np.abs(out - plain).max() < 2e-2
+    for b in (0, 7, 13, w.B - 1):
+        ref, _ = oracle_one_sequence(w, b, gen_device=DEV)
+        assert_close(out[b], ref, f"int8 prefix seq {b}")
