@@ -355,11 +355,12 @@ def run_native(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                      "traffic": recorded_traffic(args.workload),
-                     "kernel": ("pa::share_detect_kernel + pa::decode_kernel (prefix pass, "
-                                "decode pass)" if share else "pa::decode_kernel"),
+                     "kernel": ("pa::share_detect_kernel + pa::decode_kernel (shared-prefix "
+                                "groups and suffixes in one launch)" if share
+                                else "pa::decode_kernel"),
                      "peak_source": pk["source"],
                      "algorithmic_bytes_per_launch": db["bytes"]},
-        "gpu_launches": (4 if share else 2) * args.steps,
+        "gpu_launches": (3 if share else 2) * args.steps,
         "clocks": clocks,
     }
 
@@ -403,7 +404,7 @@ def run_native(args, rank, world, local_rank):
         result["e2e"] = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2),
                          "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-        result["gpu_launches"] += (4 if share else 2) * args.steps
+        result["gpu_launches"] += (3 if share else 2) * args.steps
 
     # ---- the oracle on the host cores (rank 0 only, N=1 only)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

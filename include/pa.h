@@ -238,11 +238,11 @@ pa_status pa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
  *             Copy-on-Write") have those blocks attended once per group: a
  *             first kernel finds runs of adjacent sequences sharing >= 8
  *             leading full blocks (groups of at most 8 sequences for g <= 2,
- *             16/g otherwise), a prefix pass attends the shared blocks with
- *             all the group's query rows at once and keeps their softmax
- *             states, and the decode of each sequence's remaining blocks
- *             merges them (log-sum-exp). The result equals pa_decode's up to
- *             rounding. Sharers must be adjacent in the batch. Not with a
+ *             16/g otherwise); a second kernel attends each group's shared
+ *             blocks once with all the group's query rows and, in the same
+ *             launch, each sequence's remaining blocks, and the last piece of
+ *             a sequence to finish merges the softmax states (log-sum-exp).
+ *             The result equals pa_decode's up to rounding. Sharers must be adjacent in the batch. Not with a
  *             window or sink rows; g <= 8. The workspace is
  *             pa_decode_opt_workspace_size(geom, num_seqs, opts).
  */

@@ -235,8 +235,12 @@ _WS_SIZES: dict = {}
 _WS_LOCK = threading.Lock()
 
 
-def _counter_bytes(g: pa_geom, num_seqs: int) -> int:
-    return (4 * num_seqs * g.n_kv + 255) // 256 * 256
+def _counter_bytes(g: pa_geom, num_seqs: int, share_prefix: bool = False) -> int:
+    """Leading workspace bytes that must be zero on entry (the library leaves
+    them zero): the unit counters (a shared-prefix call has 2 * num_seqs
+    units per kv head: the groups, then the sequences)."""
+    n = 2 * num_seqs * g.n_kv if share_prefix else num_seqs * g.n_kv
+    return (4 * n + 255) // 256 * 256
 
 
 def decode_workspace(g: pa_geom, num_seqs: int, device: torch.device, num_ctas: int = 0,
@@ -262,7 +266,7 @@ def decode_workspace(g: pa_geom, num_seqs: int, device: torch.device, num_ctas: 
         if nbytes == 0:
             raise PAError(-4 if n_q > 1 else -2, "pa_decode_workspace_size")
         _WS_SIZES[size_key] = nbytes
-    need_zero = _counter_bytes(g, num_seqs)
+    need_zero = _counter_bytes(g, num_seqs, share_prefix)
     with _WS_LOCK:
         ent = _WS.get(key)
         if ent is None or ent[0].numel() < nbytes:

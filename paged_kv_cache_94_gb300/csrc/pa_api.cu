@@ -152,28 +152,25 @@ size_t workspace_bytes_for(const pa_geom &g, int num_seqs, int grid, int nq = 1)
     return counters_bytes(units) + (size_t)((grid + units) * rec);
 }
 
-// CTAs per SM of the prefix pass: at most its occupancy (its units are few
-// and long, so fewer, fuller CTAs split them less).
-#ifndef PA_PREFIX_CTAS_PER_SM
-#define PA_PREFIX_CTAS_PER_SM 2
-#endif
-
-// Shared-prefix decode: after the counters and records (sized for the larger
-// of the two passes) come skip[B], groups[3B] and the prefix states
-// pre[B][n_h][d_h + 2].
+// Shared-prefix decode (one launch over 2B "sequences": B group units, then
+// B sequences' remaining blocks). Workspace:
+//   counters  [2B * n_kv] int32 (zero on entry and on exit)
+//   records   (grid + 2B * n_kv) x (g * members) x (d_h + 2) fp32
+//   skip[B], groups[3B] int32, pre[B][n_h][d_h + 2] fp32
 struct ShareLayout {
-    size_t records_end, skip, groups, pre, end;
+    size_t zero_end, records, skip, groups, pre, end;
 };
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
-ShareLayout share_layout(const pa_geom &g, int num_seqs, int grid_dec, int grid_pre)
+ShareLayout share_layout(const pa_geom &g, int num_seqs, int grid)
 {
     ShareLayout L;
-    const size_t dec = workspace_bytes_for(g, num_seqs, grid_dec);
-    const size_t pre = workspace_bytes_for(g, num_seqs, grid_pre, pa::kShareMembers(group_of(g)));
-    L.records_end = round256(dec > pre ? dec : pre);
-    L.skip = L.records_end;
+    const size_t units2 = 2 * (size_t)num_seqs * g.n_kv;
+    L.zero_end = round256(4 * units2);
+    L.records = L.zero_end;
+    const size_t rec = (size_t)group_of(g) * pa::kShareMembers(group_of(g)) * (g.d_h + 2) * 4;
+    L.skip = round256(L.records + (grid + units2) * rec);
     L.groups = L.skip + round256(4 * (size_t)num_seqs);
     L.pre = L.groups + round256(12 * (size_t)num_seqs);
     L.end = L.pre + (size_t)num_seqs * g.n_h * (g.d_h + 2) * 4;
@@ -318,20 +315,20 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     const size_t smem = kd->smem_bytes(num_seqs);
     if ((st = ctas_per_sm(kd, smem, per)) != PA_OK)
         return st;
-    const int grid = num_ctas > 0 ? num_ctas : sms * per;
+    int grid = num_ctas > 0 ? num_ctas : sms * per;
     const DecodeKernel *kp = share ? pa::find_prefix_kernel(g.kv_dtype, g.d_h, group_of(g)) : nullptr;
     if (share && !kp)
         return PA_ERR_UNSUPPORTED;
-    size_t smem_pre = 0;
-    int grid_pre = 0;
+    size_t smem_sh = 0;
     if (share) {
-        smem_pre = kp->smem_bytes(num_seqs);
-        int per_pre;
-        if ((st = ctas_per_sm(kp, smem_pre, per_pre)) != PA_OK)
+        // one wave of resident CTAs
+        smem_sh = kp->smem_bytes(2 * num_seqs);
+        int per_sh;
+        if ((st = ctas_per_sm(kp, smem_sh, per_sh)) != PA_OK)
             return st;
-        grid_pre = sms * (per_pre < PA_PREFIX_CTAS_PER_SM ? per_pre : PA_PREFIX_CTAS_PER_SM);
+        grid = sms * per_sh;
     }
-    const ShareLayout SL = share ? share_layout(g, num_seqs, grid, grid_pre) : ShareLayout{};
+    const ShareLayout SL = share ? share_layout(g, num_seqs, grid) : ShareLayout{};
     if (workspace_bytes < (share ? SL.end : workspace_bytes_for(g, num_seqs, grid, nq)))
         return PA_ERR_WORKSPACE;
 
@@ -368,27 +365,28 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     p.pre = nullptr;
     p.groups = nullptr;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    p.num_real = num_seqs;
     if (share) {
-        // 1) groups of sequences sharing leading blocks, 2) the prefix pass
-        //    over them, 3) the decode of the rest, merging the prefix states
+        // 1) groups of adjacent sequences sharing leading blocks; 2) one
+        //    launch over the group units, then every sequence's remaining
+        //    blocks; the last arrival on each sequence merges its records and
+        //    its group's prefix state
         uint8_t *ws = static_cast<uint8_t *>(workspace);
         int32_t *skip = reinterpret_cast<int32_t *>(ws + SL.skip);
         int32_t *groups = reinterpret_cast<int32_t *>(ws + SL.groups);
-        float *pre = reinterpret_cast<float *>(ws + SL.pre);
         cudaError_t e = pa::launch_share_detect(block_tables, max_blocks, context_lens, num_seqs,
                                                 pa::kShareMembers(p.g), pa::kShareMinBlocks, skip,
                                                 groups, cs);
         if (e != cudaSuccess)
             return PA_ERR_CUDA;
-        DecodeParams pp = p;
-        pp.num_ctas = grid_pre;
-        pp.seg_cost = 0;
-        pp.groups = groups;
-        pp.pre = pre;
-        if ((e = kp->launch(tk, tv, pp, grid_pre, smem_pre, cs)) != cudaSuccess)
-            return PA_ERR_CUDA;
+        p.num_seqs = 2 * num_seqs;
+        p.counters = reinterpret_cast<int32_t *>(ws);
+        p.partials = reinterpret_cast<float *>(ws + SL.records);
         p.skip = skip;
-        p.pre = pre;
+        p.groups = groups;
+        p.pre = reinterpret_cast<float *>(ws + SL.pre);
+        p.num_ctas = grid;
+        return kp->launch(tk, tv, p, grid, smem_sh, cs) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     }
     const cudaError_t e = kd->launch(tk, tv, p, grid, smem, cs);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -562,10 +560,9 @@ size_t pa_decode_opt_workspace_size(pa_geom geom, int32_t num_seqs, const pa_dec
     const DecodeKernel *kp = pa::find_prefix_kernel(geom.kv_dtype, geom.d_h, group_of(geom));
     int dev, sms, per;
     if (!kp || current_device(dev, sms) != PA_OK ||
-        ctas_per_sm(kp, kp->smem_bytes(num_seqs), per) != PA_OK)
+        ctas_per_sm(kp, kp->smem_bytes(2 * num_seqs), per) != PA_OK)
         return 0;
-    const int per_pre = per < PA_PREFIX_CTAS_PER_SM ? per : PA_PREFIX_CTAS_PER_SM;
-    return share_layout(geom, num_seqs, grid, sms * per_pre).end;
+    return share_layout(geom, num_seqs, sms * per).end;
 }
 
 pa_status pa_decode_opt(const void *q, const void *k_cache, const void *v_cache,

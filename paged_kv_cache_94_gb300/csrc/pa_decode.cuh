@@ -68,24 +68,24 @@ struct DecodeParams {
     const __nv_bfloat16 *sink_v;
     int32_t g;                   // query heads per kv head
     int32_t seg_cost;            // virtual items charged per (sequence, kv head) unit
-    // Shared prefixes (see pa_share.cu). Decode pass: skip[b] leading blocks of
-    // sequence b were attended by the prefix pass, whose partial state for
-    // each query head is pre[b][h] = (m, l, acc[D]) (skip NULL: none).
-    // Prefix pass: "sequence" s is the group groups[3s..3s+2] = (first
-    // member, members, shared blocks); its query rows are the g heads of each
-    // member and its results go to pre.
+    // Shared prefixes (PASS 2, see pa_share.cu): the line holds num_real
+    // group units first, group s = groups[3s..3s+2] = (first member, members,
+    // shared blocks), whose query rows are the g heads of each member; then
+    // the num_real sequences' blocks after their first skip[b]. A group's
+    // softmax state of each member's head h goes to pre[b][h] = (m, l, acc[D]).
     const int32_t *skip;
     float *pre;
     const int32_t *groups;
+    int32_t num_real;
 };
 
-// Pass 0: decode of each sequence; pass 1: the prefix pass over groups.
-// First block, block count and block-table row of "sequence" s.
+// Pass 0: decode of each sequence; pass 2: shared-prefix groups, then each
+// sequence's remaining blocks. Block-table row of "sequence" s.
 template <int PASS>
 __device__ __forceinline__ int32_t seq_table_row(const DecodeParams &p, int s)
 {
-    if constexpr (PASS == 1)
-        return __ldg(p.groups + 3 * s);
+    if constexpr (PASS == 2)
+        return s < p.num_real ? __ldg(p.groups + 3 * s) : s - p.num_real;
     else
         return s;
 }
@@ -108,12 +108,9 @@ __device__ __forceinline__ int32_t window_start(const DecodeParams &p, int32_t c
     return (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
 }
 
-// First block a decode-pass sequence reads: the window's first block, or the
-// first block after the prefix the prefix pass attended.
-__device__ __forceinline__ int32_t seq_first_block(const DecodeParams &p, int b, int32_t ctx)
+// First block a sequence reads: the window's first block.
+__device__ __forceinline__ int32_t seq_first_block(const DecodeParams &p, int32_t ctx)
 {
-    if (p.skip)
-        return __ldg(p.skip + b);
     return window_start(p, ctx) / kBlockTokens;
 }
 
@@ -135,7 +132,7 @@ struct SmemLayout {
     static constexpr int kMeta = NW * S * 4;
     static constexpr int kMerge = NW * GQ * (D + 2) * 4;                // per-warp (m, l, acc)
     static constexpr int kSinkSc = GQ * 16 * 4;                         // sink-row scores
-    static constexpr int kMisc = 64;
+    static constexpr int kMisc = 128; // 32 int32 of per-CTA scratch (flags, scan sums)
     static constexpr int kOffExtra = kRing;
     static constexpr int kOffQ = kOffExtra + kExtra;
     static constexpr int kOffBars = (kOffQ + kQ + 15) / 16 * 16;
@@ -144,7 +141,8 @@ struct SmemLayout {
     static constexpr int kOffSinkSc = kOffMerge + kMerge;
     static constexpr int kOffMisc = kOffSinkSc + kSinkSc;
     static constexpr int kOffPrefix = kOffMisc + kMisc;
-    static size_t bytes(int num_seqs) { return 1024 + kOffPrefix + 4 * (size_t)(num_seqs + 1); }
+    // P[num_seqs + 1] (blocks) then Z[num_seqs + 1] (sequences with blocks)
+    static size_t bytes(int num_seqs) { return 1024 + kOffPrefix + 8 * (size_t)(num_seqs + 1); }
 };
 
 // ---------------------------------------------------------------------------
@@ -158,15 +156,29 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NWARP = NT / 32;
-    int32_t carry = 0;
-    if (tid == 0)
+    int32_t carry = 0, zcarry = 0;
+    int32_t *Z = P + p.num_seqs + 1; // Z[b]: sequences before b that have blocks
+    if (tid == 0) {
         P[0] = 0;
+        Z[0] = 0;
+    }
     for (int base = 0; base < p.num_seqs; base += NT) {
         const int b = base + tid;
         int32_t v = 0;
         if (b < p.num_seqs) {
-            if constexpr (PASS == 1) {
-                v = __ldg(p.groups + 3 * b + 2); // the group's shared blocks (0: unused entry)
+            if constexpr (PASS == 2) {
+                if (b < p.num_real) {
+                    v = __ldg(p.groups + 3 * b + 2); // the group's shared blocks (0: unused)
+                } else {
+                    const int sb = b - p.num_real;
+                    const int32_t ctx = p.context_lens[sb];
+                    if (ctx < 0 || (int64_t)ctx > (int64_t)p.max_blocks * kBlockTokens) {
+                        if (blockIdx.x == 0)
+                            flag_error(p.dev_status, PA_DEV_BAD_CONTEXT_BIT);
+                    } else {
+                        v = (ctx + kBlockTokens - 1) / kBlockTokens - __ldg(p.skip + sb);
+                    }
+                }
             } else {
                 const int32_t ctx = p.context_lens[b];
                 if (ctx < 0 || (int64_t)ctx > (int64_t)p.max_blocks * kBlockTokens) {
@@ -174,36 +186,51 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
                         flag_error(p.dev_status, PA_DEV_BAD_CONTEXT_BIT);
                 } else {
                     // blocks from the first one the sequence reads (window / shared prefix)
-                    v = (ctx + kBlockTokens - 1) / kBlockTokens - seq_first_block(p, b, ctx);
+                    v = (ctx + kBlockTokens - 1) / kBlockTokens - seq_first_block(p, ctx);
                 }
             }
         }
-        int32_t x = v;
+        int32_t x = v, z = v > 0 ? 1 : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int32_t y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o)
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            const int32_t yz = __shfl_up_sync(0xffffffffu, z, o);
+            if (lane >= o) {
                 x += y;
+                z += yz;
+            }
         }
-        if (lane == 31)
+        if (lane == 31) {
             wsum[warp] = x;
+            wsum[8 + warp] = z;
+        }
         __syncthreads();
         if (warp == 0) {
             int32_t t = lane < NWARP ? wsum[lane] : 0;
+            int32_t tz = lane < NWARP ? wsum[8 + lane] : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                int32_t y = __shfl_up_sync(0xffffffffu, t, o);
-                if (lane >= o)
+                const int32_t y = __shfl_up_sync(0xffffffffu, t, o);
+                const int32_t yz = __shfl_up_sync(0xffffffffu, tz, o);
+                if (lane >= o) {
                     t += y;
+                    tz += yz;
+                }
             }
-            if (lane < NWARP)
+            if (lane < NWARP) {
                 wsum[lane] = t; // inclusive
+                wsum[8 + lane] = tz;
+            }
         }
         __syncthreads();
         const int32_t before = warp ? wsum[warp - 1] : 0;
-        if (b < p.num_seqs)
+        const int32_t zbefore = warp ? wsum[8 + warp - 1] : 0;
+        if (b < p.num_seqs) {
             P[b + 1] = carry + before + x;
+            Z[b + 1] = zcarry + zbefore + z;
+        }
         carry += wsum[NWARP - 1];
+        zcarry += wsum[8 + NWARP - 1];
         __syncthreads();
     }
 }
@@ -215,24 +242,30 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
 // first kSegCost positions stand for the merge, the rest for its blocks in
 // order. CTA c of G owns virtual [plan_lo(c, Wv, G), plan_lo(c+1, Wv, G)),
 // i.e. the contiguous real items whose virtual positions fall there, so a CTA
-// covering many short units gets fewer blocks. Every sequence (even an empty
-// one) carries n_kv * kSegCost, so the virtual prefix is P[b] + kSegCost * b.
-// The prefix pass charges nothing (p.seg_cost = 0): its few units are long.
+// covering many short units gets fewer blocks. Every sequence with blocks
+// carries n_kv * kSegCost, so the virtual prefix is P[b] + kSegCost * Z[b].
 // ---------------------------------------------------------------------------
 constexpr int kSegCost = 8;
 
 // Virtual position of the first block of unit (b, kvh) (nb = blocks of b).
+// Z = P + num_seqs + 1 counts the sequences with blocks: an empty sequence
+// has no segment and costs nothing.
+__device__ __forceinline__ int64_t virt_start(const DecodeParams &p, const int32_t *P, int b)
+{
+    const int32_t *Z = P + p.num_seqs + 1;
+    return (int64_t)p.n_kv * (P[b] + (int64_t)p.seg_cost * Z[b]);
+}
+
 __device__ __forceinline__ int64_t virt_first(const DecodeParams &p, const int32_t *P, int b,
                                               int kvh, int nb)
 {
-    return (int64_t)p.n_kv * (P[b] + (int64_t)p.seg_cost * b) + (int64_t)kvh * (nb + p.seg_cost) +
-           p.seg_cost;
+    return virt_start(p, P, b) + (int64_t)kvh * (nb + p.seg_cost) + p.seg_cost;
 }
 
 // Total virtual length.
 __device__ __forceinline__ int64_t virt_total(const DecodeParams &p, const int32_t *P)
 {
-    return (int64_t)p.n_kv * (P[p.num_seqs] + (int64_t)p.seg_cost * p.num_seqs);
+    return virt_start(p, P, p.num_seqs);
 }
 
 // First real item whose virtual position is >= y (W for y >= the total).
@@ -245,16 +278,16 @@ __device__ __forceinline__ int64_t real_at_virtual(const DecodeParams &p, const 
     const int64_t C = p.seg_cost;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if ((int64_t)p.n_kv * (P[mid] + C * mid) <= y)
+        if (virt_start(p, P, mid) <= y)
             lo = mid;
         else
             hi = mid;
     }
-    // b has a nonzero virtual length (C > 0, or blocks: an empty b would not
-    // be the largest b with a start <= y)
+    // b has blocks: an empty b has a zero virtual length, so it would not be
+    // the largest b with a start <= y
     const int b = lo;
     const int64_t nb = P[b + 1] - P[b], v = nb + C;
-    const int64_t r = y - (int64_t)p.n_kv * (P[b] + C * b);
+    const int64_t r = y - virt_start(p, P, b);
     const int64_t kvh = r / v, off = r - kvh * v;
     const int64_t base = (int64_t)p.n_kv * P[b] + kvh * nb;
     return off < C ? base : base + (off - C);
@@ -294,6 +327,18 @@ __device__ __forceinline__ void zero_empty_sequences(const DecodeParams &p, cons
         for (int i = threadIdx.x; i < rows16; i += blockDim.x)
             dst[i] = make_uint4(0, 0, 0, 0);
     }
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t *addr)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int32_t *addr, int v)
+{
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
 }
 
 // atom.add with acquire-release semantics at GPU scope: releases this CTA's
@@ -343,12 +388,20 @@ __device__ __forceinline__ void sink_scores(const DecodeParams &p, int b, int kv
 }
 
 // Row of query row v of unit (s, kvh) in q, out and pre, or -1 for a padding
-// row. Pass 0: qo_row. Pass 1 (s a group): member j = v / g of the group,
-// query head kvh * g + v % g of that sequence.
+// row. Pass 0: qo_row. Pass 2: for a group unit s, member j = v / g of the
+// group, query head kvh * g + v % g of that sequence; for a sequence's
+// remaining blocks, its g query heads.
 template <int GQ, int NQ, int PASS>
 __device__ __forceinline__ int64_t unit_row(const DecodeParams &p, int s, int kvh, int v)
 {
-    if constexpr (PASS == 1) {
+    if constexpr (PASS == 2) {
+        if (s >= p.num_real) { // a sequence's remaining blocks: its g query heads
+            if (v >= p.g)
+                return -1;
+            return ((int64_t)(s - p.num_real) * p.n_kv + kvh) * p.g + v;
+        }
+    }
+    if constexpr (PASS == 2) {
         const int j = v / p.g, h = v - j * p.g;
         if (j >= __ldg(p.groups + 3 * s + 1))
             return -1;
@@ -359,32 +412,21 @@ __device__ __forceinline__ int64_t unit_row(const DecodeParams &p, int s, int kv
     }
 }
 
-// Final (M, L, O) of query row h, column d: the bf16 output (pass 0) or the
-// unnormalised partial state in pre (pass 1).
-template <int D, int GQ, int NQ, int PASS>
-__device__ __forceinline__ void emit(const DecodeParams &p, int s, int kvh, int h, int d, float M,
+// Final (M, L, O) of query row h, column d of (sequence b, kv head kvh):
+// the bf16 output.
+template <int D, int GQ, int NQ>
+__device__ __forceinline__ void emit(const DecodeParams &p, int b, int kvh, int h, int d, float M,
                                      float L, float O)
 {
-    const int64_t row = unit_row<GQ, NQ, PASS>(p, s, kvh, h);
-    if constexpr (PASS == 1) {
-        if (row < 0)
-            return;
-        float *r = p.pre + row * (D + 2);
-        if (d == 0) {
-            r[0] = M;
-            r[1] = L;
-        }
-        r[2 + d] = O;
-    } else {
-        p.out[row * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
-    }
+    const size_t row = qo_row<GQ, NQ>(p, b, kvh, h);
+    p.out[row * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
 }
 
-template <int D, int GQ, int NW, int NQ, int PASS>
+template <int D, int GQ, int NW, int NQ>
 __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int32_t *P,
                                                const float *merge, int32_t *misc, float *sink_sc,
                                                int b, int kvh, int nb, int64_t Wv, int64_t G,
-                                               bool whole, int s_lo, int s_hi, bool pre_merge)
+                                               bool whole, int s_lo, int s_hi)
 {
     constexpr int NT = NW * 32;
     constexpr int REC = D + 2;
@@ -409,15 +451,6 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
         }
         for (int j = 0; j < ns; ++j)
             M = fmaxf(M, sink_sc[h * 16 + j]);
-        // the prefix pass's state of this query row joins as one more partial
-        float pm = -INFINITY, pl = 0.f, po = 0.f;
-        if (pre_merge) {
-            const float *pr = p.pre + unit_row<GQ, NQ, PASS>(p, b, kvh, h) * REC;
-            pm = pr[0];
-            pl = pr[1];
-            po = pr[2 + d];
-            M = fmaxf(M, pm);
-        }
         float O = 0.f, L = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
@@ -426,11 +459,6 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
                 L = fmaf(sc, merge[(w * GQ + h) * REC + 1], L);
                 O = fmaf(sc, merge[(w * GQ + h) * REC + 2 + d], O);
             }
-            if (pm != -INFINITY) {
-                const float sc = fast_exp2(pm - M);
-                L = fmaf(sc, pl, L);
-                O = fmaf(sc, po, O);
-            }
             for (int j = 0; j < ns; ++j) {
                 const float e = fast_exp2(sink_sc[h * 16 + j] - M);
                 L += e;
@@ -438,7 +466,7 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
             }
         }
         if (whole) {
-            emit<D, GQ, NQ, PASS>(p, b, kvh, h, d, M, L, O);
+            emit<D, GQ, NQ>(p, b, kvh, h, d, M, L, O);
         } else {
             if (d == 0) {
                 rec[h * REC] = M;
@@ -500,8 +528,216 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
                 }
             }
         }
-        emit<D, GQ, NQ, PASS>(p, b, kvh, h, d, M, L, O);
+        emit<D, GQ, NQ>(p, b, kvh, h, d, M, L, O);
     }
+}
+
+// ---------------------------------------------------------------------------
+// Fused shared-prefix pass (PASS 2). Units s < B are groups (their rows are
+// the query heads of every member); units s >= B are sequence b = s - B's
+// blocks after its group's prefix. Sequence b's output combines its own
+// records and, for a group member, the group's state in pre. Counting both
+// kinds of arrival on b's counter (nseg + 1 for a member), whichever comes
+// last merges: no CTA ever waits for another.
+// ---------------------------------------------------------------------------
+
+// CTAs owning the blocks of unit (s, kvh): first and count.
+__device__ __forceinline__ void unit_owners(const DecodeParams &p, const int32_t *P, int s,
+                                            int kvh, int64_t Wv, int64_t G, int64_t &c_first,
+                                            int &nseg)
+{
+    const int nb = P[s + 1] - P[s];
+    const int64_t v0 = virt_first(p, P, s, kvh, nb);
+    c_first = plan_owner(v0, Wv, G);
+    nseg = (int)(plan_owner(v0 + nb - 1, Wv, G) - c_first + 1);
+}
+
+// Output element (h, d) of sequence b, kv head kvh: its records, written
+// by CTAs c_first .. c_first + nseg - 1, and its group's prefix state.
+template <int D, int GQ>
+__device__ __forceinline__ void merge_element(const DecodeParams &p, int b, int kvh,
+                                              int64_t c_first, int nseg, int h, int d)
+{
+    constexpr int REC = D + 2;
+    const int u = (p.num_real + b) * p.n_kv + kvh;
+    const float *base = p.partials + ((size_t)c_first + u) * (GQ * REC) + h * REC;
+    const int64_t row = ((int64_t)b * p.n_kv + kvh) * p.g + h;
+    float M = -INFINITY, pm = -INFINITY, pl = 0.f, po = 0.f;
+    if (__ldg(p.skip + b) > 0) {
+        const float *pr = p.pre + row * REC;
+        pm = __ldcg(pr);
+        pl = __ldcg(pr + 1);
+        po = __ldcg(pr + 2 + d);
+        M = pm;
+    }
+    for (int j = 0; j < nseg; ++j)
+        M = fmaxf(M, __ldcg(base + (size_t)j * GQ * REC));
+    float O = 0.f, L = 0.f;
+    if (M != -INFINITY) {
+        if (pm != -INFINITY) {
+            const float sc = fast_exp2(pm - M);
+            L = sc * pl;
+            O = sc * po;
+        }
+        for (int j = 0; j < nseg; ++j) {
+            const float *r = base + (size_t)j * GQ * REC;
+            const float m = __ldcg(r);
+            const float sc = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
+            L = fmaf(sc, __ldcg(r + 1), L);
+            O = fmaf(sc, __ldcg(r + 2 + d), O);
+        }
+    }
+    p.out[row * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+}
+
+// One arrival on sequence b's counter, which expects nseg arrivals (+1 for
+// a group member). Returns whether this was the last; then the caller merges
+// and the counter is reset for the next launch.
+__device__ __forceinline__ bool arrive_one(const DecodeParams &p, const int32_t *P, int b,
+                                           int kvh, int64_t Wv, int64_t G, int64_t &c_first,
+                                           int &nseg)
+{
+    const int s = p.num_real + b, u = s * p.n_kv + kvh;
+    unit_owners(p, P, s, kvh, Wv, G, c_first, nseg);
+    const int expect = nseg + (__ldg(p.skip + b) > 0 ? 1 : 0);
+    const int old = atomic_add_acq_rel_gpu(&p.counters[u], 1);
+    const bool last = (old == expect - 1);
+    if (last)
+        p.counters[u] = 0;
+    return last;
+}
+
+// Arrivals of sequences b0 .. b0 + n - 1 (n <= 8), one thread each, then the
+// merges of those that arrived last, all threads together. Called by all
+// threads; the records and pre rows this CTA wrote are published by the
+// barrier before the release of each arrival.
+template <int D, int GQ, int NW>
+__device__ __forceinline__ void arrive_sequences(const DecodeParams &p, const int32_t *P,
+                                                 int32_t *misc, int b0, int n, int kvh,
+                                                 int64_t Wv, int64_t G)
+{
+    constexpr int NT = NW * 32;
+    int32_t *last = misc, *cf = misc + 8, *ns = misc + 16;
+    if (threadIdx.x < n) {
+        int64_t c_first;
+        int nseg;
+        const bool l = arrive_one(p, P, b0 + threadIdx.x, kvh, Wv, G, c_first, nseg);
+        last[threadIdx.x] = l;
+        cf[threadIdx.x] = (int32_t)c_first;
+        ns[threadIdx.x] = nseg;
+    }
+    __syncthreads();
+    const int per = p.g * D;
+#pragma unroll 1
+    for (int idx = threadIdx.x; idx < n * per; idx += NT) {
+        const int j = idx / per, r = idx - j * per;
+        if (last[j])
+            merge_element<D, GQ>(p, b0 + j, kvh, cf[j], ns[j], r / D, r % D);
+    }
+    __syncthreads(); // misc is reused by the next segment
+}
+
+template <int D, int GQ, int NW>
+__device__ __forceinline__ void finish_fused(const DecodeParams &p, const int32_t *P,
+                                             const float *merge, int32_t *misc, int s, int kvh,
+                                             int64_t Wv, int64_t G, bool whole)
+{
+    constexpr int NT = NW * 32, REC = D + 2;
+    const bool group = s < p.num_real;
+    const int b = s - p.num_real;
+    const bool member = !group && __ldg(p.skip + b) > 0;
+    const int u = s * p.n_kv + kvh;
+    float *rec = p.partials + ((size_t)blockIdx.x + u) * (GQ * REC);
+    const bool direct = whole && !group && !member; // a plain sequence in one piece
+    // live rows: a group's members' heads, else the sequence's g heads
+    const int rows = group ? __ldg(p.groups + 3 * s + 1) * p.g : p.g;
+    // warps' states -> this CTA's state of the unit: output or record
+#pragma unroll 1
+    for (int idx = threadIdx.x; idx < rows * D; idx += NT) {
+        const int h = idx / D, d = idx - h * D;
+        float mw[NW];
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            mw[w] = merge[(w * GQ + h) * REC];
+            M = fmaxf(M, mw[w]);
+        }
+        float O = 0.f, L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float sc = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
+                L = fmaf(sc, merge[(w * GQ + h) * REC + 1], L);
+                O = fmaf(sc, merge[(w * GQ + h) * REC + 2 + d], O);
+            }
+        }
+        if (direct) {
+            p.out[(((int64_t)b * p.n_kv + kvh) * p.g + h) * D + d] =
+                __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+        } else {
+            if (d == 0) {
+                rec[h * REC] = M;
+                rec[h * REC + 1] = L;
+            }
+            rec[h * REC + 2 + d] = O;
+        }
+    }
+    __syncthreads();
+    if (direct)
+        return;
+    if (!group) { // a piece of sequence b: one arrival
+        arrive_sequences<D, GQ, NW>(p, P, misc, b, 1, kvh, Wv, G);
+        return;
+    }
+    // a piece of group s: the last one merges the group's state into pre and
+    // then arrives once on every member's counter
+    if (threadIdx.x == 0) {
+        int64_t c_first;
+        int nseg;
+        unit_owners(p, P, s, kvh, Wv, G, c_first, nseg);
+        const int old = atomic_add_acq_rel_gpu(&p.counters[u], 1);
+        const int last = (old == nseg - 1);
+        if (last)
+            p.counters[u] = 0;
+        misc[0] = last;
+        misc[1] = (int)c_first;
+        misc[3] = nseg;
+    }
+    __syncthreads();
+    if (!misc[0]) {
+        __syncthreads(); // misc is reused by the next segment
+        return;
+    }
+    const int64_t c_first = misc[1];
+    const int nseg = misc[3];
+    const int b0 = __ldg(p.groups + 3 * s), n = __ldg(p.groups + 3 * s + 1);
+    const float *base = p.partials + ((size_t)c_first + u) * (GQ * REC);
+#pragma unroll 1
+    for (int idx = threadIdx.x; idx < n * p.g * D; idx += NT) {
+        const int h = idx / D, d = idx - h * D;
+        const int j = h / p.g;
+        float M = -INFINITY;
+        for (int k = 0; k < nseg; ++k)
+            M = fmaxf(M, __ldcg(base + (size_t)k * GQ * REC + h * REC));
+        float O = 0.f, L = 0.f;
+        if (M != -INFINITY) {
+            for (int k = 0; k < nseg; ++k) {
+                const float *r = base + (size_t)k * GQ * REC + h * REC;
+                const float m = __ldcg(r);
+                const float sc = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
+                L = fmaf(sc, __ldcg(r + 1), L);
+                O = fmaf(sc, __ldcg(r + 2 + d), O);
+            }
+        }
+        float *pr = p.pre + (((int64_t)(b0 + j) * p.n_kv + kvh) * p.g + (h - j * p.g)) * REC;
+        if (d == 0) {
+            pr[0] = M;
+            pr[1] = L;
+        }
+        pr[2 + d] = O;
+    }
+    __syncthreads(); // the pre rows are written (released by the arrivals below)
+    arrive_sequences<D, GQ, NW>(p, P, misc, b0, n, kvh, Wv, G);
 }
 
 // Byte offset of 16-byte chunk `c` of row `r` in a TMA-swizzled tile whose
@@ -547,8 +783,11 @@ __device__ __forceinline__ void load_item(const DecodeParams &p, const int32_t *
     int b, i, nb;
     locate_item(x, P, p.num_seqs, p.n_kv, b, kvh, i, nb);
     if constexpr (PASS == 0) {
-        if (p.window > 0 || p.skip)
-            i += seq_first_block(p, b, __ldg(p.context_lens + b));
+        if (p.window > 0)
+            i += seq_first_block(p, __ldg(p.context_lens + b));
+    } else if constexpr (PASS == 2) {
+        if (b >= p.num_real)
+            i += __ldg(p.skip + (b - p.num_real));
     }
     phys = __ldg(p.block_tables + (size_t)seq_table_row<PASS>(p, b) * p.max_blocks + i);
 }

@@ -38,13 +38,14 @@ template <int G>
 const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G>>),
                              Pol<G>::NW * 32, &smem_of<Pol<G>>, &launch_of<Pol<G>>};
 
-// Prefix pass of a shared-prefix decode: the query rows of up to kShareMembers(G)
-// sequences of a group (G heads each) share every K/V tile.
+// Shared-prefix decode, one launch: group units (the query rows of
+// up to kShareMembers(G) sequences, G heads each, share every K/V tile) and
+// then every sequence's remaining blocks.
 template <int G>
 const DecodeKernel kPrefix = {
-    reinterpret_cast<const void *>(&decode_kernel<Pol<G * kShareMembers(G)>, 1>),
+    reinterpret_cast<const void *>(&decode_kernel<Pol<G * kShareMembers(G)>, 2>),
     Pol<G * kShareMembers(G)>::NW * 32, &smem_of<Pol<G * kShareMembers(G)>>,
-    &launch_of<Pol<G * kShareMembers(G)>, 1>};
+    &launch_of<Pol<G * kShareMembers(G)>, 2>};
 
 } // namespace
 

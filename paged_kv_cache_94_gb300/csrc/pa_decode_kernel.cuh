@@ -310,8 +310,9 @@ namespace pa {
 // ---------------------------------------------------------------------------
 // The kernel: split, ring, segments, merge.
 // ---------------------------------------------------------------------------
-// PASS 0: decode (optionally skipping shared prefixes done by pass 1 and
-// merging their states); PASS 1: the prefix pass over groups of sequences.
+// PASS 0: decode of each sequence. PASS 2: shared-prefix decode, the groups'
+// shared blocks (all query rows of the group at once) and then every
+// sequence's remaining blocks, in one launch.
 template <class Pol, int PASS = 0>
 __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -339,8 +340,20 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     }
     prefix_blocks<NW * 32, PASS>(p, P, misc + 8);
     __syncthreads();
-    if constexpr (PASS == 0)
+    if constexpr (PASS == 0) {
         zero_empty_sequences<D, Pol::NQ>(p, P, n_h);
+    } else if constexpr (PASS == 2) {
+        // sequences with no blocks (ctx 0 or invalid) sit after the group units
+        const int nh = p.n_kv * p.g;
+        const int rows16 = nh * D * 2 / 16;
+        for (int b = blockIdx.x; b < p.num_real; b += p.num_ctas) {
+            if (P[p.num_real + b + 1] != P[p.num_real + b])
+                continue;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + (size_t)b * nh * D);
+            for (int i = threadIdx.x; i < rows16; i += blockDim.x)
+                dst[i] = make_uint4(0, 0, 0, 0);
+        }
+    }
     // Cost-weighted split on the virtual line (see virt_first). A CTA whose
     // virtual range holds no block does nothing; the CTAs owning a (sequence,
     // kv head) are exactly the owners of its first through last block, which
@@ -452,17 +465,23 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         const bool whole = (i0 == 0) && (unit_end <= hi);
         // Attended positions: [ws, ctx); the pool serves [max(ws, n_sink), ctx)
         // from logical block fb on, the sink rows serve [ws, min(n_sink, ctx)).
-        // A shared prefix done by the prefix pass starts the pool at block fb.
-        // Pass 1: a group's shared blocks, all full.
+        // Pass 2: a group's shared blocks are all full; a sequence's own
+        // blocks start after its group's, at block fb = skip[b].
         int32_t ctx, ws, pool_from, fb;
-        if constexpr (PASS == 1) {
-            ctx = nb * kBlockTokens;
-            ws = pool_from = fb = 0;
+        if constexpr (PASS == 2) {
+            ws = pool_from = 0;
+            if (b < p.num_real) { // a group's shared blocks, all full
+                ctx = nb * kBlockTokens;
+                fb = 0;
+            } else {              // a sequence's blocks after its group's prefix
+                ctx = __ldg(p.context_lens + (b - p.num_real));
+                fb = __ldg(p.skip + (b - p.num_real));
+            }
         } else {
             ctx = __ldg(p.context_lens + b);
             ws = window_start(p, ctx);
             pool_from = ws > p.n_sink ? ws : p.n_sink;
-            fb = seq_first_block(p, b, ctx);
+            fb = seq_first_block(p, ctx);
         }
 
         Pol::finish_q(st);
@@ -507,10 +526,12 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         Pol::to_merge(st, merge);
         __syncthreads();
         const int32_t s_hi = (PASS == 0 && i0_cur == 0 && p.n_sink > ws) ? min(p.n_sink, ctx) : 0;
-        const bool pre_merge = PASS == 0 && i0_cur == 0 && fb > 0 && p.skip != nullptr;
-        finish_segment<D, GQ, NW, Pol::NQ, PASS>(p, P, merge, misc, sink_sc, b_cur, kvh_cur,
-                                                 (int)nb_cur, Wv, G, whole, ws,
-                                                 s_hi > ws ? s_hi : ws, pre_merge);
+        if constexpr (PASS == 2)
+            finish_fused<D, GQ, NW>(p, P, merge, misc, b_cur, kvh_cur, Wv, G, whole);
+        else
+            finish_segment<D, GQ, NW, Pol::NQ>(p, P, merge, misc, sink_sc, b_cur, kvh_cur,
+                                               (int)nb_cur, Wv, G, whole, ws,
+                                               s_hi > ws ? s_hi : ws);
         seg_lo = seg_hi;
     }
 

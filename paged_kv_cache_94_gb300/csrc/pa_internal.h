@@ -28,9 +28,9 @@ struct DecodeKernel {
 const DecodeKernel *find_decode_kernel_bf16(int d_h, int group);
 const DecodeKernel *find_decode_kernel_int8(int d_h, int group);
 const DecodeKernel *find_decode_kernel_int4(int d_h, int group);
-// Shared-prefix decode: members per group of the prefix pass for group size
-// g (g * members <= 16 query rows per kv head), its kernels, and the group
-// detection kernel (pa_share.cu).
+// Shared-prefix decode: members per group for group size g (g * members <=
+// 16 query rows per kv head), its kernels, and the group detection kernel
+// (pa_share.cu).
 constexpr int kShareMembers(int g) { return g <= 2 ? 8 : 16 / g; }
 constexpr int kShareMinBlocks = 8;
 const DecodeKernel *find_prefix_kernel(int kv_dtype, int d_h, int group);

@@ -1,4 +1,4 @@
-// Shared-prefix groups for the prefix pass of a decode step.
+// Shared-prefix groups of a decode step.
 //
 // With prefix caching ("LLM 推理底层：KV Cache 显存几何、GQA/MLA 压缩与
 // PagedAttention 调度", section "Prefix Caching 与 Copy-on-Write"), sequences
