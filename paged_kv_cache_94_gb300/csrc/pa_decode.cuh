@@ -151,7 +151,7 @@ struct SmemLayout {
 // context length outside [0, max_blocks*16] counts as 0 blocks (and is
 // reported).
 // ---------------------------------------------------------------------------
-template <int NT, int PASS>
+template <int NT, int PASS, int BPI>
 __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P, int32_t *wsum)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -190,6 +190,7 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
                 }
             }
         }
+        v = (v + BPI - 1) / BPI; // items of BPI blocks
         int32_t x = v, z = v > 0 ? 1 : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -754,42 +755,65 @@ __device__ __forceinline__ uint32_t swz(int r, int c)
 // ---------------------------------------------------------------------------
 // Per-warp producer: the TMA ring and the block-table prefetch.
 // ---------------------------------------------------------------------------
+// An item is BPI consecutive blocks of one (sequence, kv head) unit; the
+// last item of a unit may hold fewer.
+template <int BPI>
 struct WarpRing {
-    int64_t lo;        // CTA range start
-    int64_t n_items;   // items this warp owns
+    int64_t lo;             // CTA range start
+    int64_t n_items;        // items this warp owns
     int warp;
-    int64_t issued;    // items whose loads were issued
-    int64_t batch;     // index of the 32-item batch held in the *_cur registers
-    int32_t phys_cur;  // lane l: physical block of item 32*batch + l (raw table entry)
-    int32_t kvh_cur;   //         and its kv head
-    int32_t phys_next; // the same for batch + 1
+    int64_t issued;         // items whose loads were issued
+    int64_t batch;          // index of the 32-item batch held in the *_cur registers
+    int32_t phys_cur[BPI];  // lane l: physical blocks of item 32*batch + l (raw table entries)
+    int32_t kvh_cur;        //         its kv head | (mask of absent blocks) << 16
+    int32_t phys_next[BPI]; // the same for batch + 1
     int32_t kvh_next;
 };
 
-// Block-table entry and kv head of this warp's item k. The loaded value is
-// not used here, so the load's latency overlaps other work; the entry is
-// checked when the item is issued.
-template <int NW, int PASS>
+// Block-table entries and kv head of this warp's item k. The loaded values
+// are not used here, so the loads' latency overlaps other work; the entries
+// are checked when the item is issued.
+template <int NW, int PASS, int BPI>
 __device__ __forceinline__ void load_item(const DecodeParams &p, const int32_t *P,
-                                          const WarpRing &r, int64_t k, int32_t &phys,
-                                          int32_t &kvh)
+                                          const WarpRing<BPI> &r, int64_t k,
+                                          int32_t (&phys)[BPI], int32_t &kvh)
 {
     if (k >= r.n_items) {
-        phys = -1;
+#pragma unroll
+        for (int j = 0; j < BPI; ++j)
+            phys[j] = -1;
         kvh = 0;
         return;
     }
     const int64_t x = r.lo + r.warp + k * NW;
     int b, i, nb;
     locate_item(x, P, p.num_seqs, p.n_kv, b, kvh, i, nb);
+    // first block of the item, and (BPI > 1) the blocks the unit reads
+    int first = i * BPI, nblk = 0;
     if constexpr (PASS == 0) {
-        if (p.window > 0)
-            i += seq_first_block(p, __ldg(p.context_lens + b));
+        if (p.window > 0 || BPI > 1) {
+            const int32_t ctx = __ldg(p.context_lens + b);
+            const int32_t fb = p.window > 0 ? seq_first_block(p, ctx) : 0;
+            first += fb;
+            nblk = (ctx + kBlockTokens - 1) / kBlockTokens;
+        }
     } else if constexpr (PASS == 2) {
-        if (b >= p.num_real)
-            i += __ldg(p.skip + (b - p.num_real));
+        if (b >= p.num_real) {
+            first += __ldg(p.skip + (b - p.num_real));
+            if constexpr (BPI > 1)
+                nblk = (__ldg(p.context_lens + (b - p.num_real)) + kBlockTokens - 1) / kBlockTokens;
+        } else if constexpr (BPI > 1) {
+            nblk = __ldg(p.groups + 3 * b + 2);
+        }
     }
-    phys = __ldg(p.block_tables + (size_t)seq_table_row<PASS>(p, b) * p.max_blocks + i);
+    const int32_t *row = p.block_tables + (size_t)seq_table_row<PASS>(p, b) * p.max_blocks;
+#pragma unroll
+    for (int j = 0; j < BPI; ++j) {
+        const bool present = j == 0 || first + j < nblk;
+        phys[j] = present ? __ldg(row + first + j) : -1;
+        if (!present)
+            kvh |= 1 << (16 + j);
+    }
 }
 
 } // namespace pa

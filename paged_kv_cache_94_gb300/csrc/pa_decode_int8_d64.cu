@@ -9,8 +9,20 @@
 #ifndef PA_INT8_D64_MINB
 #define PA_INT8_D64_MINB 1
 #endif
+#ifndef PA_INT8_D64_BPI
+#define PA_INT8_D64_BPI 2 // blocks per ring item
+#endif
 #ifndef PA_INT8_D64_STAGES
-#define PA_INT8_D64_STAGES 8
+#define PA_INT8_D64_STAGES 4
+#endif
+
+// The shared-prefix kernel keeps a GQ = g * members merge area per warp, so
+// its ring uses one-block items to leave room for the same CTAs per SM.
+#ifndef PA_INT8_D64_SHARE_BPI
+#define PA_INT8_D64_SHARE_BPI 1
+#endif
+#ifndef PA_INT8_D64_SHARE_STAGES
+#define PA_INT8_D64_SHARE_STAGES 8
 #endif
 
 namespace pa {
@@ -32,7 +44,8 @@ cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const Decode
 
 template <int G>
 using Pol = QuantMmaPolicy<8, 64, G, PA_INT8_D64_NW, PA_INT8_D64_STAGES,
-                           (G >= 16 ? 1 : PA_INT8_D64_MINB)>; // g = 16 needs its registers
+                           (G >= 16 ? 1 : PA_INT8_D64_MINB), // g = 16 needs its registers
+                           PA_INT8_D64_BPI>;
 
 template <int G>
 const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G>>),
@@ -42,10 +55,14 @@ const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G
 // up to kShareMembers(G) sequences, G heads each, share every K/V tile) and
 // then every sequence's remaining blocks.
 template <int G>
+using PolShare = QuantMmaPolicy<8, 64, G, PA_INT8_D64_NW, PA_INT8_D64_SHARE_STAGES,
+                                (G >= 16 ? 1 : PA_INT8_D64_MINB), PA_INT8_D64_SHARE_BPI>;
+
+template <int G>
 const DecodeKernel kPrefix = {
-    reinterpret_cast<const void *>(&decode_kernel<Pol<G * kShareMembers(G)>, 2>),
-    Pol<G * kShareMembers(G)>::NW * 32, &smem_of<Pol<G * kShareMembers(G)>>,
-    &launch_of<Pol<G * kShareMembers(G)>, 2>};
+    reinterpret_cast<const void *>(&decode_kernel<PolShare<G * kShareMembers(G)>, 2>),
+    PolShare<G * kShareMembers(G)>::NW * 32, &smem_of<PolShare<G * kShareMembers(G)>>,
+    &launch_of<PolShare<G * kShareMembers(G)>, 2>};
 
 } // namespace
 

@@ -65,6 +65,7 @@ struct Bf16Policy {
     static constexpr int kMinBlocks = 1;
     static constexpr bool kLsuLoad = false;           // tiles arrive by TMA (lane 0 issues)
     static constexpr uint32_t kArrivals = 1;
+    static constexpr int BPI = 1;                     // blocks per ring item
     static constexpr int NT = (GQ + 7) / 8;           // 8-head n-tiles
     static constexpr int KS = D / 16;                 // k-steps / m-tiles over D
     static constexpr int HALVES = D / 64;             // 64-column TMA boxes per tile
@@ -80,11 +81,6 @@ struct Bf16Policy {
         float m[NT][2], l[NT][2];
         float acc[NT][KS][4];   // O^T accumulators: rows d, cols heads
     };
-
-    __device__ static void issue_lanes(uint32_t, uint32_t, int32_t, const DecodeParams &,
-                                       const void *, const void *, uint64_t, int)
-    {
-    }
 
     __device__ static void issue(uint32_t dst, uint32_t /*extra*/, int32_t row, uint32_t bar,
                                  const CUtensorMap *tk, const CUtensorMap *tv,
@@ -338,7 +334,9 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
-    prefix_blocks<NW * 32, PASS>(p, P, misc + 8);
+    constexpr int BPI = Pol::BPI;                // blocks per item
+    constexpr int TOK = BPI * kBlockTokens;      // tokens per item
+    prefix_blocks<NW * 32, PASS, BPI>(p, P, misc + 8);
     __syncthreads();
     if constexpr (PASS == 0) {
         zero_empty_sequences<D, Pol::NQ>(p, P, n_h);
@@ -372,7 +370,7 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     __syncthreads();
 
     // ---- per-warp producer state
-    WarpRing r;
+    WarpRing<BPI> r;
     r.lo = lo;
     r.warp = warp;
     r.n_items = (hi - lo > warp) ? (hi - lo - warp + NW - 1) / NW : 0;
@@ -394,45 +392,54 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         const int64_t k = r.issued;
         const int64_t bt = k >> 5;
         if (bt != r.batch) {
-            r.phys_cur = r.phys_next;
+#pragma unroll
+            for (int j = 0; j < BPI; ++j)
+                r.phys_cur[j] = r.phys_next[j];
             r.kvh_cur = r.kvh_next;
             r.batch = bt;
             load_item<NW, PASS>(p, P, r, (bt + 1) * 32 + lane, r.phys_next, r.kvh_next);
         }
-        const int32_t phys = __shfl_sync(0xffffffffu, r.phys_cur, (int)(k & 31));
-        const int32_t kvh = __shfl_sync(0xffffffffu, r.kvh_cur, (int)(k & 31));
+        const int32_t kw = __shfl_sync(0xffffffffu, r.kvh_cur, (int)(k & 31));
+        const int32_t kvh = kw & 0xffff;
+        // rows of the item's blocks in the pool; mask: the blocks to load
+        int32_t rows[BPI];
+        uint32_t mask = 0;
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < BPI; ++j) {
+            const int32_t phys = __shfl_sync(0xffffffffu, r.phys_cur[j], (int)(k & 31));
+            const bool absent = (kw >> (16 + j)) & 1;
+            const bool bad_j = !absent && (phys < 0 || (int64_t)phys >= p.num_blocks);
+            bad |= bad_j;
+            rows[j] = (absent || bad_j) ? -1 : phys * p.n_kv + kvh;
+            mask |= (rows[j] >= 0 ? 1u : 0u) << j;
+        }
+        const uint32_t bar = bar_base + 8u * istage;
+        if (lane == 0) {
+            wmeta[istage] = (int32_t)mask;
+            if (bad)
+                flag_error(p.dev_status, PA_DEV_BAD_BLOCK_BIT);
+        }
         if constexpr (Pol::kLsuLoad) {
             // every lane copies its share and arrives when its copies land
-            const uint32_t bar = bar_base + 8u * istage;
-            const bool bad = phys < 0 || (int64_t)phys >= p.num_blocks;
-            const int32_t row = bad ? -1 : phys * p.n_kv + kvh;
-            if (lane == 0) {
-                wmeta[istage] = row;
-                if (bad)
-                    flag_error(p.dev_status, PA_DEV_BAD_BLOCK_BIT);
-            }
-            if (bad) {
+            if (mask == 0) {
                 mbar_arrive(bar); // the phase completes with no data: the item is skipped
             } else {
                 Pol::issue_lanes(ring_base + (uint32_t)(istage * Pol::STAGE),
-                                 extra_base + (uint32_t)(istage * Pol::EXTRA), row, p, p.k_cache,
+                                 extra_base + (uint32_t)(istage * Pol::EXTRA), rows, p, p.k_cache,
                                  p.v_cache, pol, lane);
                 cp_async_mbar_arrive_noinc(bar);
             }
         } else if (lane == 0) {
-            const uint32_t bar = bar_base + 8u * istage;
-            const bool bad = phys < 0 || (int64_t)phys >= p.num_blocks;
-            const int32_t row = bad ? -1 : phys * p.n_kv + kvh;
-            wmeta[istage] = row;
-            if (bad) {
-                flag_error(p.dev_status, PA_DEV_BAD_BLOCK_BIT);
+            static_assert(Pol::kLsuLoad || BPI == 1, "TMA stages hold one block");
+            if (mask == 0) {
                 mbar_arrive(bar); // completes the phase with no data: the item is skipped
             } else {
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(bar, Pol::TX);
                 Pol::issue(ring_base + (uint32_t)(istage * Pol::STAGE),
-                           extra_base + (uint32_t)(istage * Pol::EXTRA), row, bar, &tmK, &tmV, p,
-                           pol);
+                           extra_base + (uint32_t)(istage * Pol::EXTRA), rows[0], bar, &tmK, &tmV,
+                           p, pol);
             }
         }
         __syncwarp();
@@ -471,7 +478,7 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         if constexpr (PASS == 2) {
             ws = pool_from = 0;
             if (b < p.num_real) { // a group's shared blocks, all full
-                ctx = nb * kBlockTokens;
+                ctx = __ldg(p.groups + 3 * b + 2) * kBlockTokens;
                 fb = 0;
             } else {              // a sequence's blocks after its group's prefix
                 ctx = __ldg(p.context_lens + (b - p.num_real));
@@ -497,14 +504,22 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
                 if (lane == 0)
                     flag_error(p.dev_status, PA_DEV_TIMEOUT_BIT);
             }
-            if (ok && wmeta[cstage] >= 0) {
-                const int32_t t0 = (fb + (int32_t)(x - unit_start)) * kBlockTokens;
-                const int lo = pool_from > t0 ? (int)min(pool_from - t0, kBlockTokens) : 0;
-                const int rem = (int)min(ctx - t0, 2 * kBlockTokens); // >= 16 + NQ - 1
-                const int valid = (int)min(rem, kBlockTokens);
-                Pol::compute(st, ring_base + (uint32_t)(cstage * Pol::STAGE),
-                             extra_base + (uint32_t)(cstage * Pol::EXTRA), lo, valid, rem,
-                             p.scale_log2);
+            const int32_t mask = ok ? wmeta[cstage] : 0;
+            if (mask != 0) {
+                const int32_t t0 = (fb + BPI * (int32_t)(x - unit_start)) * kBlockTokens;
+                int lo = pool_from > t0 ? (int)min(pool_from - t0, TOK) : 0;
+                const int rem = (int)min(ctx - t0, TOK + kBlockTokens); // >= TOK + NQ - 1
+                int valid = (int)min(rem, TOK);
+                if constexpr (BPI == 2) { // a bad block's tokens are not attended
+                    if (!(mask & 1))
+                        lo = max(lo, kBlockTokens);
+                    if (!(mask & 2))
+                        valid = min(valid, kBlockTokens);
+                }
+                if (lo < valid)
+                    Pol::compute(st, ring_base + (uint32_t)(cstage * Pol::STAGE),
+                                 extra_base + (uint32_t)(cstage * Pol::EXTRA), lo, valid, rem,
+                                 p.scale_log2);
             }
             __syncwarp();
             if (!dead && r.issued < r.n_items)

@@ -21,6 +21,11 @@
 //       (d on M, so the query group only pads N to 8; the rows of O^T are
 //        permuted so each thread's A fragments for all D/16 row tiles come
 //        from one load of each of its four token rows)
+// INT4 codes take one AND-XOR each (no shifts into place): the nibble at
+// bits 0-3 of a 16-bit half becomes 1024 + (c + 8) = 1032 + c, the nibble at
+// bits 4-7 becomes 1024 + 16 (c + 8) = 1152 + 16 c. The two kinds feed
+// separate accumulators (Q.K: even and odd k-steps; V: even and odd d rows),
+// each with its own bias, and the x16 ones are divided by 16 at the end.
 // Q' = q * 2^-e with e >= 0 chosen per (sequence, kv head) so that
 // max|Q'| < 2^15: the bf16 -> fp16 conversion is then exact for every
 // normal value. W = p * v_scale[tok] / s_base, where s_base is a running
@@ -84,12 +89,18 @@ __device__ __forceinline__ float lds_f32(uint32_t addr)
     return v;
 }
 
-// Two 4-bit codes (offset form, nibbles j and j+4 of `w`) -> fp16x2
-// {1032 + code_j, 1032 + code_j+4} (biased as bytes_to_h2).
-template <int J>
-__device__ __forceinline__ uint32_t nibs_to_h2(uint32_t w)
+// INT4 codes (two's complement nibbles) -> fp16x2. nib_lo: the nibbles at
+// bits 0-3 and 16-19 of w as {1032 + c0, 1032 + c1}; nib_hi: those at bits
+// 4-7 and 20-23 as {1152 + 16 c0, 1152 + 16 c1}. XOR with 8 (in place) turns
+// a code into its offset form c + 8, which lies inside the mantissa of 1024.
+__device__ __forceinline__ uint32_t nib_lo(uint32_t w)
 {
-    return ((w >> (4 * J)) & 0x000F000Fu) | 0x64006400u;
+    return (w & 0x000F000Fu) ^ 0x64086408u;
+}
+
+__device__ __forceinline__ uint32_t nib_hi(uint32_t w)
+{
+    return (w & 0x00F000F0u) ^ 0x64806480u;
 }
 
 // fp32 values of the two halves of an fp16x2.
@@ -108,22 +119,27 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 }
 
 // ---------------------------------------------------------------------------
-template <int BITS, int D_, int GQ_, int NW_, int S_, int MINB_ = 1>
+template <int BITS, int D_, int GQ_, int NW_, int S_, int MINB_ = 1, int BPI_ = 2>
 struct QuantMmaPolicy {
     static_assert(BITS == 8 || BITS == 4, "INT8 or INT4 codes");
+    static_assert(BPI_ == 1 || BPI_ == 2, "one or two blocks per ring item");
     static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_, NQ = 1;
+    static constexpr int BPI = BPI_;               // blocks per ring item
     static constexpr int kMinBlocks = MINB_;       // resident CTAs per SM the registers allow
     static constexpr int NT = (GQ + 7) / 8;        // 8-head tiles of S^T
     static constexpr int KS = D / 16;              // k-steps of Q.K
     static constexpr int CW = D / 8;               // d values of O^T per thread (see to_merge)
     static constexpr int ROWB = D * BITS / 8;      // bytes per code row: 128/64 (8), 64/32 (4)
     static constexpr int TILE = kBlockTokens * ROWB; // bytes of a K (or V) code tile
-    static constexpr int STAGE = 2 * TILE;
-    static constexpr int EXTRA = 128;              // 16 K scales + 16 V scales
+    // A stage: the K tiles of the item's blocks, then their V tiles; the
+    // extra area: 16 K scales per block, then 16 V scales per block.
+    static constexpr int STAGE = 2 * BPI * TILE;
+    static constexpr int EXTRA = 128 * BPI;
     static constexpr int QBYTES = 0;
     static constexpr uint32_t TX = STAGE + EXTRA;
     static constexpr float kScaleRatio = 64.f;     // V-scale base moves beyond this
     static constexpr float kBias = BITS == 8 ? 1152.f : 1032.f; // fp16 value of code 0
+    static constexpr float kBiasHi = 1152.f;       // INT4, x16 nibbles: 1152 + 16 c
     using Layout = SmemLayout<D, GQ, NW, S, STAGE, EXTRA, QBYTES>;
 
     struct State {
@@ -133,14 +149,16 @@ struct QuantMmaPolicy {
         float acc[NT][KS][4];   // O^T accumulators: rows permuted d, cols heads
         float sbase;            // V-scale base of acc (0 until a nonzero scale is seen)
         float sinv;             // 1 / sbase (0 while sbase is 0)
-        float qsum[NT][2];      // sum_d of the fp16 Q' values of head 2t4 + e
+        float qsum[NT][2];      // sum_d of the fp16 Q' values of head 2t4 + e (INT4: even k-steps)
+        float qsum1[NT][2];     // INT4: the same over the odd k-steps
         float wpart[NT][2];     // this lane's sum of the fp16 weights of head 2t4 + e
     };
 
     // Tiles of 1-2 KiB move faster as 16-byte cp.async copies spread over the
     // warp's lanes than as TMA boxes: every lane issues its share of the K
-    // and V tiles (and lanes 0-7 the 128 bytes of scales), then arrives on the
-    // stage barrier once its copies land (the barrier expects 32 arrivals).
+    // and V tiles (and lanes 0-8*BPI-1 the scales), then arrives on the stage
+    // barrier once its copies land (the barrier expects 32 arrivals). A block
+    // whose row is < 0 (absent or bad) is not loaded.
     static constexpr bool kLsuLoad = true;
     static constexpr uint32_t kArrivals = 32;
     static constexpr int CHUNKS = TILE / 16;       // 16-byte chunks per tile
@@ -156,34 +174,39 @@ struct QuantMmaPolicy {
             return (uint32_t)(c * 16);
     }
 
-    __device__ static void issue_lanes(uint32_t dst, uint32_t extra, int32_t row,
+    __device__ static void issue_lanes(uint32_t dst, uint32_t extra, const int32_t (&rows)[BPI],
                                        const DecodeParams &p, const void *kc, const void *vc,
                                        uint64_t pol, int lane)
     {
-        const uint8_t *ks = static_cast<const uint8_t *>(kc) + (size_t)row * TILE;
-        const uint8_t *vs = static_cast<const uint8_t *>(vc) + (size_t)row * TILE;
 #pragma unroll
-        for (int c = lane; c < CHUNKS; c += 32) {
-            cp_async_16(dst + chunk_off(c), ks + 16 * c, pol);
-            cp_async_16(dst + TILE + chunk_off(c), vs + 16 * c, pol);
+        for (int j = 0; j < BPI; ++j) {
+            if (rows[j] < 0)
+                continue;
+            const uint8_t *ks = static_cast<const uint8_t *>(kc) + (size_t)rows[j] * TILE;
+            const uint8_t *vs = static_cast<const uint8_t *>(vc) + (size_t)rows[j] * TILE;
+#pragma unroll
+            for (int c = lane; c < CHUNKS; c += 32) {
+                cp_async_16(dst + j * TILE + chunk_off(c), ks + 16 * c, pol);
+                cp_async_16(dst + (BPI + j) * TILE + chunk_off(c), vs + 16 * c, pol);
+            }
         }
-        if (lane < 8) {
-            const float *sc = (lane < 4 ? p.k_scale : p.v_scale) + (size_t)row * kBlockTokens;
-            cp_async_16(extra + 16 * lane, sc + 4 * (lane & 3), pol);
+        if (lane < 8 * BPI) {
+            const int t = lane >> 2, kind = t / BPI, j = t - kind * BPI; // t = kind*BPI + j
+            const int32_t rj = j == 0 ? rows[0] : rows[BPI - 1];           // no local array
+            if (rj >= 0) {
+                const float *sc = (kind ? p.v_scale : p.k_scale) + (size_t)rj * kBlockTokens;
+                cp_async_16(extra + 64 * t + 16 * (lane & 3), sc + 4 * (lane & 3), pol);
+            }
         }
-    }
-
-    __device__ static void issue(uint32_t, uint32_t, int32_t, uint32_t, const CUtensorMap *,
-                                 const CUtensorMap *, const DecodeParams &, uint64_t)
-    {
     }
 
     // Physical d of the k values thread t holds in k-step kk; the A and B
     // fragments agree on this permutation, so the dot product is unchanged.
     //   INT8: register 0 = (d0, d0+1), register 1 = (d0+2, d0+3), d0 below
     //         (four consecutive bytes of one 16-byte chunk of the row).
-    //   INT4: register r = (d, d+4) with d = D/4*t + 8*(kk/2) + 2*(kk%2) + r
-    //         (nibbles j, j+4 of one 32-bit word of the thread's slice).
+    //   INT4: register r = (d, d+4) with d = D/4*t + 8*(kk/2) + (kk%2) + 2*r
+    //         (nibbles j, j+4 of one 32-bit word of the thread's slice; odd
+    //         k-steps hold the x16 nibbles).
     __device__ static int kperm_d0(int kk, int t) { return 64 * (kk >> 2) + 16 * t + 4 * (kk & 3); }
 
     // Issue the loads of a segment's raw bf16 q words into st.qf (they land
@@ -250,11 +273,11 @@ struct QuantMmaPolicy {
                         x[2 * i + 1] = __uint_as_float(ww[i] & 0xffff0000u);
                     }
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) { // k-step 2*wi + h: nibbles 2h, 2h+1 (+4)
-                        qv[nt][2 * wi + h][0] = x[2 * h];
-                        qv[nt][2 * wi + h][1] = x[2 * h + 4];
-                        qv[nt][2 * wi + h][2] = x[2 * h + 1];
-                        qv[nt][2 * wi + h][3] = x[2 * h + 5];
+                    for (int h = 0; h < 2; ++h) { // k-step 2*wi + h: nibbles h, h+2 (+4)
+                        qv[nt][2 * wi + h][0] = x[h];
+                        qv[nt][2 * wi + h][1] = x[h + 4];
+                        qv[nt][2 * wi + h][2] = x[h + 2];
+                        qv[nt][2 * wi + h][3] = x[h + 6];
                     }
                 }
             }
@@ -274,7 +297,9 @@ struct QuantMmaPolicy {
         const float down = __uint_as_float((uint32_t)(127 - e) << 23);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            float part = 0.f; // sum of this thread's fp16 values of head nt*8 + gid
+            // sums of this thread's fp16 values of head nt*8 + gid: even and
+            // odd k-steps (INT8 adds both)
+            float part[2] = {0.f, 0.f};
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
                 st.qf[nt][kk][0] = pack_f16x2(qv[nt][kk][0] * down, qv[nt][kk][1] * down);
@@ -283,15 +308,20 @@ struct QuantMmaPolicy {
                 for (int r = 0; r < 2; ++r) {
                     float lo, hi;
                     h2_to_f2(st.qf[nt][kk][r], lo, hi);
-                    part += lo + hi;
+                    part[BITS == 4 ? (kk & 1) : 0] += lo + hi;
                 }
             }
-            part += __shfl_xor_sync(0xffffffffu, part, 1);
-            part += __shfl_xor_sync(0xffffffffu, part, 2);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                part[i] += __shfl_xor_sync(0xffffffffu, part[i], 1);
+                part[i] += __shfl_xor_sync(0xffffffffu, part[i], 2);
+            }
             // score columns are heads 2t4 + e: their sums sit in lanes 4 (2t4 + e)
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-                st.qsum[nt][e] = __shfl_sync(0xffffffffu, part, 4 * (2 * t4 + e));
+            for (int e = 0; e < 2; ++e) {
+                st.qsum[nt][e] = __shfl_sync(0xffffffffu, part[0], 4 * (2 * t4 + e));
+                st.qsum1[nt][e] = __shfl_sync(0xffffffffu, part[1], 4 * (2 * t4 + e));
+            }
         }
     }
 
@@ -320,87 +350,107 @@ struct QuantMmaPolicy {
                 st.wpart[nt][e] = 0.f;
     }
 
-    // One 16-token block: K codes at kt, V codes at kt + TILE, scales at extra
-    // (16 K scales, then 16 V scales). Rows [lo, valid) are attended.
+    // One item of BPI 16-token blocks: block j's K codes at kt + j*TILE, its V
+    // codes at kt + (BPI+j)*TILE, its scales at extra + 64*j (K) and
+    // extra + 64*(BPI+j) (V). Tokens [lo, valid) of the item are attended.
     __device__ static void compute(State &st, uint32_t kt, uint32_t extra, int lo, int valid,
                                    int /*rem*/, float scale_log2)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
-        const uint32_t vt = kt + TILE;
 
-        // ---- S^T = Kcode . Q'^T (two accumulator chains for ILP)
-        float s0[NT][4], s1[NT][4];
+        // ---- S^T = Kcode . Q'^T per block (two accumulator chains per block)
+        float s0[BPI][NT][4], s1[BPI][NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int j = 0; j < BPI; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                s0[nt][e] = s1[nt][e] = 0.f;
-        auto kstep = [&](int kk, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    s0[j][nt][e] = s1[j][nt][e] = 0.f;
+        auto kstep = [&](int j, int kk, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 if (kk & 1)
-                    mma_f16_16816(s1[nt], a0, a1, a2, a3, st.qf[nt][kk][0], st.qf[nt][kk][1]);
+                    mma_f16_16816(s1[j][nt], a0, a1, a2, a3, st.qf[nt][kk][0], st.qf[nt][kk][1]);
                 else
-                    mma_f16_16816(s0[nt], a0, a1, a2, a3, st.qf[nt][kk][0], st.qf[nt][kk][1]);
+                    mma_f16_16816(s0[j][nt], a0, a1, a2, a3, st.qf[nt][kk][0], st.qf[nt][kk][1]);
             }
         };
         if constexpr (BITS == 8) {
             // rows gid, gid+8: 16-byte chunks 4*g4 + t4 (swizzled), 16 codes each
 #pragma unroll
-            for (int g4 = 0; g4 < D / 64; ++g4) {
-                const uint4 ka = lds128(kt + swz<ROWB>(gid, 4 * g4 + t4));
-                const uint4 kb = lds128(kt + swz<ROWB>(gid + 8, 4 * g4 + t4));
-                const uint32_t wa[4] = {ka.x ^ 0x80808080u, ka.y ^ 0x80808080u,
-                                        ka.z ^ 0x80808080u, ka.w ^ 0x80808080u};
-                const uint32_t wb[4] = {kb.x ^ 0x80808080u, kb.y ^ 0x80808080u,
-                                        kb.z ^ 0x80808080u, kb.w ^ 0x80808080u};
+            for (int g4 = 0; g4 < D / 64; ++g4)
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    kstep(4 * g4 + j, bytes_to_h2<0x4140>(wa[j]), bytes_to_h2<0x4140>(wb[j]),
-                          bytes_to_h2<0x4342>(wa[j]), bytes_to_h2<0x4342>(wb[j]));
-            }
+                for (int j = 0; j < BPI; ++j) {
+                    const uint32_t kj = kt + j * TILE;
+                    const uint4 ka = lds128(kj + swz<ROWB>(gid, 4 * g4 + t4));
+                    const uint4 kb = lds128(kj + swz<ROWB>(gid + 8, 4 * g4 + t4));
+                    const uint32_t wa[4] = {ka.x ^ 0x80808080u, ka.y ^ 0x80808080u,
+                                            ka.z ^ 0x80808080u, ka.w ^ 0x80808080u};
+                    const uint32_t wb[4] = {kb.x ^ 0x80808080u, kb.y ^ 0x80808080u,
+                                            kb.z ^ 0x80808080u, kb.w ^ 0x80808080u};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        kstep(j, 4 * g4 + i, bytes_to_h2<0x4140>(wa[i]), bytes_to_h2<0x4140>(wb[i]),
+                              bytes_to_h2<0x4342>(wa[i]), bytes_to_h2<0x4342>(wb[i]));
+                }
         } else {
             // rows gid, gid+8: the thread's D/8 contiguous bytes (D/4 codes), unswizzled
-            uint32_t wa[KS / 2], wb[KS / 2];
-            if constexpr (D == 128) {
-                const uint4 ka = lds128(kt + gid * ROWB + 16 * t4);
-                const uint4 kb = lds128(kt + (gid + 8) * ROWB + 16 * t4);
-                wa[0] = ka.x; wa[1] = ka.y; wa[2] = ka.z; wa[3] = ka.w;
-                wb[0] = kb.x; wb[1] = kb.y; wb[2] = kb.z; wb[3] = kb.w;
-            } else {
-                const uint2 ka = lds64(kt + gid * ROWB + 8 * t4);
-                const uint2 kb = lds64(kt + (gid + 8) * ROWB + 8 * t4);
-                wa[0] = ka.x; wa[1] = ka.y;
-                wb[0] = kb.x; wb[1] = kb.y;
-            }
 #pragma unroll
-            for (int wi = 0; wi < KS / 2; ++wi) {
-                const uint32_t xa = wa[wi] ^ 0x88888888u, xb = wb[wi] ^ 0x88888888u;
-                kstep(2 * wi, nibs_to_h2<0>(xa), nibs_to_h2<0>(xb), nibs_to_h2<1>(xa),
-                      nibs_to_h2<1>(xb));
-                kstep(2 * wi + 1, nibs_to_h2<2>(xa), nibs_to_h2<2>(xb), nibs_to_h2<3>(xa),
-                      nibs_to_h2<3>(xb));
+            for (int j = 0; j < BPI; ++j) {
+                const uint32_t kj = kt + j * TILE;
+                uint32_t wa[KS / 2], wb[KS / 2];
+                if constexpr (D == 128) {
+                    const uint4 ka = lds128(kj + gid * ROWB + 16 * t4);
+                    const uint4 kb = lds128(kj + (gid + 8) * ROWB + 16 * t4);
+                    wa[0] = ka.x; wa[1] = ka.y; wa[2] = ka.z; wa[3] = ka.w;
+                    wb[0] = kb.x; wb[1] = kb.y; wb[2] = kb.z; wb[3] = kb.w;
+                } else {
+                    const uint2 ka = lds64(kj + gid * ROWB + 8 * t4);
+                    const uint2 kb = lds64(kj + (gid + 8) * ROWB + 8 * t4);
+                    wa[0] = ka.x; wa[1] = ka.y;
+                    wb[0] = kb.x; wb[1] = kb.y;
+                }
+#pragma unroll
+                for (int wi = 0; wi < KS / 2; ++wi) {
+                    // nibbles 0, 4 and (after >> 8) 2, 6: even k-step; 1, 5 and 3, 7 (x16): odd
+                    const uint32_t xa = wa[wi], xb = wb[wi], ya = xa >> 8, yb = xb >> 8;
+                    kstep(j, 2 * wi, nib_lo(xa), nib_lo(xb), nib_lo(ya), nib_lo(yb));
+                    kstep(j, 2 * wi + 1, nib_hi(xa), nib_hi(xb), nib_hi(ya), nib_hi(yb));
+                }
             }
         }
 
-        // ---- scores in the log2 domain; rows gid, gid+8 are tokens
-        const bool lo_ok = gid >= lo && gid < valid, hi_ok = gid + 8 >= lo && gid + 8 < valid;
-        const float f_lo = st.qexp * lds_f32(extra + 4 * gid) * scale_log2;
-        const float f_hi = st.qexp * lds_f32(extra + 4 * (gid + 8)) * scale_log2;
-        float pr[NT][4];
+        // ---- scores in the log2 domain; rows gid, gid+8 of block j are
+        // tokens 16j + gid, 16j + gid + 8
+        bool lo_ok[BPI], hi_ok[BPI];
+        float pr[BPI][NT][4];
         bool need = false; // some lane's score exceeds its column's base by 2^kRescaleLog2
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            // S^T element c: token row gid (c < 2) or gid+8, head column 2t4 + (c & 1)
+        for (int j = 0; j < BPI; ++j) {
+            const int tl = 16 * j + gid, th = tl + 8;
+            lo_ok[j] = tl >= lo && tl < valid;
+            hi_ok[j] = th >= lo && th < valid;
+            const float f_lo = st.qexp * lds_f32(extra + 64 * j + 4 * gid) * scale_log2;
+            const float f_hi = st.qexp * lds_f32(extra + 64 * j + 4 * (gid + 8)) * scale_log2;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float sb = s0[nt][c] + s1[nt][c];
-                const float sc = fmaf(-kBias, st.qsum[nt][c & 1], sb) * ((c & 2) ? f_hi : f_lo);
-                pr[nt][c] = ((c & 2) ? hi_ok : lo_ok) ? sc : -INFINITY;
+            for (int nt = 0; nt < NT; ++nt) {
+                // S^T element c: token row gid (c < 2) or gid+8, head column 2t4 + (c & 1)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float sb;
+                    if constexpr (BITS == 8)
+                        sb = fmaf(-kBias, st.qsum[nt][c & 1], s0[j][nt][c] + s1[j][nt][c]);
+                    else
+                        sb = fmaf(fmaf(-kBiasHi, st.qsum1[nt][c & 1], s1[j][nt][c]), 0.0625f,
+                                  fmaf(-kBias, st.qsum[nt][c & 1], s0[j][nt][c]));
+                    const float sc = sb * ((c & 2) ? f_hi : f_lo);
+                    pr[j][nt][c] = ((c & 2) ? hi_ok[j] : lo_ok[j]) ? sc : -INFINITY;
+                }
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                    need |= fmaxf(pr[j][nt][e], pr[j][nt][e + 2]) > st.m[nt][e] + kRescaleLog2;
             }
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-                need |= fmaxf(pr[nt][e], pr[nt][e + 2]) > st.m[nt][e] + kRescaleLog2;
         }
         // Lazy rescale (as in the bf16 policy), and the column maxima are only
         // reduced across the lanes when some lane exceeds its base.
@@ -409,7 +459,10 @@ struct QuantMmaPolicy {
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    float mx = fmaxf(pr[nt][e], pr[nt][e + 2]);
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < BPI; ++j)
+                        mx = fmaxf(mx, fmaxf(pr[j][nt][e], pr[j][nt][e + 2]));
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -431,17 +484,24 @@ struct QuantMmaPolicy {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const float base = (st.m[nt][e] == -INFINITY) ? 0.f : st.m[nt][e];
-                pr[nt][e] = fast_exp2(pr[nt][e] - base);
-                pr[nt][e + 2] = fast_exp2(pr[nt][e + 2] - base);
-                st.l[nt][e] += pr[nt][e] + pr[nt][e + 2];
+#pragma unroll
+                for (int j = 0; j < BPI; ++j) {
+                    pr[j][nt][e] = fast_exp2(pr[j][nt][e] - base);
+                    pr[j][nt][e + 2] = fast_exp2(pr[j][nt][e + 2] - base);
+                    st.l[nt][e] += pr[j][nt][e] + pr[j][nt][e + 2];
+                }
             }
 
         // ---- V scales: fold sv / s_base into the weights; the base moves only
         // when some row's scale exceeds it kScaleRatio-fold (then to the max)
-        const float sv_lo = lo_ok ? lds_f32(extra + 64 + 4 * gid) : 0.f;
-        const float sv_hi = hi_ok ? lds_f32(extra + 64 + 4 * (gid + 8)) : 0.f;
-        if (__any_sync(0xffffffffu, fmaxf(sv_lo, sv_hi) > st.sbase * kScaleRatio)) {
-            float svm = fmaxf(sv_lo, sv_hi);
+        float sv_lo[BPI], sv_hi[BPI], svm = 0.f;
+#pragma unroll
+        for (int j = 0; j < BPI; ++j) {
+            sv_lo[j] = lo_ok[j] ? lds_f32(extra + 64 * (BPI + j) + 4 * gid) : 0.f;
+            sv_hi[j] = hi_ok[j] ? lds_f32(extra + 64 * (BPI + j) + 4 * (gid + 8)) : 0.f;
+            svm = fmaxf(svm, fmaxf(sv_lo[j], sv_hi[j]));
+        }
+        if (__any_sync(0xffffffffu, svm > st.sbase * kScaleRatio)) {
             svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, 4));
             svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, 8));
             svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, 16));
@@ -462,97 +522,106 @@ struct QuantMmaPolicy {
             st.sbase = svm;
             st.sinv = 1.f / svm;
         }
-        const float r_lo = sv_lo * st.sinv, r_hi = sv_hi * st.sinv;
         // W^T as B fragments (tokens x heads): transpose of the score layout.
         // The lane's weights, as rounded to fp16, join its bias sums.
-        uint32_t pb0[NT], pb1[NT];
+        uint32_t pb0[BPI][NT], pb1[BPI][NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const uint32_t w0 = pack_f16x2(pr[nt][0] * r_lo, pr[nt][1] * r_lo);
-            const uint32_t w1 = pack_f16x2(pr[nt][2] * r_hi, pr[nt][3] * r_hi);
-            float a, b, c, d;
-            h2_to_f2(w0, a, b);
-            h2_to_f2(w1, c, d);
-            st.wpart[nt][0] += a + c;
-            st.wpart[nt][1] += b + d;
-            pb0[nt] = movmatrix_trans(w0);
-            pb1[nt] = movmatrix_trans(w1);
+        for (int j = 0; j < BPI; ++j) {
+            const float r_lo = sv_lo[j] * st.sinv, r_hi = sv_hi[j] * st.sinv;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint32_t w0 = pack_f16x2(pr[j][nt][0] * r_lo, pr[j][nt][1] * r_lo);
+                const uint32_t w1 = pack_f16x2(pr[j][nt][2] * r_hi, pr[j][nt][3] * r_hi);
+                float a, b, c, d;
+                h2_to_f2(w0, a, b);
+                h2_to_f2(w1, c, d);
+                st.wpart[nt][0] += a + c;
+                st.wpart[nt][1] += b + d;
+                pb0[j][nt] = movmatrix_trans(w0);
+                pb1[j][nt] = movmatrix_trans(w1);
+            }
         }
-        auto pv = [&](int mt, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                mma_f16_16816(st.acc[nt][mt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
-        };
 
-        // ---- O^T += Vcode^T . W^T. Thread rows (tokens) 2t, 2t+1, 2t+8, 2t+9;
-        // its d values are CW*gid + 2*mt + r for row tile mt, r = 0 (A rows
-        // gid) or 1 (A rows gid+8): CW contiguous codes of each token row.
-        if constexpr (BITS == 8) {
-            constexpr int WPR = D / 32; // 32-bit words per thread per row
-            uint32_t ra[WPR], rb[WPR], rc[WPR], rd[WPR];
-            if constexpr (D == 128) {
-                const uint4 x0 = lds128(vt + swz<128>(2 * t4, gid));
-                const uint4 x1 = lds128(vt + swz<128>(2 * t4 + 1, gid));
-                const uint4 x2 = lds128(vt + swz<128>(2 * t4 + 8, gid));
-                const uint4 x3 = lds128(vt + swz<128>(2 * t4 + 9, gid));
-                ra[0] = x0.x; ra[1] = x0.y; ra[2] = x0.z; ra[3] = x0.w;
-                rb[0] = x1.x; rb[1] = x1.y; rb[2] = x1.z; rb[3] = x1.w;
-                rc[0] = x2.x; rc[1] = x2.y; rc[2] = x2.z; rc[3] = x2.w;
-                rd[0] = x3.x; rd[1] = x3.y; rd[2] = x3.z; rd[3] = x3.w;
+        // ---- O^T += Vcode^T . W^T, one k-step per block. Thread rows
+        // (tokens) 2t, 2t+1, 2t+8, 2t+9 of the block; its d values are
+        // CW*gid + 2*mt + r for row tile mt, r = 0 (A rows gid) or 1 (A rows
+        // gid+8): CW contiguous codes of each token row.
+#pragma unroll
+        for (int j = 0; j < BPI; ++j) {
+            const uint32_t vt = kt + (BPI + j) * TILE;
+            auto pv = [&](int mt, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_f16_16816(st.acc[nt][mt], a0, a1, a2, a3, pb0[j][nt], pb1[j][nt]);
+            };
+            if constexpr (BITS == 8) {
+                constexpr int WPR = D / 32; // 32-bit words per thread per row
+                uint32_t ra[WPR], rb[WPR], rc[WPR], rd[WPR];
+                if constexpr (D == 128) {
+                    const uint4 x0 = lds128(vt + swz<128>(2 * t4, gid));
+                    const uint4 x1 = lds128(vt + swz<128>(2 * t4 + 1, gid));
+                    const uint4 x2 = lds128(vt + swz<128>(2 * t4 + 8, gid));
+                    const uint4 x3 = lds128(vt + swz<128>(2 * t4 + 9, gid));
+                    ra[0] = x0.x; ra[1] = x0.y; ra[2] = x0.z; ra[3] = x0.w;
+                    rb[0] = x1.x; rb[1] = x1.y; rb[2] = x1.z; rb[3] = x1.w;
+                    rc[0] = x2.x; rc[1] = x2.y; rc[2] = x2.z; rc[3] = x2.w;
+                    rd[0] = x3.x; rd[1] = x3.y; rd[2] = x3.z; rd[3] = x3.w;
+                } else {
+                    const uint32_t off = 8u * (gid & 1);
+                    const uint2 x0 = lds64(vt + swz<64>(2 * t4, gid >> 1) + off);
+                    const uint2 x1 = lds64(vt + swz<64>(2 * t4 + 1, gid >> 1) + off);
+                    const uint2 x2 = lds64(vt + swz<64>(2 * t4 + 8, gid >> 1) + off);
+                    const uint2 x3 = lds64(vt + swz<64>(2 * t4 + 9, gid >> 1) + off);
+                    ra[0] = x0.x; ra[1] = x0.y;
+                    rb[0] = x1.x; rb[1] = x1.y;
+                    rc[0] = x2.x; rc[1] = x2.y;
+                    rd[0] = x3.x; rd[1] = x3.y;
+                }
+#pragma unroll
+                for (int i = 0; i < WPR; ++i) {
+                    // word i holds d values 4i..4i+3: row tiles 2i (bytes 0, 1), 2i+1 (bytes 2, 3)
+                    const uint32_t A = ra[i] ^ 0x80808080u, B = rb[i] ^ 0x80808080u;
+                    const uint32_t C = rc[i] ^ 0x80808080u, E = rd[i] ^ 0x80808080u;
+                    const uint32_t ab_lo = __byte_perm(A, B, 0x5140);
+                    const uint32_t ab_hi = __byte_perm(A, B, 0x7362);
+                    const uint32_t ce_lo = __byte_perm(C, E, 0x5140);
+                    const uint32_t ce_hi = __byte_perm(C, E, 0x7362);
+                    pv(2 * i, bytes_to_h2<0x4140>(ab_lo), bytes_to_h2<0x4342>(ab_lo),
+                       bytes_to_h2<0x4140>(ce_lo), bytes_to_h2<0x4342>(ce_lo));
+                    pv(2 * i + 1, bytes_to_h2<0x4140>(ab_hi), bytes_to_h2<0x4342>(ab_hi),
+                       bytes_to_h2<0x4140>(ce_hi), bytes_to_h2<0x4342>(ce_hi));
+                }
             } else {
-                const uint32_t off = 8u * (gid & 1);
-                const uint2 x0 = lds64(vt + swz<64>(2 * t4, gid >> 1) + off);
-                const uint2 x1 = lds64(vt + swz<64>(2 * t4 + 1, gid >> 1) + off);
-                const uint2 x2 = lds64(vt + swz<64>(2 * t4 + 8, gid >> 1) + off);
-                const uint2 x3 = lds64(vt + swz<64>(2 * t4 + 9, gid >> 1) + off);
-                ra[0] = x0.x; ra[1] = x0.y;
-                rb[0] = x1.x; rb[1] = x1.y;
-                rc[0] = x2.x; rc[1] = x2.y;
-                rd[0] = x3.x; rd[1] = x3.y;
-            }
+                // CW/2 bytes per row; byte k of word i holds d values 8i+2k (low
+                // nibble) and 8i+2k+1 (high nibble): row tile 4i+k
+                constexpr int WPR = CW / 8;
+                uint32_t ra[WPR], rb[WPR], rc[WPR], rd[WPR];
+                if constexpr (D == 128) {
+                    const uint2 x0 = lds64(vt + (2 * t4) * ROWB + 8 * gid);
+                    const uint2 x1 = lds64(vt + (2 * t4 + 1) * ROWB + 8 * gid);
+                    const uint2 x2 = lds64(vt + (2 * t4 + 8) * ROWB + 8 * gid);
+                    const uint2 x3 = lds64(vt + (2 * t4 + 9) * ROWB + 8 * gid);
+                    ra[0] = x0.x; ra[1] = x0.y;
+                    rb[0] = x1.x; rb[1] = x1.y;
+                    rc[0] = x2.x; rc[1] = x2.y;
+                    rd[0] = x3.x; rd[1] = x3.y;
+                } else {
+                    ra[0] = lds32(vt + (2 * t4) * ROWB + 4 * gid);
+                    rb[0] = lds32(vt + (2 * t4 + 1) * ROWB + 4 * gid);
+                    rc[0] = lds32(vt + (2 * t4 + 8) * ROWB + 4 * gid);
+                    rd[0] = lds32(vt + (2 * t4 + 9) * ROWB + 4 * gid);
+                }
 #pragma unroll
-            for (int i = 0; i < WPR; ++i) {
-                // word i holds d values 4i..4i+3: row tiles 2i (bytes 0, 1), 2i+1 (bytes 2, 3)
-                const uint32_t A = ra[i] ^ 0x80808080u, B = rb[i] ^ 0x80808080u;
-                const uint32_t C = rc[i] ^ 0x80808080u, E = rd[i] ^ 0x80808080u;
-                const uint32_t ab_lo = __byte_perm(A, B, 0x5140), ab_hi = __byte_perm(A, B, 0x7362);
-                const uint32_t ce_lo = __byte_perm(C, E, 0x5140), ce_hi = __byte_perm(C, E, 0x7362);
-                pv(2 * i, bytes_to_h2<0x4140>(ab_lo), bytes_to_h2<0x4342>(ab_lo),
-                   bytes_to_h2<0x4140>(ce_lo), bytes_to_h2<0x4342>(ce_lo));
-                pv(2 * i + 1, bytes_to_h2<0x4140>(ab_hi), bytes_to_h2<0x4342>(ab_hi),
-                   bytes_to_h2<0x4140>(ce_hi), bytes_to_h2<0x4342>(ce_hi));
-            }
-        } else {
-            // CW/2 bytes per row; byte k of word i holds d values 8i+2k (low
-            // nibble) and 8i+2k+1 (high nibble): row tile 4i+k
-            constexpr int WPR = CW / 8;
-            uint32_t ra[WPR], rb[WPR], rc[WPR], rd[WPR];
-            if constexpr (D == 128) {
-                const uint2 x0 = lds64(vt + (2 * t4) * ROWB + 8 * gid);
-                const uint2 x1 = lds64(vt + (2 * t4 + 1) * ROWB + 8 * gid);
-                const uint2 x2 = lds64(vt + (2 * t4 + 8) * ROWB + 8 * gid);
-                const uint2 x3 = lds64(vt + (2 * t4 + 9) * ROWB + 8 * gid);
-                ra[0] = x0.x; ra[1] = x0.y;
-                rb[0] = x1.x; rb[1] = x1.y;
-                rc[0] = x2.x; rc[1] = x2.y;
-                rd[0] = x3.x; rd[1] = x3.y;
-            } else {
-                ra[0] = lds32(vt + (2 * t4) * ROWB + 4 * gid);
-                rb[0] = lds32(vt + (2 * t4 + 1) * ROWB + 4 * gid);
-                rc[0] = lds32(vt + (2 * t4 + 8) * ROWB + 4 * gid);
-                rd[0] = lds32(vt + (2 * t4 + 9) * ROWB + 4 * gid);
-            }
+                for (int i = 0; i < WPR; ++i) {
+                    const uint32_t A = ra[i], B = rb[i], C = rc[i], E = rd[i];
 #pragma unroll
-            for (int i = 0; i < WPR; ++i) {
-                const uint32_t A = ra[i] ^ 0x88888888u, B = rb[i] ^ 0x88888888u;
-                const uint32_t C = rc[i] ^ 0x88888888u, E = rd[i] ^ 0x88888888u;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    // bytes {A_k, A_k, B_k, B_k}: nibble pairs (row 2t, row 2t+1) of one d
-                    const uint32_t sel = k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12);
-                    const uint32_t Y = __byte_perm(A, B, sel), Z = __byte_perm(C, E, sel);
-                    pv(4 * i + k, nibs_to_h2<0>(Y), nibs_to_h2<1>(Y), nibs_to_h2<0>(Z),
-                       nibs_to_h2<1>(Z));
+                    for (int k = 0; k < 4; ++k) {
+                        // bytes {A_k, A_k, B_k, B_k}: nibble pairs (row 2t, row 2t+1) of
+                        // d (low nibbles) and d + 1 (high nibbles, x16: A rows gid + 8)
+                        const uint32_t sel = k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12);
+                        const uint32_t Y = __byte_perm(A, B, sel), Z = __byte_perm(C, E, sel);
+                        pv(4 * i + k, nib_lo(Y), nib_hi(Y), nib_lo(Z), nib_hi(Z));
+                    }
                 }
             }
         }
@@ -580,7 +649,8 @@ struct QuantMmaPolicy {
             }
         // acc[nt][mt][e]: row gid (e < 2) or gid+8 (e >= 2) of row tile mt is
         // d = CW*gid + 2*mt + (e >> 1); column 2t4 + (e & 1) is the head. The
-        // codes' bias contributed kBias * (sum of the head's weights) to every d.
+        // codes' bias contributed kBias * (sum of the head's weights) to every d
+        // (INT4: kBiasHi to the odd d, whose codes entered x16).
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -590,13 +660,15 @@ struct QuantMmaPolicy {
                 ws += __shfl_xor_sync(0xffffffffu, ws, 8);
                 ws += __shfl_xor_sync(0xffffffffu, ws, 16);
                 const float bias = kBias * ws;
+                const float bias1 = (BITS == 8 ? kBias : kBiasHi) * ws;
+                const float sb1 = BITS == 8 ? st.sbase : st.sbase * 0.0625f;
                 const int h = nt * 8 + 2 * t4 + c;
                 if (h < GQ) {
                     float *mb = merge + (warp * GQ + h) * (D + 2) + 2 + CW * gid;
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
                         mb[2 * mt] = (st.acc[nt][mt][c] - bias) * st.sbase;
-                        mb[2 * mt + 1] = (st.acc[nt][mt][c + 2] - bias) * st.sbase;
+                        mb[2 * mt + 1] = (st.acc[nt][mt][c + 2] - bias1) * sb1;
                     }
                 }
             }
