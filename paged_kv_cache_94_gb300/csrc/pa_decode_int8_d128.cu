@@ -21,6 +21,12 @@
 #ifndef PA_INT8_D128_SHARE_BPI
 #define PA_INT8_D128_SHARE_BPI 1
 #endif
+#ifndef PA_INT8_D128_SHARE_NW
+#define PA_INT8_D128_SHARE_NW PA_INT8_D128_NW
+#endif
+#ifndef PA_INT8_D128_SHARE_MINB
+#define PA_INT8_D128_SHARE_MINB PA_INT8_D128_MINB
+#endif
 #ifndef PA_INT8_D128_SHARE_STAGES
 #define PA_INT8_D128_SHARE_STAGES 3
 #endif
@@ -55,8 +61,8 @@ const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G
 // up to kShareMembers(G) sequences, G heads each, share every K/V tile) and
 // then every sequence's remaining blocks.
 template <int G>
-using PolShare = QuantMmaPolicy<8, 128, G, PA_INT8_D128_NW, PA_INT8_D128_SHARE_STAGES,
-                                (G >= 16 ? 1 : PA_INT8_D128_MINB), PA_INT8_D128_SHARE_BPI>;
+using PolShare = QuantMmaPolicy<8, 128, G, PA_INT8_D128_SHARE_NW, PA_INT8_D128_SHARE_STAGES,
+                                (G >= 16 ? 1 : PA_INT8_D128_SHARE_MINB), PA_INT8_D128_SHARE_BPI>;
 
 template <int G>
 const DecodeKernel kPrefix = {

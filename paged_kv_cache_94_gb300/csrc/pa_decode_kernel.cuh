@@ -139,7 +139,7 @@ struct Bf16Policy {
     // Rows [lo, valid) of the block are attended; the others are masked. rem =
     // ctx - the block's first position (the multi-query causal limit).
     __device__ static void compute(State &st, uint32_t kt, uint32_t /*extra*/, int lo, int valid,
-                                   int rem, float scale_log2)
+                                   int rem, float scale_log2, uint32_t /*mask: 1*/)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
         const int mi = lane >> 3, rr = lane & 7;
@@ -507,19 +507,14 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
             const int32_t mask = ok ? wmeta[cstage] : 0;
             if (mask != 0) {
                 const int32_t t0 = (fb + BPI * (int32_t)(x - unit_start)) * kBlockTokens;
-                int lo = pool_from > t0 ? (int)min(pool_from - t0, TOK) : 0;
+                const int lo = pool_from > t0 ? (int)min(pool_from - t0, TOK) : 0;
                 const int rem = (int)min(ctx - t0, TOK + kBlockTokens); // >= TOK + NQ - 1
-                int valid = (int)min(rem, TOK);
-                if constexpr (BPI == 2) { // a bad block's tokens are not attended
-                    if (!(mask & 1))
-                        lo = max(lo, kBlockTokens);
-                    if (!(mask & 2))
-                        valid = min(valid, kBlockTokens);
-                }
+                const int valid = (int)min(rem, TOK);
+                // (mask: the item's blocks that were loaded; a bad one is not attended)
                 if (lo < valid)
                     Pol::compute(st, ring_base + (uint32_t)(cstage * Pol::STAGE),
                                  extra_base + (uint32_t)(cstage * Pol::EXTRA), lo, valid, rem,
-                                 p.scale_log2);
+                                 p.scale_log2, (uint32_t)mask);
             }
             __syncwarp();
             if (!dead && r.issued < r.n_items)

@@ -122,7 +122,7 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 template <int BITS, int D_, int GQ_, int NW_, int S_, int MINB_ = 1, int BPI_ = 2>
 struct QuantMmaPolicy {
     static_assert(BITS == 8 || BITS == 4, "INT8 or INT4 codes");
-    static_assert(BPI_ == 1 || BPI_ == 2, "one or two blocks per ring item");
+    static_assert(BPI_ == 1 || BPI_ == 2 || BPI_ == 4, "1, 2 or 4 blocks per ring item");
     static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_, NQ = 1;
     static constexpr int BPI = BPI_;               // blocks per ring item
     static constexpr int kMinBlocks = MINB_;       // resident CTAs per SM the registers allow
@@ -192,7 +192,10 @@ struct QuantMmaPolicy {
         }
         if (lane < 8 * BPI) {
             const int t = lane >> 2, kind = t / BPI, j = t - kind * BPI; // t = kind*BPI + j
-            const int32_t rj = j == 0 ? rows[0] : rows[BPI - 1];           // no local array
+            int32_t rj = rows[0]; // selects, not an indexed (local-memory) array
+#pragma unroll
+            for (int i = 1; i < BPI; ++i)
+                rj = j == i ? rows[i] : rj;
             if (rj >= 0) {
                 const float *sc = (kind ? p.v_scale : p.k_scale) + (size_t)rj * kBlockTokens;
                 cp_async_16(extra + 64 * t + 16 * (lane & 3), sc + 4 * (lane & 3), pol);
@@ -352,9 +355,10 @@ struct QuantMmaPolicy {
 
     // One item of BPI 16-token blocks: block j's K codes at kt + j*TILE, its V
     // codes at kt + (BPI+j)*TILE, its scales at extra + 64*j (K) and
-    // extra + 64*(BPI+j) (V). Tokens [lo, valid) of the item are attended.
+    // extra + 64*(BPI+j) (V). Tokens [lo, valid) of the item are attended,
+    // those of block j only if bit j of mask is set (the block was loaded).
     __device__ static void compute(State &st, uint32_t kt, uint32_t extra, int lo, int valid,
-                                   int /*rem*/, float scale_log2)
+                                   int /*rem*/, float scale_log2, uint32_t mask)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
 
@@ -429,8 +433,9 @@ struct QuantMmaPolicy {
 #pragma unroll
         for (int j = 0; j < BPI; ++j) {
             const int tl = 16 * j + gid, th = tl + 8;
-            lo_ok[j] = tl >= lo && tl < valid;
-            hi_ok[j] = th >= lo && th < valid;
+            const bool in = (mask >> j) & 1u;
+            lo_ok[j] = in && tl >= lo && tl < valid;
+            hi_ok[j] = in && th >= lo && th < valid;
             const float f_lo = st.qexp * lds_f32(extra + 64 * j + 4 * gid) * scale_log2;
             const float f_hi = st.qexp * lds_f32(extra + 64 * j + 4 * (gid + 8)) * scale_log2;
 #pragma unroll
