@@ -282,9 +282,9 @@ pa_status pa_decode_opt(const void *q, const void *k_cache, const void *v_cache,
  * whose range is empty (ctx_b < n_q - i) gets a zero output.
  *
  *   q    bf16 [num_seqs][n_q][n_h][d_h]; out the same shape
- *   n_q  1 (pa_decode), or 2, 4, 8 with g * n_q <= 16; bf16 pools only
- *        (PA_ERR_UNSUPPORTED otherwise)
- * Every other argument is pa_decode's. All n_q * g query rows of a kv head
+ *   n_q  1 (pa_decode), or 2, 4, 8 with g * n_q <= 16, on bf16, INT8 and
+ *        INT4 pools (PA_ERR_UNSUPPORTED otherwise)
+ * Every other argument is pa_decode's (k_scale/v_scale for INT8/INT4 pools). All n_q * g query rows of a kv head
  * read each K/V tile once: the bytes moved are those of one decode step.
  * The workspace is pa_decode_mq_workspace_size(geom, num_seqs, n_q, 0).
  */

@@ -359,12 +359,15 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
 def pa_decode_mq(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                  block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
                  out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                 dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                 dev_status: Optional[torch.Tensor] = None, stream=None,
+                 k_scale: Optional[torch.Tensor] = None,
+                 v_scale: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Multi-query decode: q [B, n_q, n_h, d_h] bf16 (the last n_q tokens of each
-    sequence, attending causally) over a bf16 pool -> out of q's shape."""
+    sequence, attending causally) over a bf16, INT8 or INT4 pool (scales as
+    pa_decode's) -> out of q's shape."""
     _need_cuda("q", q, torch.bfloat16)
-    _need_cuda("k_cache", k_cache, torch.bfloat16)
-    _need_cuda("v_cache", v_cache, torch.bfloat16)
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
     _need_cuda("block_tables", block_tables, torch.int32)
     _need_cuda("context_lens", context_lens, torch.int32)
     if q.dim() != 4:
@@ -374,6 +377,11 @@ def pa_decode_mq(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     if d != g.d_h or block_tables.dim() != 2 or block_tables.shape[0] != B or \
             context_lens.shape != (B,):
         raise ValueError("q, block_tables, context_lens disagree on num_seqs or d_h")
+    if g.kv_dtype != PA_KV_BF16:
+        for nm, s in (("k_scale", k_scale), ("v_scale", v_scale)):
+            if s is None:
+                raise ValueError(f"{nm} is required for an int8/int4 pool")
+            _need_cuda(nm, s, torch.float32)
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -386,7 +394,7 @@ def pa_decode_mq(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         _need_cuda("workspace", workspace)
     if dev_status is not None:
         _need_cuda("dev_status", dev_status, torch.int32)
-    st = _lib().pa_decode_mq(_ptr(q), _ptr(k_cache), _ptr(v_cache), None, None,
+    st = _lib().pa_decode_mq(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
                              _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B,
                              n_q, float(scale), _ptr(out), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), g, _ptr(dev_status),

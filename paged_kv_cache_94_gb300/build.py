@@ -32,6 +32,10 @@ SOURCES = [
     "pa_decode_int4_d128.cu",
     "pa_decode_int4_d64.cu",
     "pa_decode_bf16_mq.cu",
+    "pa_decode_int8_mq_d128.cu",
+    "pa_decode_int8_mq_d64.cu",
+    "pa_decode_int4_mq_d128.cu",
+    "pa_decode_int4_mq_d64.cu",
     "pa_share.cu",
     "pa_decode_noalloc.cu",
     "pa_block_copy.cu",

@@ -45,7 +45,9 @@ const DecodeKernel *kernel_for(const pa_geom &g, int nq = 1)
 {
     const int gq = group_of(g);
     if (nq != 1)
-        return g.kv_dtype == PA_KV_BF16 ? pa::find_decode_kernel_bf16_mq(g.d_h, gq, nq) : nullptr;
+        return g.kv_dtype == PA_KV_INT8   ? pa::find_decode_kernel_int8_mq(g.d_h, gq, nq)
+               : g.kv_dtype == PA_KV_INT4 ? pa::find_decode_kernel_int4_mq(g.d_h, gq, nq)
+                                          : pa::find_decode_kernel_bf16_mq(g.d_h, gq, nq);
     return g.kv_dtype == PA_KV_INT8   ? pa::find_decode_kernel_int8(g.d_h, gq)
            : g.kv_dtype == PA_KV_INT4 ? pa::find_decode_kernel_int4(g.d_h, gq)
                                       : pa::find_decode_kernel_bf16(g.d_h, gq);
@@ -432,6 +434,23 @@ const DecodeKernel *find_decode_kernel_int4(int d_h, int group)
 {
     return d_h == 128 ? find_decode_kernel_int4_d128(group)
                       : d_h == 64 ? find_decode_kernel_int4_d64(group) : nullptr;
+}
+
+const DecodeKernel *find_decode_kernel_int8_mq_d128(int group, int nq);
+const DecodeKernel *find_decode_kernel_int8_mq_d64(int group, int nq);
+const DecodeKernel *find_decode_kernel_int4_mq_d128(int group, int nq);
+const DecodeKernel *find_decode_kernel_int4_mq_d64(int group, int nq);
+
+const DecodeKernel *find_decode_kernel_int8_mq(int d_h, int group, int nq)
+{
+    return d_h == 128 ? find_decode_kernel_int8_mq_d128(group, nq)
+                      : d_h == 64 ? find_decode_kernel_int8_mq_d64(group, nq) : nullptr;
+}
+
+const DecodeKernel *find_decode_kernel_int4_mq(int d_h, int group, int nq)
+{
+    return d_h == 128 ? find_decode_kernel_int4_mq_d128(group, nq)
+                      : d_h == 64 ? find_decode_kernel_int4_mq_d64(group, nq) : nullptr;
 }
 
 const DecodeKernel *find_decode_kernel_int8(int d_h, int group)

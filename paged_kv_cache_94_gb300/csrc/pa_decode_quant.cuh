@@ -119,11 +119,14 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 }
 
 // ---------------------------------------------------------------------------
-template <int BITS, int D_, int GQ_, int NW_, int S_, int MINB_ = 1, int BPI_ = 2>
+// GQ query rows share each K/V tile: the g query heads of a kv head for each
+// of NQ new tokens (NQ > 1: multi-query decode, each token masked causally).
+template <int BITS, int D_, int GQ_, int NW_, int S_, int MINB_ = 1, int BPI_ = 2, int NQ_ = 1>
 struct QuantMmaPolicy {
     static_assert(BITS == 8 || BITS == 4, "INT8 or INT4 codes");
     static_assert(BPI_ == 1 || BPI_ == 2 || BPI_ == 4, "1, 2 or 4 blocks per ring item");
-    static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_, NQ = 1;
+    static_assert(GQ_ % NQ_ == 0, "GQ = g * NQ");
+    static constexpr int D = D_, GQ = GQ_, NW = NW_, S = S_, NQ = NQ_;
     static constexpr int BPI = BPI_;               // blocks per ring item
     static constexpr int kMinBlocks = MINB_;       // resident CTAs per SM the registers allow
     static constexpr int NT = (GQ + 7) / 8;        // 8-head tiles of S^T
@@ -356,9 +359,10 @@ struct QuantMmaPolicy {
     // One item of BPI 16-token blocks: block j's K codes at kt + j*TILE, its V
     // codes at kt + (BPI+j)*TILE, its scales at extra + 64*j (K) and
     // extra + 64*(BPI+j) (V). Tokens [lo, valid) of the item are attended,
-    // those of block j only if bit j of mask is set (the block was loaded).
+    // those of block j only if bit j of mask is set (the block was loaded);
+    // rem = ctx - (the item's first position), for the causal mask (NQ > 1).
     __device__ static void compute(State &st, uint32_t kt, uint32_t extra, int lo, int valid,
-                                   int /*rem*/, float scale_log2, uint32_t mask)
+                                   int rem, float scale_log2, uint32_t mask)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
 
@@ -452,6 +456,8 @@ struct QuantMmaPolicy {
                     const float sc = sb * ((c & 2) ? f_hi : f_lo);
                     pr[j][nt][c] = ((c & 2) ? hi_ok[j] : lo_ok[j]) ? sc : -INFINITY;
                 }
+                if constexpr (NQ > 1) // block j starts 16j tokens into the item
+                    causal_mask<GQ, NQ>(pr[j][nt], nt, gid, t4, rem - 16 * j);
 #pragma unroll
                 for (int e = 0; e < 2; ++e)
                     need |= fmaxf(pr[j][nt][e], pr[j][nt][e + 2]) > st.m[nt][e] + kRescaleLog2;

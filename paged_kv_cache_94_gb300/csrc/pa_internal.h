@@ -40,6 +40,8 @@ cudaError_t launch_share_detect(const int32_t *block_tables, int max_blocks,
 
 // Multi-query (nq new tokens per sequence) bf16 kernels; NULL when not compiled.
 const DecodeKernel *find_decode_kernel_bf16_mq(int d_h, int group, int nq);
+const DecodeKernel *find_decode_kernel_int8_mq(int d_h, int group, int nq);
+const DecodeKernel *find_decode_kernel_int4_mq(int d_h, int group, int nq);
 
 cudaError_t launch_cache_write(const void *k, const void *v, const int64_t *slots, int64_t T,
                                int n_kv, int d_h, int kind, int64_t num_slots, void *k_cache,

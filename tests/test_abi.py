@@ -174,3 +174,14 @@ def test_decode_opt_argument_checks(lib):
     assert call(g, share_prefix=2) == -2
     assert call(g, share_prefix=1, window=64) == -4                 # not with a window
     assert call(_geom(n_h=128, n_kv=8), share_prefix=1) == -4      # g = 16
+
+
+@pytest.mark.parametrize("kv_dtype", [0, 1, 2])
+def test_mq_workspace_size_per_pool_type(lib, kv_dtype):
+    # multi-query kernels exist for every pool type at g * n_q <= 16 (explicit
+    # CTA count: no device query); other shapes report 0
+    for n_h, n_q, ok in [(16, 2, True), (16, 8, True), (32, 4, True), (64, 2, True),
+                         (32, 8, False), (16, 3, False), (128, 2, False)]:
+        g = _geom(n_h=n_h, n_kv=8, kv_dtype=kv_dtype)
+        size = lib.pa_decode_mq_workspace_size(g, 4, n_q, 304)
+        assert (size > 0) == ok, (n_h, n_q, kv_dtype)
