@@ -246,7 +246,10 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
 // covering many short units gets fewer blocks. Every sequence with blocks
 // carries n_kv * kSegCost, so the virtual prefix is P[b] + kSegCost * Z[b].
 // ---------------------------------------------------------------------------
-constexpr int kSegCost = 8;
+#ifndef PA_SEG_COST
+#define PA_SEG_COST 8
+#endif
+constexpr int kSegCost = PA_SEG_COST;
 
 // Virtual position of the first block of unit (b, kvh) (nb = blocks of b).
 // Z = P + num_seqs + 1 counts the sequences with blocks: an empty sequence
