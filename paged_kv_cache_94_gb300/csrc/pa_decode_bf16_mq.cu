@@ -13,6 +13,9 @@
 #ifndef PA_BF16_MQ_D128_STAGES
 #define PA_BF16_MQ_D128_STAGES 2
 #endif
+#ifndef PA_BF16_MQ_D128_STAGES_R16
+#define PA_BF16_MQ_D128_STAGES_R16 2
+#endif
 #ifndef PA_BF16_MQ_D64_NW
 #define PA_BF16_MQ_D64_NW 4
 #endif
@@ -41,7 +44,9 @@ template <int D, int G, int NQ>
 using Pol = Bf16Policy<D, G * NQ,
                        D == 128 ? (G * NQ >= 16 ? PA_BF16_MQ_D128_NW_R16 : PA_BF16_MQ_D128_NW)
                                 : PA_BF16_MQ_D64_NW,
-                       D == 128 ? PA_BF16_MQ_D128_STAGES : PA_BF16_MQ_D64_STAGES, NQ>;
+                       D == 128 ? (G * NQ >= 16 ? PA_BF16_MQ_D128_STAGES_R16 : PA_BF16_MQ_D128_STAGES)
+                                : PA_BF16_MQ_D64_STAGES,
+                       NQ>;
 
 template <int D, int G, int NQ>
 const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<D, G, NQ>>),
