@@ -47,6 +47,16 @@ L2_NOTE = ("flushed between timed steps: a 512 MiB write, then a 384 MiB read so
            "write-back would land inside the next timed kernel)")
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest x over all ranks (x itself when world == 1): the timed
+    region of a multi-replica run ends when its slowest rank ends."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 class StagedInputs:
     """Tensors packed into one pinned host buffer (each 256-byte aligned) and a
     device buffer of the same layout: one host-to-device copy moves them all."""
@@ -367,11 +377,7 @@ def run_native(args, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"device status {st}: {pa.pa_status_from_device(st)}")
 
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
 
     db = decode_bytes(w)
@@ -435,11 +441,7 @@ def run_native(args, rank, world, local_rank):
             e2e_step()
             e2e_ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_ev), world, dev)
         e2e_ms /= args.steps
         result["e2e"] = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2),
                          "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
@@ -504,11 +506,7 @@ def run_block_copy(args, rank, world, local_rank):
     clocks = sampler.stop()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
-    total_ms = sum(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), world, dev)
     ms = total_ms / args.steps
     nbytes = block_copy_bytes(g, args.pairs)
     achieved = nbytes / (ms * 1e-3) / 1e9
