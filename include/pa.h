@@ -242,7 +242,10 @@ pa_status pa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
  *             blocks once with all the group's query rows and, in the same
  *             launch, each sequence's remaining blocks, and the last piece of
  *             a sequence to finish merges the softmax states (log-sum-exp).
- *             The result equals pa_decode's up to rounding. Sharers must be adjacent in the batch. Not with a
+ *             The result equals pa_decode's up to rounding. A batch whose
+ *             2 * num_seqs units' tables do not fit the kernel's shared
+ *             memory (thousands of sequences at d_h 128) is decoded without
+ *             sharing, with the same result. Sharers must be adjacent in the batch. Not with a
  *             window or sink rows; g <= 8. The workspace is
  *             pa_decode_opt_workspace_size(geom, num_seqs, opts).
  */

@@ -165,6 +165,22 @@ struct ShareLayout {
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Shared memory and resident CTAs per SM of the shared-prefix kernel for a
+// batch (its 2 * num_seqs units' prefix arrays grow with the batch);
+// PA_ERR_UNSUPPORTED when not even one CTA fits on an SM.
+pa_status share_fits(const DecodeKernel *kp, int num_seqs, size_t &smem, int &per)
+{
+    smem = kp->smem_bytes(2 * num_seqs);
+    int dev = -1, max_optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+        return PA_ERR_CUDA;
+    if (smem > (size_t)max_optin)
+        return PA_ERR_UNSUPPORTED;
+    return ctas_per_sm(kp, smem, per);
+}
+
 ShareLayout share_layout(const pa_geom &g, int num_seqs, int grid)
 {
     ShareLayout L;
@@ -280,7 +296,7 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     if (o.window < 0 || o.n_sink < 0 || o.n_sink > 16 || o.reserved != 0 ||
         (o.share_prefix != 0 && o.share_prefix != 1))
         return PA_ERR_SHAPE;
-    const bool share = o.share_prefix == 1;
+    bool share = o.share_prefix == 1;
     if (share && (nq != 1 || o.window != 0 || o.n_sink != 0 || group_of(g) > 8))
         return PA_ERR_UNSUPPORTED;
     if (o.n_sink > 0) {
@@ -322,14 +338,14 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     if (share && !kp)
         return PA_ERR_UNSUPPORTED;
     size_t smem_sh = 0;
-    if (share) {
-        // one wave of resident CTAs
-        smem_sh = kp->smem_bytes(2 * num_seqs);
-        int per_sh;
-        if ((st = ctas_per_sm(kp, smem_sh, per_sh)) != PA_OK)
+    int per_sh = 0;
+    if (share && (st = share_fits(kp, num_seqs, smem_sh, per_sh)) != PA_OK) {
+        if (st != PA_ERR_UNSUPPORTED)
             return st;
-        grid = sms * per_sh;
+        share = false; // the batch's prefix arrays do not fit: decode without sharing
     }
+    if (share) // default: one wave of resident CTAs
+        grid = num_ctas > 0 ? num_ctas : sms * per_sh;
     const ShareLayout SL = share ? share_layout(g, num_seqs, grid) : ShareLayout{};
     if (workspace_bytes < (share ? SL.end : workspace_bytes_for(g, num_seqs, grid, nq)))
         return PA_ERR_WORKSPACE;
@@ -578,10 +594,15 @@ size_t pa_decode_opt_workspace_size(pa_geom geom, int32_t num_seqs, const pa_dec
         return workspace_bytes_for(geom, num_seqs, grid);
     const DecodeKernel *kp = pa::find_prefix_kernel(geom.kv_dtype, geom.d_h, group_of(geom));
     int dev, sms, per;
-    if (!kp || current_device(dev, sms) != PA_OK ||
-        ctas_per_sm(kp, kp->smem_bytes(2 * num_seqs), per) != PA_OK)
+    size_t smem;
+    if (!kp || current_device(dev, sms) != PA_OK)
         return 0;
-    return share_layout(geom, num_seqs, sms * per).end;
+    const pa_status st = share_fits(kp, num_seqs, smem, per);
+    if (st == PA_ERR_UNSUPPORTED) // decoded without sharing
+        return workspace_bytes_for(geom, num_seqs, grid);
+    if (st != PA_OK)
+        return 0;
+    return share_layout(geom, num_seqs, num_ctas > 0 ? num_ctas : sms * per).end;
 }
 
 pa_status pa_decode_opt(const void *q, const void *k_cache, const void *v_cache,

@@ -141,8 +141,8 @@ struct SmemLayout {
     static constexpr int kOffSinkSc = kOffMerge + kMerge;
     static constexpr int kOffMisc = kOffSinkSc + kSinkSc;
     static constexpr int kOffPrefix = kOffMisc + kMisc;
-    // P[num_seqs + 1] (blocks) then Z[num_seqs + 1] (sequences with blocks)
-    static size_t bytes(int num_seqs) { return 1024 + kOffPrefix + 8 * (size_t)(num_seqs + 1); }
+    // P[num_seqs + 1] (int32 items) then Z[num_seqs + 1] (uint16: units with items)
+    static size_t bytes(int num_seqs) { return 1024 + kOffPrefix + 6 * (size_t)(num_seqs + 1); }
 };
 
 // ---------------------------------------------------------------------------
@@ -157,7 +157,7 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NWARP = NT / 32;
     int32_t carry = 0, zcarry = 0;
-    int32_t *Z = P + p.num_seqs + 1; // Z[b]: sequences before b that have blocks
+    uint16_t *Z = reinterpret_cast<uint16_t *>(P + p.num_seqs + 1); // sequences before b with blocks
     if (tid == 0) {
         P[0] = 0;
         Z[0] = 0;
@@ -228,7 +228,7 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
         const int32_t zbefore = warp ? wsum[8 + warp - 1] : 0;
         if (b < p.num_seqs) {
             P[b + 1] = carry + before + x;
-            Z[b + 1] = zcarry + zbefore + z;
+            Z[b + 1] = (uint16_t)(zcarry + zbefore + z);
         }
         carry += wsum[NWARP - 1];
         zcarry += wsum[8 + NWARP - 1];
@@ -256,7 +256,7 @@ constexpr int kSegCost = PA_SEG_COST;
 // has no segment and costs nothing.
 __device__ __forceinline__ int64_t virt_start(const DecodeParams &p, const int32_t *P, int b)
 {
-    const int32_t *Z = P + p.num_seqs + 1;
+    const uint16_t *Z = reinterpret_cast<const uint16_t *>(P + p.num_seqs + 1);
     return (int64_t)p.n_kv * (P[b] + (int64_t)p.seg_cost * Z[b]);
 }
 

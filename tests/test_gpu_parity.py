@@ -189,3 +189,17 @@ def test_full_size_config_sampled(dev, name):
         if ks is not None:
             np.testing.assert_array_equal(ks.index_select(0, phys).cpu().numpy(), opool.k_scale)
             np.testing.assert_array_equal(vs.index_select(0, phys).cpu().numpy(), opool.v_scale)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "int8", "int4"])
+def test_maximum_batch(dev, dt):
+    # 8192 sequences (the largest batch the ABI takes), tiny and ragged
+    # contexts, a few empty: the per-sequence prefix arrays are at their largest
+    rng = np.random.default_rng(5)
+    ctx = rng.integers(1, 40, 8192)
+    ctx[[0, 1000, 8191]] = 0
+    w = make_workload("maxb", Geometry(8, 2, 64, kv_dtype=dt), ctx.tolist(), seed=13)
+    ref, _ = oracle_full(w)
+    out, st = gpu_decode(w, gpu_pool(w, dev), dev)
+    assert st == 0
+    assert_close(out.float().cpu().numpy(), ref, f"{dt} B=8192")

@@ -77,3 +77,39 @@ def test_shared_prefix_full_size_int8_workload():
     for b in (0, 7, 13, w.B - 1):
         ref, _ = oracle_one_sequence(w, b, gen_device=DEV)
         assert_close(out[b], ref, f"int8 prefix seq {b}")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "int8"])
+def test_shared_prefix_maximum_batch(kv_dtype):
+    # 8192 sequences in runs of 8 sharing 8 full blocks (the shortest prefix
+    # that forms a group), ragged suffixes: the detection's largest input and
+    # the fused launch's 2 x 8192 units
+    rng = np.random.default_rng(6)
+    B = 8192
+    groups = np.repeat(np.arange(B // 8), 8)
+    prefix = np.full(B, 128)
+    suffix = rng.integers(1, 50, B)
+    w = make_workload("share_maxb", Geometry(n_h=4, n_kv=2, d_h=64, kv_dtype=kv_dtype),
+                      (prefix + suffix).tolist(), 17, prefix_len=prefix.tolist(),
+                      group=groups.tolist())
+    pool = gpu_pool(w, DEV)
+    ref, _ = oracle_full(w)
+    out, st = run(w, pool, share=True)
+    assert st == 0
+    assert_close(out, ref, f"{kv_dtype} B=8192 shared")
+
+
+def test_shared_prefix_too_large_for_the_kernel_decodes_without_sharing():
+    # at d_h 128, g = 1, the 2 x 8192 units' prefix arrays do not fit beside
+    # the ring: the call decodes without sharing and returns the plain result
+    B = 8192
+    groups = np.repeat(np.arange(B // 8), 8)
+    w = make_workload("share_fallback", Geometry(n_h=2, n_kv=2, d_h=128), [130] * B, 18,
+                      prefix_len=[128] * B, group=groups.tolist())
+    pool = gpu_pool(w, DEV)
+    a, st0 = run(w, pool, share=False)
+    b, st1 = run(w, pool, share=True)
+    assert st0 == 0 and st1 == 0 and np.array_equal(a, b)
+    for s in (0, 4097, B - 1):
+        ref, _ = oracle_one_sequence(w, s)
+        assert_close(b[s], ref, f"seq {s}")
