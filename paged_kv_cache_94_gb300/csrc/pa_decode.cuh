@@ -8,12 +8,13 @@
 // KV head (same page, GQA row of the "注意力头架构演进" table).
 //
 // How the work is split.
-//   An "item" is one (sequence, kv head, 16-token block). Items are laid out
+//   An "item" is BPI consecutive 16-token blocks of one (sequence, kv head)
+//   unit (one block for bf16 tiles, two for INT8/INT4). Items are laid out
 //   sequence-major, then kv head, then block, so the W items of the whole
-//   batch form one line. The split is by cost: each (sequence, kv head) also
-//   counts kSegCost items for the merge that ends each of its segments (see
-//   virt_first), and CTA c of G takes the items in [c/G, (c+1)/G) of that
-//   weighted line. Every CTA gets about the same work whatever the mix of
+//   batch form one line. The split is by cost: each (sequence, kv head) unit
+//   with blocks also counts kSegCost items for the merge that ends each of
+//   its segments (see virt_first), and CTA c of G takes the items in
+//   [c/G, (c+1)/G) of that weighted line. Every CTA gets about the same work whatever the mix of
 //   context lengths, and long contexts are split across CTAs
 //   ("split-context" decode). A CTA's range is cut at (sequence, kv head)
 //   boundaries into segments.
@@ -21,9 +22,11 @@
 //   is read from HBM once for all g heads.
 // Inside a CTA.
 //   Each warp owns every NW-th item of the range and a private ring of S
-//   shared-memory stages. Lane 0 issues TMA tile loads (cp.async.bulk.tensor,
-//   128-byte swizzle) S items ahead; completion is tracked by one mbarrier per
-//   stage. Block-table entries are fetched 32 items ahead, one per lane.
+//   shared-memory stages. bf16: lane 0 issues TMA tile loads
+//   (cp.async.bulk.tensor, 128-byte swizzle) S items ahead; INT8/INT4: every
+//   lane issues 16-byte cp.async copies of its share. Completion is tracked
+//   by one mbarrier per stage. Block-table entries are fetched 32 items
+//   ahead, one item per lane.
 //   A warp keeps an online-softmax state (running max m, sum l, accumulator)
 //   per query head, in the log2 domain.
 // Merging.
@@ -33,7 +36,9 @@
 //   that (sequence, kv head) -- found with one atomic counter, no waiting --
 //   merges all slots with the log-sum-exp rule
 //       M = max_p m_p,  out = sum_p 2^(m_p-M) acc_p / sum_p 2^(m_p-M) l_p
-//   and resets the counter to zero for the next call.
+//   and resets the counter to zero for the next call. With shared prefixes
+//   (PASS 2) a sequence's counter also counts its group's arrival, and the
+//   group's prefix state joins the same merge (see finish_fused).
 #pragma once
 
 #include "pa_internal.h"
