@@ -379,6 +379,8 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     p.sink_v = static_cast<const __nv_bfloat16 *>(o.n_sink > 0 ? o.sink_v : nullptr);
     p.g = group_of(g);
     p.seg_cost = pa::kSegCost;
+    p.seg_cost_lead = pa::kSegCost;
+    p.lead_units = 0;
     p.skip = nullptr;
     p.pre = nullptr;
     p.groups = nullptr;
@@ -398,6 +400,9 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
         if (e != cudaSuccess)
             return PA_ERR_CUDA;
         p.num_seqs = 2 * num_seqs;
+        p.seg_cost = pa::kShareSegCost; // every unit ends in records and a merge
+        p.seg_cost_lead = pa::kShareGroupSegCost;
+        p.lead_units = num_seqs;
         p.counters = reinterpret_cast<int32_t *>(ws);
         p.partials = reinterpret_cast<float *>(ws + SL.records);
         p.skip = skip;

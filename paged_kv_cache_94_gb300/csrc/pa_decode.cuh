@@ -73,6 +73,8 @@ struct DecodeParams {
     const __nv_bfloat16 *sink_v;
     int32_t g;                   // query heads per kv head
     int32_t seg_cost;            // virtual items charged per (sequence, kv head) unit
+    int32_t seg_cost_lead;       // ... per unit of the first lead_units "sequences"
+    int32_t lead_units;          //     (the group units of the shared-prefix launch)
     // Shared prefixes (PASS 2, see pa_share.cu): the line holds num_real
     // group units first, group s = groups[3s..3s+2] = (first member, members,
     // shared blocks), whose query rows are the g heads of each member; then
@@ -258,17 +260,26 @@ constexpr int kSegCost = PA_SEG_COST;
 
 // Virtual position of the first block of unit (b, kvh) (nb = blocks of b).
 // Z = P + num_seqs + 1 counts the sequences with blocks: an empty sequence
-// has no segment and costs nothing.
+// has no segment and costs nothing. A unit of one of the first lead_units
+// sequences is charged seg_cost_lead, any other seg_cost.
+__device__ __forceinline__ int64_t unit_cost(const DecodeParams &p, int b)
+{
+    return b < p.lead_units ? p.seg_cost_lead : p.seg_cost;
+}
+
 __device__ __forceinline__ int64_t virt_start(const DecodeParams &p, const int32_t *P, int b)
 {
     const uint16_t *Z = reinterpret_cast<const uint16_t *>(P + p.num_seqs + 1);
-    return (int64_t)p.n_kv * (P[b] + (int64_t)p.seg_cost * Z[b]);
+    const int64_t zl = Z[b < p.lead_units ? b : p.lead_units];
+    return (int64_t)p.n_kv * (P[b] + (int64_t)p.seg_cost * Z[b] +
+                              ((int64_t)p.seg_cost_lead - p.seg_cost) * zl);
 }
 
 __device__ __forceinline__ int64_t virt_first(const DecodeParams &p, const int32_t *P, int b,
                                               int kvh, int nb)
 {
-    return virt_start(p, P, b) + (int64_t)kvh * (nb + p.seg_cost) + p.seg_cost;
+    const int64_t c = unit_cost(p, b);
+    return virt_start(p, P, b) + (int64_t)kvh * (nb + c) + c;
 }
 
 // Total virtual length.
@@ -284,7 +295,6 @@ __device__ __forceinline__ int64_t real_at_virtual(const DecodeParams &p, const 
     if (y >= virt_total(p, P))
         return (int64_t)p.n_kv * P[p.num_seqs];
     int lo = 0, hi = p.num_seqs;
-    const int64_t C = p.seg_cost;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (virt_start(p, P, mid) <= y)
@@ -295,6 +305,7 @@ __device__ __forceinline__ int64_t real_at_virtual(const DecodeParams &p, const 
     // b has blocks: an empty b has a zero virtual length, so it would not be
     // the largest b with a start <= y
     const int b = lo;
+    const int64_t C = unit_cost(p, b);
     const int64_t nb = P[b + 1] - P[b], v = nb + C;
     const int64_t r = y - virt_start(p, P, b);
     const int64_t kvh = r / v, off = r - kvh * v;

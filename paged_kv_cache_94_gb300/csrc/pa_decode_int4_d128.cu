@@ -9,6 +9,12 @@
 #ifndef PA_INT4_D128_MINB
 #define PA_INT4_D128_MINB 3
 #endif
+#ifndef PA_INT4_D128_TMA
+#define PA_INT4_D128_TMA 0 // 1: TMA boxes instead of per-lane 16-byte copies
+#endif
+#ifndef PA_INT4_D128_SHARE_TMA
+#define PA_INT4_D128_SHARE_TMA PA_INT4_D128_TMA
+#endif
 #ifndef PA_INT4_D128_BPI
 #define PA_INT4_D128_BPI 2 // blocks per ring item
 #endif
@@ -51,7 +57,7 @@ cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const Decode
 template <int G>
 using Pol = QuantMmaPolicy<4, 128, G, PA_INT4_D128_NW, PA_INT4_D128_STAGES,
                            (G >= 16 ? 1 : PA_INT4_D128_MINB), // g = 16 needs its registers
-                           PA_INT4_D128_BPI>;
+                           PA_INT4_D128_BPI, 1, PA_INT4_D128_TMA != 0>;
 
 template <int G>
 const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G>>),
@@ -62,7 +68,8 @@ const DecodeKernel kEntry = {reinterpret_cast<const void *>(&decode_kernel<Pol<G
 // then every sequence's remaining blocks.
 template <int G>
 using PolShare = QuantMmaPolicy<4, 128, G, PA_INT4_D128_SHARE_NW, PA_INT4_D128_SHARE_STAGES,
-                                (G >= 16 ? 1 : PA_INT4_D128_SHARE_MINB), PA_INT4_D128_SHARE_BPI>;
+                                (G >= 16 ? 1 : PA_INT4_D128_SHARE_MINB), PA_INT4_D128_SHARE_BPI, 1,
+                                PA_INT4_D128_SHARE_TMA != 0>;
 
 template <int G>
 const DecodeKernel kPrefix = {

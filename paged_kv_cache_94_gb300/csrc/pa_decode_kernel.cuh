@@ -82,11 +82,13 @@ struct Bf16Policy {
         float acc[NT][KS][4];   // O^T accumulators: rows d, cols heads
     };
 
-    __device__ static void issue(uint32_t dst, uint32_t /*extra*/, int32_t row, uint32_t bar,
-                                 const CUtensorMap *tk, const CUtensorMap *tv,
+    __device__ static uint32_t tx_bytes(uint32_t /*mask: 1*/) { return TX; }
+
+    __device__ static void issue(uint32_t dst, uint32_t /*extra*/, const int32_t (&rows)[1],
+                                 uint32_t bar, const CUtensorMap *tk, const CUtensorMap *tv,
                                  const DecodeParams & /*p*/, uint64_t pol)
     {
-        const int32_t y = row * kBlockTokens;
+        const int32_t y = rows[0] * kBlockTokens;
 #pragma unroll
         for (int h = 0; h < HALVES; ++h)
             tma_load_2d(dst + h * (TILE / HALVES), tk, h * 64, y, bar, pol);
@@ -431,14 +433,13 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
                 cp_async_mbar_arrive_noinc(bar);
             }
         } else if (lane == 0) {
-            static_assert(Pol::kLsuLoad || BPI == 1, "TMA stages hold one block");
             if (mask == 0) {
                 mbar_arrive(bar); // completes the phase with no data: the item is skipped
             } else {
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(bar, Pol::TX);
+                mbar_arrive_expect_tx(bar, Pol::tx_bytes(mask));
                 Pol::issue(ring_base + (uint32_t)(istage * Pol::STAGE),
-                           extra_base + (uint32_t)(istage * Pol::EXTRA), rows[0], bar, &tmK, &tmV,
+                           extra_base + (uint32_t)(istage * Pol::EXTRA), rows, bar, &tmK, &tmV,
                            p, pol);
             }
         }

@@ -121,7 +121,8 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 // ---------------------------------------------------------------------------
 // GQ query rows share each K/V tile: the g query heads of a kv head for each
 // of NQ new tokens (NQ > 1: multi-query decode, each token masked causally).
-template <int BITS, int D_, int GQ_, int NW_, int S_, int MINB_ = 1, int BPI_ = 2, int NQ_ = 1>
+template <int BITS, int D_, int GQ_, int NW_, int S_, int MINB_ = 1, int BPI_ = 2, int NQ_ = 1,
+          bool TMA_ = false>
 struct QuantMmaPolicy {
     static_assert(BITS == 8 || BITS == 4, "INT8 or INT4 codes");
     static_assert(BPI_ == 1 || BPI_ == 2 || BPI_ == 4, "1, 2 or 4 blocks per ring item");
@@ -162,8 +163,11 @@ struct QuantMmaPolicy {
     // and V tiles (and lanes 0-8*BPI-1 the scales), then arrives on the stage
     // barrier once its copies land (the barrier expects 32 arrivals). A block
     // whose row is < 0 (absent or bad) is not loaded.
-    static constexpr bool kLsuLoad = true;
-    static constexpr uint32_t kArrivals = 32;
+    // TMA_: lane 0 instead loads each block's K and V tiles as TMA boxes (the
+    // pool's tensor maps: 128/64-byte swizzle for INT8 as the readers expect,
+    // none for INT4) and its scale rows as 64-byte bulk copies.
+    static constexpr bool kLsuLoad = !TMA_;
+    static constexpr uint32_t kArrivals = TMA_ ? 1 : 32;
     static constexpr int CHUNKS = TILE / 16;       // 16-byte chunks per tile
 
     // Shared-memory offset of chunk c of a tile: 16-byte chunk c % (ROWB/16)
@@ -203,6 +207,28 @@ struct QuantMmaPolicy {
                 const float *sc = (kind ? p.v_scale : p.k_scale) + (size_t)rj * kBlockTokens;
                 cp_async_16(extra + 64 * t + 16 * (lane & 3), sc + 4 * (lane & 3), pol);
             }
+        }
+    }
+
+    __device__ static uint32_t tx_bytes(uint32_t mask)
+    {
+        return (uint32_t)__popc(mask) * (2u * TILE + 128u);
+    }
+
+    __device__ static void issue(uint32_t dst, uint32_t extra, const int32_t (&rows)[BPI],
+                                 uint32_t bar, const CUtensorMap *tk, const CUtensorMap *tv,
+                                 const DecodeParams &p, uint64_t pol)
+    {
+#pragma unroll
+        for (int j = 0; j < BPI; ++j) {
+            if (rows[j] < 0)
+                continue;
+            const int32_t y = rows[j] * kBlockTokens;
+            tma_load_2d(dst + j * TILE, tk, 0, y, bar, pol);
+            tma_load_2d(dst + (BPI + j) * TILE, tv, 0, y, bar, pol);
+            bulk_load_1d(extra + 64 * j, p.k_scale + (size_t)rows[j] * kBlockTokens, 64, bar, pol);
+            bulk_load_1d(extra + 64 * (BPI + j), p.v_scale + (size_t)rows[j] * kBlockTokens, 64,
+                         bar, pol);
         }
     }
 

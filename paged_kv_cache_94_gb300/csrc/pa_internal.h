@@ -33,6 +33,16 @@ const DecodeKernel *find_decode_kernel_int4(int d_h, int group);
 // (pa_share.cu).
 constexpr int kShareMembers(int g) { return g <= 2 ? 8 : 16 / g; }
 constexpr int kShareMinBlocks = 8;
+// Split charge per unit in the shared-prefix launch (items; see kSegCost):
+// sequence units, and group units.
+#ifndef PA_SHARE_SEG_COST
+#define PA_SHARE_SEG_COST 8
+#endif
+constexpr int kShareSegCost = PA_SHARE_SEG_COST;
+#ifndef PA_SHARE_GROUP_SEG_COST
+#define PA_SHARE_GROUP_SEG_COST PA_SHARE_SEG_COST
+#endif
+constexpr int kShareGroupSegCost = PA_SHARE_GROUP_SEG_COST;
 const DecodeKernel *find_prefix_kernel(int kv_dtype, int d_h, int group);
 cudaError_t launch_share_detect(const int32_t *block_tables, int max_blocks,
                                 const int32_t *context_lens, int B, int gm, int min_blocks,
