@@ -333,15 +333,14 @@ def run_native(args, rank, world, local_rank):
     flush = L2Flush(dev)
     torch.cuda.synchronize(dev)
 
-    def attend(q_, bt_, cl_, out_=None):
+    def attend(q_, bt_, cl_, out_=None, prepare=False):
         o = out if out_ is None else out_
         if w.n_q > 1:  # multi-query step: the n_q new tokens of each sequence at once
-            pa.pa_decode_mq(q_, kc, vc, bt_, cl_, w.scale, out=o, workspace=ws,
-                            dev_status=status, k_scale=ks, v_scale=vs)
-        else:
-            pa.pa_decode(q_, kc, vc, bt_, cl_, w.scale, out=o, k_scale=ks, v_scale=vs,
-                         workspace=ws, dev_status=status, num_ctas=args.num_ctas,
-                         window=w.window, share_prefix=share)
+            return pa.pa_decode_mq(q_, kc, vc, bt_, cl_, w.scale, out=o, workspace=ws,
+                                   dev_status=status, k_scale=ks, v_scale=vs, prepare=prepare)
+        return pa.pa_decode(q_, kc, vc, bt_, cl_, w.scale, out=o, k_scale=ks, v_scale=vs,
+                            workspace=ws, dev_status=status, num_ctas=args.num_ctas,
+                            window=w.window, share_prefix=share, prepare=prepare)
 
     def step():
         pa.pa_cache_write(kn, vn, slots_new, kc, vc, ks, vs, dev_status=status)
@@ -434,6 +433,13 @@ def run_native(args, rank, world, local_rank):
         returned = [torch.cuda.Event() for _ in range(2)]   # out j copied to the host
         for e in uploaded + consumed + returned:
             e.record(stream)
+        # the step's two calls, validated once per buffer (pa.Prepared)
+        calls = []
+        for j in range(2):
+            dq, dk, dv, ds, dbt, dcl = hins[j].device_views
+            calls.append((pa.pa_cache_write(dk, dv, ds, kc, vc, ks, vs, dev_status=status,
+                                            prepare=True),
+                          attend(dq, dbt, dcl, outs[j], prepare=True)))
 
         def e2e_steps(n):
             for i in range(n):
@@ -444,9 +450,8 @@ def run_native(args, rank, world, local_rank):
                 uploaded[j].record(up)
                 stream.wait_event(uploaded[j])
                 stream.wait_event(returned[j])   # out j of step i-2 is on the host
-                dq, dk, dv, ds, dbt, dcl = hins[j].device_views
-                pa.pa_cache_write(dk, dv, ds, kc, vc, ks, vs, dev_status=status)
-                attend(dq, dbt, dcl, outs[j])
+                calls[j][0]()                    # pa_cache_write
+                calls[j][1]()                    # pa_decode (or pa_decode_mq)
                 consumed[j].record(stream)
                 down.wait_event(consumed[j])
                 with torch.cuda.stream(down):

@@ -173,6 +173,27 @@ def _stream_ptr(stream) -> Optional[int]:
     return ctypes.c_void_p(s.cuda_stream)
 
 
+class Prepared:
+    """One validated library call with its arguments marshalled, issued again
+    by calling it: for a serving loop that repeats the same call on the same
+    buffers (the tensors' contents may change, not their addresses or shapes).
+    The stream is the one given at preparation, else the current stream at
+    each call. Returns what the unprepared call returns (the output tensor)."""
+
+    __slots__ = ("_fn", "_args", "_si", "_what", "_result", "_stream")
+
+    def __init__(self, fn, args, stream_index, what, result, stream):
+        self._fn, self._args, self._si = fn, list(args), stream_index
+        self._what, self._result, self._stream = what, result, stream
+
+    def __call__(self):
+        self._args[self._si] = _stream_ptr(self._stream)
+        st = self._fn(*self._args)
+        if st != 0:
+            raise PAError(st, self._what)
+        return self._result
+
+
 def _need_cuda(name: str, t: torch.Tensor, dtype=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -205,8 +226,10 @@ def geometry(k_cache: torch.Tensor, n_h: int) -> pa_geom:
 def pa_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                    k_cache: torch.Tensor, v_cache: torch.Tensor,
                    k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
-                   dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
-    """Append rows k, v [T, n_kv, d_h] (bf16) at slot_mapping [T] (int64) into the pool."""
+                   dev_status: Optional[torch.Tensor] = None, stream=None,
+                   prepare: bool = False):
+    """Append rows k, v [T, n_kv, d_h] (bf16) at slot_mapping [T] (int64) into the pool.
+    prepare=True validates and returns a Prepared call instead of running it."""
     _need_cuda("k", k, torch.bfloat16)
     _need_cuda("v", v, torch.bfloat16)
     _need_cuda("slot_mapping", slot_mapping, torch.int64)
@@ -224,10 +247,11 @@ def pa_cache_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                 raise ValueError(f"{nm} must be [num_blocks, n_kv, block_size]")
     if dev_status is not None:
         _need_cuda("dev_status", dev_status, torch.int32)
-    st = _lib().pa_cache_write(_ptr(k), _ptr(v), _ptr(slot_mapping), slot_mapping.shape[0],
-                               _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), g,
-                               _ptr(dev_status), _stream_ptr(stream))
-    _check(st, "pa_cache_write")
+    call = Prepared(_lib().pa_cache_write,
+                    [_ptr(k), _ptr(v), _ptr(slot_mapping), slot_mapping.shape[0], _ptr(k_cache),
+                     _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), g, _ptr(dev_status), None],
+                    10, "pa_cache_write", None, stream)
+    return call if prepare else call()
 
 
 _WS: dict = {}
@@ -291,7 +315,8 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
               v_scale: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
               dev_status: Optional[torch.Tensor] = None, stream=None, num_ctas: int = 0,
               window: int = 0, sink_k: Optional[torch.Tensor] = None,
-              sink_v: Optional[torch.Tensor] = None, share_prefix: bool = False) -> torch.Tensor:
+              sink_v: Optional[torch.Tensor] = None, share_prefix: bool = False,
+              prepare: bool = False):
     """Decode attention: q [B, n_h, d_h] bf16 over the paged pool -> out [B, n_h, d_h] bf16.
 
     block_tables [B, max_blocks] int32 and context_lens [B] int32 live on the device.
@@ -300,6 +325,7 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     (bf16 [B, n_kv, n_sink, d_h], INT8 pools) hold the unquantised rows of the
     first n_sink positions (pa_decode_opt). share_prefix attends blocks that
     adjacent sequences share once per group (pa_decode_opt, share_prefix).
+    prepare=True validates and returns a Prepared call instead of running it.
     """
     _need_cuda("q", q, torch.bfloat16)
     _need_cuda("k_cache", k_cache)
@@ -347,13 +373,13 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         opts = pa_decode_opts(window=int(window), n_sink=n_sink, sink_k=_ptr(sink_k),
                               sink_v=_ptr(sink_v), num_ctas=int(num_ctas),
                               share_prefix=1 if share_prefix else 0, reserved=0)
-        st = lib.pa_decode_opt(*args[:14], ctypes.byref(opts), *args[14:])
+        call = Prepared(lib.pa_decode_opt, args[:14] + [ctypes.byref(opts)] + args[14:], 16,
+                        "pa_decode", out, stream)
     elif num_ctas > 0:
-        st = lib.pa_decode_ex(*args, int(num_ctas))
+        call = Prepared(lib.pa_decode_ex, args + [int(num_ctas)], 15, "pa_decode", out, stream)
     else:
-        st = lib.pa_decode(*args)
-    _check(st, "pa_decode")
-    return out
+        call = Prepared(lib.pa_decode, args, 15, "pa_decode", out, stream)
+    return call if prepare else call()
 
 
 def pa_decode_mq(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -361,10 +387,10 @@ def pa_decode_mq(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                  out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                  dev_status: Optional[torch.Tensor] = None, stream=None,
                  k_scale: Optional[torch.Tensor] = None,
-                 v_scale: Optional[torch.Tensor] = None) -> torch.Tensor:
+                 v_scale: Optional[torch.Tensor] = None, prepare: bool = False):
     """Multi-query decode: q [B, n_q, n_h, d_h] bf16 (the last n_q tokens of each
     sequence, attending causally) over a bf16, INT8 or INT4 pool (scales as
-    pa_decode's) -> out of q's shape."""
+    pa_decode's) -> out of q's shape. prepare=True returns a Prepared call."""
     _need_cuda("q", q, torch.bfloat16)
     _need_cuda("k_cache", k_cache)
     _need_cuda("v_cache", v_cache, k_cache.dtype)
@@ -394,13 +420,13 @@ def pa_decode_mq(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         _need_cuda("workspace", workspace)
     if dev_status is not None:
         _need_cuda("dev_status", dev_status, torch.int32)
-    st = _lib().pa_decode_mq(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                             _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B,
-                             n_q, float(scale), _ptr(out), _ptr(workspace),
-                             workspace.numel() * workspace.element_size(), g, _ptr(dev_status),
-                             _stream_ptr(stream))
-    _check(st, "pa_decode_mq")
-    return out
+    call = Prepared(_lib().pa_decode_mq,
+                    [_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                     _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, n_q,
+                     float(scale), _ptr(out), _ptr(workspace),
+                     workspace.numel() * workspace.element_size(), g, _ptr(dev_status), None],
+                    16, "pa_decode_mq", out, stream)
+    return call if prepare else call()
 
 
 def pa_sink_write(k: torch.Tensor, v: torch.Tensor, seq_rows: torch.Tensor,

@@ -203,3 +203,22 @@ def test_maximum_batch(dev, dt):
     out, st = gpu_decode(w, gpu_pool(w, dev), dev)
     assert st == 0
     assert_close(out.float().cpu().numpy(), ref, f"{dt} B=8192")
+
+
+def test_prepared_calls_repeat_on_new_contents(dev):
+    # a Prepared call re-issues the same marshalled call: new input contents,
+    # new result, identical to the direct call's
+    w = make_workload("prep", Geometry(32, 8, 128), [300, 17, 1000], seed=19)
+    kc, vc, ks, vs = gpu_pool(w, dev)
+    q = w.q(dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    out = torch.empty_like(q)
+    call = pa.pa_decode(q, kc, vc, bt, cl, w.scale, out=out, prepare=True)
+    assert isinstance(call, pa.Prepared)
+    for seed in (1, 2):
+        q.copy_(torch.randn(q.shape, generator=torch.Generator().manual_seed(seed)).to(q))
+        got = call().clone()
+        ref = pa.pa_decode(q, kc, vc, bt, cl, w.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
