@@ -218,7 +218,8 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        out_dir = os.environ.get("PA_BENCH_OUT", os.path.join(ROOT, "bench_out"))
+        self.path = os.path.join(out_dir, f"clocks_rank{index}.csv")
 
     def start(self):
         try:
