@@ -368,6 +368,18 @@ pa_status pa_status_from_device(int32_t dev_word);
 int32_t pa_version(void);
 
 /*
+ * pa_wait_selftest -- exercise the failure path of the bounded pipeline
+ * waits: one CTA waits, with the decode kernel's wait primitive, on a shared
+ * barrier that nothing arrives on; after limit_us microseconds the wait gives
+ * up, PA_DEV_TIMEOUT is ORed into *dev_status (device, int32) and the kernel
+ * returns. Nothing faults or hangs and the context stays usable: read
+ * *dev_status after the stream finishes (pa_status_from_device gives
+ * PA_ERR_TIMEOUT). Errors: PA_ERR_NULL without dev_status, PA_ERR_SHAPE for
+ * limit_us outside 1..1000000, PA_ERR_CUDA if the launch fails.
+ */
+pa_status pa_wait_selftest(int32_t *dev_status, int32_t limit_us, void *stream);
+
+/*
  * pa_block_copy -- the device half of copy-on-write ([F] "Prefix Caching 与
  * Copy-on-Write": a branch that appends to a shared, partly filled last
  * block gets a new block holding a copy of the filled slots; [T] 考点 4:

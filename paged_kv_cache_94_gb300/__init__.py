@@ -45,7 +45,7 @@ EXPORTED = ["pa_cache_write", "pa_decode_workspace_size", "pa_decode_workspace_i
             "pa_decode", "pa_decode_ex", "pa_decode_noalloc", "pa_decode_default_ctas",
             "pa_plan_owner", "pa_block_copy", "pa_decode_opt", "pa_sink_write",
             "pa_decode_mq", "pa_decode_mq_workspace_size", "pa_decode_opt_workspace_size",
-            "pa_status_string", "pa_status_from_device", "pa_version",
+            "pa_status_string", "pa_status_from_device", "pa_version", "pa_wait_selftest",
             # host block manager (include/pa_alloc.h)
             "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate_prompt",
             "pa_allocator_append_slots", "pa_allocator_fork", "pa_allocator_free",
@@ -116,6 +116,8 @@ def _lib():
         lib.pa_status_from_device.argtypes = [i32]
         lib.pa_version.restype = i32
         lib.pa_version.argtypes = []
+        lib.pa_wait_selftest.restype = ctypes.c_int
+        lib.pa_wait_selftest.argtypes = [P, i32, P]
         lib.pa_decode_mq.restype = ctypes.c_int
         lib.pa_decode_mq.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, f32, P, P, sz, pa_geom,
                                      P, P]
@@ -171,6 +173,14 @@ def _ptr(t: Optional[torch.Tensor]):
 def _stream_ptr(stream) -> Optional[int]:
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def pa_wait_selftest(dev_status: torch.Tensor, limit_us: int = 2000, stream=None) -> None:
+    """Run the bounded-wait self-test: a wait on a barrier nothing arrives on
+    gives up after limit_us and sets PA_DEV_TIMEOUT in dev_status (int32, device)."""
+    _need_cuda("dev_status", dev_status, torch.int32)
+    _check(_lib().pa_wait_selftest(_ptr(dev_status), int(limit_us), _stream_ptr(stream)),
+           "pa_wait_selftest")
 
 
 class Prepared:

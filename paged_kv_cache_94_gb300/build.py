@@ -37,6 +37,7 @@ SOURCES = [
     "pa_decode_int4_mq_d128.cu",
     "pa_decode_int4_mq_d64.cu",
     "pa_share.cu",
+    "pa_selftest.cu",
     "pa_decode_noalloc.cu",
     "pa_block_copy.cu",
     "pa_alloc.cpp",

@@ -2,6 +2,7 @@
 // Every function here runs on the host and only enqueues work.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
 #include <cmath>
@@ -12,6 +13,16 @@
 #include "pa_internal.h"
 
 namespace {
+
+// An NVTX range around each entry point (named after it), so that a
+// profiler's timeline shows the library's calls; free when no tool listens.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 
 using pa::DecodeKernel;
 using pa::DecodeParams;
@@ -487,6 +498,7 @@ pa_status pa_cache_write(const void *k, const void *v, const int64_t *slot_mappi
                          int64_t num_tokens, void *k_cache, void *v_cache, float *k_scale,
                          float *v_scale, pa_geom geom, int32_t *dev_status, void *stream)
 {
+    const NvtxRange range("pa_cache_write");
     pa_status st = check_geom(geom);
     if (st != PA_OK)
         return st;
@@ -517,6 +529,7 @@ pa_status pa_block_copy(void *k_cache, void *v_cache, float *k_scale, float *v_s
                         const int32_t *pairs, int32_t num_pairs, pa_geom geom,
                         int32_t *dev_status, void *stream)
 {
+    const NvtxRange range("pa_block_copy");
     pa_status st = check_geom(geom);
     if (st != PA_OK)
         return st;
@@ -567,6 +580,7 @@ pa_status pa_decode(const void *q, const void *k_cache, const void *v_cache, con
                     void *workspace, size_t workspace_bytes, pa_geom geom, int32_t *dev_status,
                     void *stream)
 {
+    const NvtxRange range("pa_decode");
     return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
                        context_lens, num_seqs, scale, out, workspace, workspace_bytes, geom,
                        dev_status, stream, 0);
@@ -578,6 +592,7 @@ pa_status pa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
                        float scale, void *out, void *workspace, size_t workspace_bytes,
                        pa_geom geom, int32_t *dev_status, void *stream, int32_t num_ctas)
 {
+    const NvtxRange range("pa_decode_ex");
     if (num_ctas <= 0)
         return PA_ERR_SHAPE;
     return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
@@ -617,6 +632,7 @@ pa_status pa_decode_opt(const void *q, const void *k_cache, const void *v_cache,
                         size_t workspace_bytes, pa_geom geom, const pa_decode_opts *opts,
                         int32_t *dev_status, void *stream)
 {
+    const NvtxRange range("pa_decode_opt");
     return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
                        context_lens, num_seqs, scale, out, workspace, workspace_bytes, geom,
                        dev_status, stream, opts ? opts->num_ctas : 0, opts);
@@ -640,6 +656,7 @@ pa_status pa_decode_mq(const void *q, const void *k_cache, const void *v_cache,
                        int32_t n_q, float scale, void *out, void *workspace,
                        size_t workspace_bytes, pa_geom geom, int32_t *dev_status, void *stream)
 {
+    const NvtxRange range("pa_decode_mq");
     if (n_q < 1)
         return PA_ERR_SHAPE;
     return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
@@ -651,6 +668,7 @@ pa_status pa_sink_write(const void *k, const void *v, const int32_t *seq_rows,
                         const int32_t *positions, int64_t num_tokens, void *sink_k, void *sink_v,
                         int32_t n_sink, int32_t num_seqs, pa_geom geom, void *stream)
 {
+    const NvtxRange range("pa_sink_write");
     pa_status st = check_geom(geom);
     if (st != PA_OK)
         return st;
@@ -725,6 +743,17 @@ pa_status pa_status_from_device(int32_t w)
 }
 
 int32_t pa_version(void) { return 100; }
+
+pa_status pa_wait_selftest(int32_t *dev_status, int32_t limit_us, void *stream)
+{
+    if (!dev_status)
+        return PA_ERR_NULL;
+    if (limit_us < 1 || limit_us > 1000000)
+        return PA_ERR_SHAPE;
+    const cudaError_t e = pa::launch_wait_selftest(dev_status, (uint64_t)limit_us * 1000u,
+                                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
 
 } // extern "C"
 

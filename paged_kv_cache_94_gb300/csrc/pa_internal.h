@@ -44,6 +44,8 @@ constexpr int kShareSegCost = PA_SHARE_SEG_COST;
 #endif
 constexpr int kShareGroupSegCost = PA_SHARE_GROUP_SEG_COST;
 const DecodeKernel *find_prefix_kernel(int kv_dtype, int d_h, int group);
+// Bounded-wait self-test (pa_selftest.cu).
+cudaError_t launch_wait_selftest(int32_t *dev_status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_share_detect(const int32_t *block_tables, int max_blocks,
                                 const int32_t *context_lens, int B, int gm, int min_blocks,
                                 int32_t *skip, int32_t *groups, cudaStream_t stream);

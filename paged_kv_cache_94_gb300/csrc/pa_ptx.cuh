@@ -62,10 +62,11 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
-// Wait for phase `parity` of a barrier. Gives up after about one second of
-// wall time and returns false, so that a copy that never lands cannot hang
-// the GPU.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// Wait for phase `parity` of a barrier. Gives up after limit_ns of wall time
+// (about one second by default) and returns false, so that a copy that never
+// lands cannot hang the GPU.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = 1000000000ull)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -74,7 +75,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity))
                 return true;
-        if (global_timer_ns() - t0 > 1000000000ull)
+        if (global_timer_ns() - t0 > limit_ns)
             return false;
     }
 }
