@@ -110,6 +110,9 @@ __global__ void __launch_bounds__(256)
                        void *k_cache, void *v_cache, float *k_scale, float *v_scale,
                        int32_t *dev_status)
 {
+    // a decode launched next on the stream may be scheduled now; it waits for
+    // this grid to complete before reading the cache
+    asm volatile("griddepcontrol.launch_dependents;");
     constexpr int E = D / 32;
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (row >= rows)

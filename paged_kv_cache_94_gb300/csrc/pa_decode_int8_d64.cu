@@ -50,8 +50,7 @@ template <class Pol, int PASS = 0>
 cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int grid,
                       size_t smem, cudaStream_t stream)
 {
-    decode_kernel<Pol, PASS><<<grid, Pol::NW * 32, smem, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    return launch_decode<Pol, PASS>(tk, tv, p, grid, smem, stream);
 }
 
 template <int G>

@@ -329,6 +329,10 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     int32_t *misc = reinterpret_cast<int32_t *>(smem + L::kOffMisc);
     int32_t *P = reinterpret_cast<int32_t *>(smem + L::kOffPrefix);
 
+    // The launch may start before the previous kernel on the stream ends (a
+    // programmatic dependent launch: the cache append, or the group
+    // detection): wait for it to complete before the first read.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_h = p.n_kv * (GQ / Pol::NQ); // query heads per token
 
@@ -554,6 +558,28 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         for (int64_t kk = fail_k; kk < r.issued; ++kk)
             mbar_wait(bar_base + 8u * (uint32_t)(kk % S), (uint32_t)((kk / S) & 1));
     }
+}
+
+// Launch of decode_kernel<Pol, PASS> as a programmatic dependent launch: its
+// CTAs are scheduled while the previous kernel on the stream (the cache
+// append, or the group detection) finishes, and wait for that kernel's
+// completion in their first instruction. After anything else on the stream
+// it behaves as a plain launch.
+template <class Pol, int PASS>
+cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
+                          int grid, size_t smem, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(Pol::NW * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<Pol, PASS>, tk, tv, p);
 }
 
 } // namespace pa

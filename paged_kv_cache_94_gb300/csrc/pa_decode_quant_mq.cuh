@@ -19,8 +19,7 @@ template <class Pol>
 cudaError_t mq_launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                          int grid, size_t smem, cudaStream_t stream)
 {
-    decode_kernel<Pol><<<grid, Pol::NW * 32, smem, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    return launch_decode<Pol, 0>(tk, tv, p, grid, smem, stream);
 }
 
 // NW warps, S ring stages, BPI blocks per item, MINB resident CTAs per SM

@@ -83,6 +83,9 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ int32_t lcp[kThreads * kPer];
     __shared__ int32_t wsum[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the decode launch that reads these results may be scheduled now; it
+    // waits for this grid to complete before its first read
+    asm volatile("griddepcontrol.launch_dependents;");
 
     // ---- lcp with the previous sequence: one warp per sequence; each round
     // compares 256 entries with all loads in flight at once
