@@ -24,7 +24,7 @@ namespace pa {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kPer = 8; // sequences per thread (B <= 8192)
+constexpr int kMaxPer = 8; // sequences per thread at most (B <= 8192)
 
 __device__ __forceinline__ int32_t blocks_of(int32_t ctx, int32_t max_blocks)
 {
@@ -34,7 +34,7 @@ __device__ __forceinline__ int32_t blocks_of(int32_t ctx, int32_t max_blocks)
 }
 
 // Inclusive block-wide scan of kPer values per thread (op: add or max).
-template <bool MAX>
+template <bool MAX, int kPer>
 __device__ __forceinline__ void block_scan(int32_t (&v)[kPer], int32_t *wsum)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -75,6 +75,8 @@ __device__ __forceinline__ void block_scan(int32_t (&v)[kPer], int32_t *wsum)
     __syncthreads();
 }
 
+// kPer sequences per thread: 1 up to 1024 sequences, else 8.
+template <int kPer>
 __global__ void __launch_bounds__(kThreads)
     share_detect_kernel(const int32_t *__restrict__ block_tables, int max_blocks,
                         const int32_t *__restrict__ context_lens, int B, int gm, int min_blocks,
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(kThreads)
         const int b = tid * kPer + i;
         st[i] = (b < B && (b == 0 || lcp[b] < min_blocks)) ? b : INT32_MIN;
     }
-    block_scan<true>(st, wsum);
+    block_scan<true, kPer>(st, wsum);
 
     // ---- chunks of gm members per run: leaders own groups
     int32_t lead[kPer], cnt[kPer];
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int i = 0; i < kPer; ++i)
         idx[i] = lead[i] > 0 ? 1 : 0;
-    block_scan<false>(idx, wsum);
+    block_scan<false, kPer>(idx, wsum);
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
         const int b = tid * kPer + i;
@@ -186,10 +188,14 @@ cudaError_t launch_share_detect(const int32_t *block_tables, int max_blocks,
                                 const int32_t *context_lens, int B, int gm, int min_blocks,
                                 int32_t *skip, int32_t *groups, cudaStream_t stream)
 {
-    if (B < 1 || B > kThreads * kPer || gm < 2)
+    if (B < 1 || B > kThreads * kMaxPer || gm < 2)
         return cudaErrorInvalidValue;
-    share_detect_kernel<<<1, kThreads, 0, stream>>>(block_tables, max_blocks, context_lens, B, gm,
-                                                    min_blocks, skip, groups);
+    if (B <= kThreads)
+        share_detect_kernel<1><<<1, kThreads, 0, stream>>>(block_tables, max_blocks, context_lens,
+                                                           B, gm, min_blocks, skip, groups);
+    else
+        share_detect_kernel<kMaxPer><<<1, kThreads, 0, stream>>>(
+            block_tables, max_blocks, context_lens, B, gm, min_blocks, skip, groups);
     return cudaGetLastError();
 }
 
