@@ -155,7 +155,8 @@ struct QuantMmaPolicy {
         float sinv;             // 1 / sbase (0 while sbase is 0)
         float qsum[NT][2];      // sum_d of the fp16 Q' values of head 2t4 + e (INT4: even k-steps)
         float qsum1[NT][2];     // INT4: the same over the odd k-steps
-        float wpart[NT][2];     // this lane's sum of the fp16 weights of head 2t4 + e
+        float wacc[NT][4];      // sum of the fp16 weights per head: the PV accumulator
+                                // of an all-ones V tile (every row holds the sum)
     };
 
     // Tiles of 1-2 KiB move faster as 16-byte cp.async copies spread over the
@@ -378,8 +379,8 @@ struct QuantMmaPolicy {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-                st.wpart[nt][e] = 0.f;
+            for (int e = 0; e < 4; ++e)
+                st.wacc[nt][e] = 0.f;
     }
 
     // One item of BPI 16-token blocks: block j's K codes at kt + j*TILE, its V
@@ -392,7 +393,7 @@ struct QuantMmaPolicy {
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
 
-        // ---- S^T = Kcode . Q'^T per block (two accumulator chains per block)
+        // ---- S^T = Kcode . Q'^T per block (INT4: even and odd k-steps apart)
         float s0[BPI][NT][4], s1[BPI][NT][4];
 #pragma unroll
         for (int j = 0; j < BPI; ++j)
@@ -404,7 +405,7 @@ struct QuantMmaPolicy {
         auto kstep = [&](int j, int kk, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                if (kk & 1)
+                if (BITS == 4 && (kk & 1)) // INT4: the x16 k-steps; INT8: one chain per block
                     mma_f16_16816(s1[j][nt], a0, a1, a2, a3, st.qf[nt][kk][0], st.qf[nt][kk][1]);
                 else
                     mma_f16_16816(s0[j][nt], a0, a1, a2, a3, st.qf[nt][kk][0], st.qf[nt][kk][1]);
@@ -475,7 +476,7 @@ struct QuantMmaPolicy {
                 for (int c = 0; c < 4; ++c) {
                     float sb;
                     if constexpr (BITS == 8)
-                        sb = fmaf(-kBias, st.qsum[nt][c & 1], s0[j][nt][c] + s1[j][nt][c]);
+                        sb = fmaf(-kBias, st.qsum[nt][c & 1], s0[j][nt][c]);
                     else
                         sb = fmaf(fmaf(-kBiasHi, st.qsum1[nt][c & 1], s1[j][nt][c]), 0.0625f,
                                   fmaf(-kBias, st.qsum[nt][c & 1], s0[j][nt][c]));
@@ -507,7 +508,8 @@ struct QuantMmaPolicy {
                         const float alpha = fast_exp2(st.m[nt][e] - mx);
                         st.m[nt][e] = mx;
                         st.l[nt][e] *= alpha;
-                        st.wpart[nt][e] *= alpha;
+                        st.wacc[nt][e] *= alpha;
+                        st.wacc[nt][e + 2] *= alpha;
 #pragma unroll
                         for (int mt = 0; mt < KS; ++mt) {
                             st.acc[nt][mt][e] *= alpha;
@@ -548,8 +550,8 @@ struct QuantMmaPolicy {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-                for (int e = 0; e < 2; ++e)
-                    st.wpart[nt][e] *= f;
+                for (int e = 0; e < 4; ++e)
+                    st.wacc[nt][e] *= f;
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
@@ -560,7 +562,6 @@ struct QuantMmaPolicy {
             st.sinv = 1.f / svm;
         }
         // W^T as B fragments (tokens x heads): transpose of the score layout.
-        // The lane's weights, as rounded to fp16, join its bias sums.
         uint32_t pb0[BPI][NT], pb1[BPI][NT];
 #pragma unroll
         for (int j = 0; j < BPI; ++j) {
@@ -569,11 +570,6 @@ struct QuantMmaPolicy {
             for (int nt = 0; nt < NT; ++nt) {
                 const uint32_t w0 = pack_f16x2(pr[j][nt][0] * r_lo, pr[j][nt][1] * r_lo);
                 const uint32_t w1 = pack_f16x2(pr[j][nt][2] * r_hi, pr[j][nt][3] * r_hi);
-                float a, b, c, d;
-                h2_to_f2(w0, a, b);
-                h2_to_f2(w1, c, d);
-                st.wpart[nt][0] += a + c;
-                st.wpart[nt][1] += b + d;
                 pb0[j][nt] = movmatrix_trans(w0);
                 pb1[j][nt] = movmatrix_trans(w1);
             }
@@ -591,6 +587,11 @@ struct QuantMmaPolicy {
                 for (int nt = 0; nt < NT; ++nt)
                     mma_f16_16816(st.acc[nt][mt], a0, a1, a2, a3, pb0[j][nt], pb1[j][nt]);
             };
+            // the weights' sums (for the codes' bias): an all-ones V tile
+            constexpr uint32_t kOnes = 0x3C003C00u; // fp16x2 {1, 1}
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma_f16_16816(st.wacc[nt], kOnes, kOnes, kOnes, kOnes, pb0[j][nt], pb1[j][nt]);
             if constexpr (BITS == 8) {
                 constexpr int WPR = D / 32; // 32-bit words per thread per row
                 uint32_t ra[WPR], rb[WPR], rc[WPR], rd[WPR];
@@ -692,10 +693,7 @@ struct QuantMmaPolicy {
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                float ws = st.wpart[nt][c];
-                ws += __shfl_xor_sync(0xffffffffu, ws, 4);
-                ws += __shfl_xor_sync(0xffffffffu, ws, 8);
-                ws += __shfl_xor_sync(0xffffffffu, ws, 16);
+                const float ws = st.wacc[nt][c]; // the head's whole weight sum
                 const float bias = kBias * ws;
                 const float bias1 = (BITS == 8 ? kBias : kBiasHi) * ws;
                 const float sb1 = BITS == 8 ? st.sbase : st.sbase * 0.0625f;
