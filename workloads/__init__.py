@@ -258,6 +258,8 @@ def make_workload(name: str, geom: Geometry, context_lens, seed: int,
     bs = geom.block_size
     pl = np.zeros(B, np.int32) if prefix_len is None else np.asarray(prefix_len, np.int32)
     gr = np.full(B, -1, np.int32) if group is None else np.asarray(group, np.int32)
+    # a shared prefix is whole blocks (the blocks a group's members point at)
+    assert (pl % bs == 0).all(), "prefix_len must be a multiple of the block size"
     nblk = [-(-int(c) // bs) for c in ctx]
     # blocks actually handed out (a shared prefix counts once per group)
     needed = 0
