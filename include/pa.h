@@ -297,6 +297,16 @@ pa_status pa_decode_mq(const void *q, const void *k_cache, const void *v_cache,
                        int32_t n_q, float scale, void *out, void *workspace,
                        size_t workspace_bytes, pa_geom geom, int32_t *dev_status, void *stream);
 
+/* pa_decode_mq with the work split over exactly num_ctas CTAs (> 0), as
+ * pa_decode_ex does for pa_decode; the workspace is
+ * pa_decode_mq_workspace_size(geom, num_seqs, n_q, num_ctas). */
+pa_status pa_decode_mq_ex(const void *q, const void *k_cache, const void *v_cache,
+                          const float *k_scale, const float *v_scale,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *context_lens, int32_t num_seqs, int32_t n_q,
+                          float scale, void *out, void *workspace, size_t workspace_bytes,
+                          pa_geom geom, int32_t *dev_status, void *stream, int32_t num_ctas);
+
 /* Workspace bytes pa_decode_mq needs (num_ctas 0: the default grid); 0 when
  * the geometry or n_q is not supported. */
 size_t pa_decode_mq_workspace_size(pa_geom geom, int32_t num_seqs, int32_t n_q,
@@ -333,8 +343,10 @@ pa_status pa_sink_write(const void *k, const void *v, const int32_t *seq_rows,
  * exceeds that size is refused with PA_ERR_WORKSPACE before anything is
  * enqueued (use pa_decode with a workspace of its own instead).
  * The first call on a device looks up the array's device address (which may
- * load the library's device code); make that first call before any stream
- * capture. Each call clears the array's counter area on `stream`, then runs
+ * load the library's device code) and keeps it for the life of the process;
+ * make that first call before any stream capture. cudaDeviceReset on a
+ * device unloads the array with the context, so the kept address goes stale:
+ * after a reset, reload the library before calling this entry point again. Each call clears the array's counter area on `stream`, then runs
  * the decode there. All calls on a device share the one array, so calls whose
  * GPU work can overlap (different streams without ordering) race and give
  * wrong results: order them on one stream.

@@ -78,6 +78,9 @@ def _load():
         lib.oracle_decode_window.restype = ctypes.c_int
         lib.oracle_decode_window.argtypes = [P, P, P, P, P, i32, P, i32, P, i32, i32, i32, i32,
                                              i32, i64, dbl, i32, i32, P, P, P]
+        lib.oracle_scores.restype = ctypes.c_int
+        lib.oracle_scores.argtypes = [P, P, P, i32, P, i32, P, i32, i32, i32, i32, i32, i64, dbl,
+                                      i64, P]
         _lib = lib
     return _lib
 
@@ -181,6 +184,24 @@ def decode(q_bits: np.ndarray, pool: Pool, block_tables: np.ndarray, context_len
                            _ptr(pool.v_scale), KV_KIND[pool.kv_dtype], _ptr(bt),
                            bt.shape[1], _ptr(ctx), B, n_h, pool.n_kv, pool.d_h, pool.block_size,
                            pool.num_blocks, float(scale), _ptr(out))
+    return out, st
+
+
+def scores(q_bits: np.ndarray, pool: Pool, block_tables: np.ndarray, context_lens: np.ndarray,
+           n_h: int, scale: float) -> tuple[np.ndarray, int]:
+    """Raw scores scale * <q_h, K_j>: float64 [B, n_h, max ctx] (NaN past a
+    sequence's context) and status."""
+    lib = _load()
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B = ctx.shape[0]
+    assert q_bits.shape == (B, n_h, pool.d_h)
+    max_ctx = max(int(ctx.max()) if B else 0, 1)
+    out = np.zeros((B, n_h, max_ctx), dtype=np.float64)
+    st = lib.oracle_scores(_ptr(q_bits), _ptr(pool.k), _ptr(pool.k_scale), KV_KIND[pool.kv_dtype],
+                           _ptr(bt), bt.shape[1], _ptr(ctx), B, n_h, pool.n_kv, pool.d_h,
+                           pool.block_size, pool.num_blocks, float(scale), max_ctx, _ptr(out))
     return out, st
 
 

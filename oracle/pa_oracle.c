@@ -524,3 +524,53 @@ int oracle_decode_mq(const uint16_t *q, const void *k_cache, const void *v_cache
     free(scores);
     return status;
 }
+
+/* ------------------------------------------------------------------------
+ * The raw attention scores s_j = scale * <q_h, K_j> of every query head over
+ * its sequence's cached tokens, in double precision: the argument of the
+ * softmax in [F] "自回归解码与 KV Cache 的物理来源" (eq. for o_t), with K_j
+ * found through the block table as in oracle_decode. Tests use them to check
+ * the dynamic range an input reaches (how far the running maximum climbs).
+ * out: double [B][n_h][max_ctx]; entries at j >= ctx_b are NaN. Sequences
+ * with a bad context length or block id report it and get NaN rows.
+ * ---------------------------------------------------------------------- */
+int oracle_scores(const uint16_t *q, const void *k_cache, const float *k_scale, int kv_kind,
+                  const int32_t *block_tables, int max_blocks_per_seq,
+                  const int32_t *context_lens, int B, int n_h, int n_kv, int d_h,
+                  int block_size, int64_t num_blocks, double scale, int64_t max_ctx,
+                  double *out)
+{
+    int status = 0;
+    int g = n_h / n_kv;
+    for (int b = 0; b < B; ++b) {
+        int64_t ctx = context_lens[b];
+        int bad = ctx < 0 || ctx > max_ctx || ctx > (int64_t)max_blocks_per_seq * block_size;
+        if (bad)
+            status |= ORC_BAD_CTX;
+        for (int64_t j = 0; !bad && j < ctx; j += block_size) {
+            int32_t blk = block_tables[(int64_t)b * max_blocks_per_seq + j / block_size];
+            if (blk < 0 || blk >= num_blocks) {
+                status |= ORC_BAD_BLOCK;
+                bad = 1;
+            }
+        }
+        for (int h = 0; h < n_h; ++h) {
+            double *row_out = out + ((int64_t)b * n_h + h) * max_ctx;
+            for (int64_t j = 0; j < max_ctx; ++j)
+                row_out[j] = NAN;
+            if (bad)
+                continue;
+            const uint16_t *qh = q + ((int64_t)b * n_h + h) * d_h;
+            for (int64_t j = 0; j < ctx; ++j) {
+                int64_t blk = block_tables[(int64_t)b * max_blocks_per_seq + j / block_size];
+                int64_t row = (blk * n_kv + h / g) * block_size + j % block_size;
+                double dot = 0.0;
+                for (int d = 0; d < d_h; ++d)
+                    dot += (double)bf16_bits_to_float(qh[d]) *
+                           cached_elem(k_cache, k_scale, kv_kind, row, d, d_h);
+                row_out[j] = dot * scale;
+            }
+        }
+    }
+    return status;
+}

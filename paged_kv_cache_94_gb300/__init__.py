@@ -44,7 +44,7 @@ PA_ERR_STATE = -13
 EXPORTED = ["pa_cache_write", "pa_decode_workspace_size", "pa_decode_workspace_init",
             "pa_decode", "pa_decode_ex", "pa_decode_noalloc", "pa_decode_default_ctas",
             "pa_plan_owner", "pa_block_copy", "pa_decode_opt", "pa_sink_write",
-            "pa_decode_mq", "pa_decode_mq_workspace_size", "pa_decode_opt_workspace_size",
+            "pa_decode_mq", "pa_decode_mq_ex", "pa_decode_mq_workspace_size", "pa_decode_opt_workspace_size",
             "pa_status_string", "pa_status_from_device", "pa_version", "pa_wait_selftest",
             # host block manager (include/pa_alloc.h)
             "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate_prompt",
@@ -121,6 +121,8 @@ def _lib():
         lib.pa_decode_mq.restype = ctypes.c_int
         lib.pa_decode_mq.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, f32, P, P, sz, pa_geom,
                                      P, P]
+        lib.pa_decode_mq_ex.restype = ctypes.c_int
+        lib.pa_decode_mq_ex.argtypes = lib.pa_decode_mq.argtypes + [i32]
         lib.pa_decode_mq_workspace_size.restype = sz
         lib.pa_decode_mq_workspace_size.argtypes = [pa_geom, i32, i32, i32]
         lib.pa_decode_opt_workspace_size.restype = sz
@@ -397,10 +399,12 @@ def pa_decode_mq(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                  out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                  dev_status: Optional[torch.Tensor] = None, stream=None,
                  k_scale: Optional[torch.Tensor] = None,
-                 v_scale: Optional[torch.Tensor] = None, prepare: bool = False):
+                 v_scale: Optional[torch.Tensor] = None, prepare: bool = False,
+                 num_ctas: int = 0):
     """Multi-query decode: q [B, n_q, n_h, d_h] bf16 (the last n_q tokens of each
     sequence, attending causally) over a bf16, INT8 or INT4 pool (scales as
-    pa_decode's) -> out of q's shape. prepare=True returns a Prepared call."""
+    pa_decode's) -> out of q's shape. num_ctas > 0 forces the CTA count
+    (pa_decode_mq_ex). prepare=True returns a Prepared call."""
     _need_cuda("q", q, torch.bfloat16)
     _need_cuda("k_cache", k_cache)
     _need_cuda("v_cache", v_cache, k_cache.dtype)
@@ -425,17 +429,20 @@ def pa_decode_mq(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         if out.shape != q.shape:
             raise ValueError("out must have the shape of q")
     if workspace is None:
-        workspace = decode_workspace(g, B, q.device, 0, stream, n_q=n_q)
+        workspace = decode_workspace(g, B, q.device, num_ctas, stream, n_q=n_q)
     else:
         _need_cuda("workspace", workspace)
     if dev_status is not None:
         _need_cuda("dev_status", dev_status, torch.int32)
-    call = Prepared(_lib().pa_decode_mq,
-                    [_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                     _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, n_q,
-                     float(scale), _ptr(out), _ptr(workspace),
-                     workspace.numel() * workspace.element_size(), g, _ptr(dev_status), None],
-                    16, "pa_decode_mq", out, stream)
+    args = [_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+            _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, n_q,
+            float(scale), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), g, _ptr(dev_status), None]
+    if num_ctas > 0:
+        call = Prepared(_lib().pa_decode_mq_ex, args + [int(num_ctas)], 16, "pa_decode_mq", out,
+                        stream)
+    else:
+        call = Prepared(_lib().pa_decode_mq, args, 16, "pa_decode_mq", out, stream)
     return call if prepare else call()
 
 

@@ -664,6 +664,21 @@ pa_status pa_decode_mq(const void *q, const void *k_cache, const void *v_cache,
                        dev_status, stream, 0, nullptr, n_q);
 }
 
+pa_status pa_decode_mq_ex(const void *q, const void *k_cache, const void *v_cache,
+                          const float *k_scale, const float *v_scale,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *context_lens, int32_t num_seqs, int32_t n_q,
+                          float scale, void *out, void *workspace, size_t workspace_bytes,
+                          pa_geom geom, int32_t *dev_status, void *stream, int32_t num_ctas)
+{
+    const NvtxRange range("pa_decode_mq_ex");
+    if (n_q < 1 || num_ctas <= 0)
+        return PA_ERR_SHAPE;
+    return decode_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                       context_lens, num_seqs, scale, out, workspace, workspace_bytes, geom,
+                       dev_status, stream, num_ctas, nullptr, n_q);
+}
+
 pa_status pa_sink_write(const void *k, const void *v, const int32_t *seq_rows,
                         const int32_t *positions, int64_t num_tokens, void *sink_k, void *sink_v,
                         int32_t n_sink, int32_t num_seqs, pa_geom geom, void *stream)

@@ -14,6 +14,9 @@
 // that device is current and remembers it. Every later call on the device
 // reuses that address. The lookup can load the library's device code, so the
 // first call on a device should happen before any stream capture begins.
+// The address belongs to the device's primary context: cudaDeviceReset
+// destroys it, and a process that resets a device must reload the library
+// before it calls this entry point on that device again.
 #include <cuda_runtime.h>
 
 #include <mutex>

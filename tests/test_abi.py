@@ -107,6 +107,10 @@ def test_decode_argument_checks(lib):
     assert lib.pa_decode(*args(q=ctypes.c_void_p(264))) == -11
     assert lib.pa_decode(*args(ws=ctypes.c_void_p(272))) == -11
     assert lib.pa_decode_ex(*args(), 0) == -2
+    mq = args()[:9] + [2] + args()[9:]   # n_q = 2 after num_seqs
+    assert lib.pa_decode_mq_ex(*mq, 0) == -2    # num_ctas must be > 0
+    mq[9] = 0
+    assert lib.pa_decode_mq_ex(*mq, 8) == -2    # n_q must be >= 1
     assert lib.pa_decode_workspace_size(_geom(n_h=30), 4, 0) == 0
 
 

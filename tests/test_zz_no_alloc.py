@@ -4,9 +4,10 @@ Some callers may not allocate device memory where they run decode attention
 (a plugin whose host framework owns all device memory, a serving loop that
 cannot afford an allocation mid-step). pa_decode_noalloc serves them with the
 library's own fixed scratch array instead of a caller workspace. These tests
-call it through the C ABI and check that it returns what pa_decode returns,
-within the parity tolerance, on two calls in a row, and that a batch too big
-for the fixed array is refused before any work is queued.
+call it through the C ABI and check, on two calls in a row, that it returns
+what pa_decode returns and what the CPU oracle computes, both within the
+parity tolerance, and that a batch too big for the fixed array is refused
+before any work is queued.
 
 This file is named so that pytest collects it last.
 """
@@ -17,7 +18,7 @@ import pytest
 import torch
 
 import paged_kv_cache_94_gb300 as pa
-from tests.gpu_helpers import TOL, gpu_pool
+from tests.gpu_helpers import TOL, assert_close, gpu_pool, oracle_full
 from workloads import Geometry, make_workload
 
 pytestmark = pytest.mark.gpu
@@ -78,6 +79,8 @@ def test_noalloc_matches_pa_decode_two_calls_in_a_row(dev):
         assert torch.isfinite(got).all()
         excess = (got - want).abs() - TOL * (1 + want.abs())
         assert excess.max().item() <= 0, f"{w.name}: max |d| {(got - want).abs().max().item()}"
+        ref, _ = oracle_full(w)
+        assert_close(got.cpu().numpy(), ref, f"{w.name} against the oracle")
 
 
 def test_noalloc_refuses_batches_beyond_its_scratch(dev):

@@ -33,6 +33,28 @@ import torch
 
 BLOCK_SIZE = 16
 
+# Value profiles of q, K and V. "normal" draws every element from N(0, 1);
+# the others reshape those draws to reach the dynamic range real K/V has:
+#   rising       keys climb a staircase along the context (RISE_LEVELS steps
+#                of RISE_PERIOD tokens, about RISE_NATS of score each, then
+#                back down); queries lean along the same direction
+#   v_range      V rows scaled per (token, kv head) by 10**U(-3, 3)
+#   kv_range     K and V rows both scaled that way, independently
+#   q_big, q_small, q_zero   queries times 1e3, times 1e-3, or zero
+#   same_keys    one key row per kv head shared by every position
+#   onehot       keys e_(j mod d_h); each sequence's first new token has key
+#                2 * e_ONEHOT_DIM and every query is e_ONEHOT_DIM
+#   sink_outlier position 0 of each sequence has a key about SINK_NATS above
+#                the typical score (the outlier first token that motivates
+#                keeping sink tokens, "kv-cache-guide" §4.3)
+PROFILES = ("normal", "rising", "v_range", "kv_range", "q_big", "q_small", "q_zero",
+            "same_keys", "onehot", "sink_outlier")
+RISE_PERIOD = 48
+RISE_LEVELS = 12
+RISE_NATS = 8.0
+SINK_NATS = 12.5
+ONEHOT_DIM = 5
+
 
 @dataclass(frozen=True)
 class Geometry:
@@ -71,6 +93,7 @@ class Workload:
     description: str = ""
     window: int = 0                   # > 0: the step attends the last `window` tokens only
     n_q: int = 1                      # new tokens per sequence (> 1: multi-query step)
+    profile: str = "normal"           # value distribution of q, K and V (see PROFILES)
     # streams are generated lazily; cache of (stream id) -> (k, v) on a device
     _cache: dict = field(default_factory=dict, repr=False)
 
@@ -94,12 +117,69 @@ class Workload:
     def _stream_seed(self, stream: int) -> int:
         return (self.seed * 1_000_003 + 7919 * (stream + 1)) & 0x7FFF_FFFF_FFFF
 
-    def _gen_rows(self, stream: int, n: int, device) -> tuple[torch.Tensor, torch.Tensor]:
+    def _gen_rows(self, stream: int, n: int, device, pos0: int = 0
+                  ) -> tuple[torch.Tensor, torch.Tensor]:
+        """K and V rows of `n` consecutive positions of one stream, starting at
+        sequence position pos0: bf16 [n, n_kv, d_h]."""
         gen = torch.Generator(device=device)
         gen.manual_seed(self._stream_seed(stream))
         shape = (n, self.geom.n_kv, self.geom.d_h)
-        k = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
-        v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+        k = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+        v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+        if self.profile != "normal":
+            k, v = self._shape_rows(k, v, gen, stream, pos0, device)
+        return k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+    def _direction(self, device) -> torch.Tensor:
+        """A fixed +-1 vector per kv head, float32 [n_kv, d_h]: the direction
+        the "rising" and "sink_outlier" profiles add to q and to keys."""
+        gen = torch.Generator(device=device)
+        gen.manual_seed(self._stream_seed(3_000_000))
+        bits = torch.randint(0, 2, (self.geom.n_kv, self.geom.d_h), generator=gen, device=device)
+        return bits.to(torch.float32) * 2 - 1
+
+    def _shape_rows(self, k, v, gen, stream, pos0, device):
+        """Apply the workload's value profile to freshly drawn N(0,1) rows."""
+        n, n_kv, d = k.shape
+        pos = torch.arange(pos0, pos0 + n, device=device)
+        prof = self.profile
+        if prof == "rising":
+            # a staircase along the context, RISE_LEVELS steps of RISE_PERIOD
+            # tokens, then back to the bottom: each step adds about RISE_NATS
+            # to every score of a query leaning along the direction
+            level = ((pos // RISE_PERIOD) % RISE_LEVELS).to(torch.float32)
+            step = RISE_NATS / math.sqrt(d)
+            k = k + (level * step)[:, None, None] * self._direction(device)[None]
+        elif prof in ("v_range", "kv_range"):
+            # per (token, kv head) magnitudes log-uniform over 1e-3 .. 1e3
+            amp_v = 10.0 ** (torch.rand((n, n_kv, 1), generator=gen, device=device) * 6 - 3)
+            v = v * amp_v
+            if prof == "kv_range":
+                amp_k = 10.0 ** (torch.rand((n, n_kv, 1), generator=gen, device=device) * 6 - 3)
+                k = k * amp_k
+        elif prof == "same_keys":
+            # every key of every sequence equals one fixed row per kv head
+            g2 = torch.Generator(device=device)
+            g2.manual_seed(self._stream_seed(3_000_001))
+            row = torch.randn((1, n_kv, d), generator=g2, device=device)
+            k = row.expand(n, n_kv, d).clone()
+        elif prof == "onehot":
+            # key at position j is the unit vector e_(j mod d_h); in a
+            # sequence's private rows, the row of its first new token is
+            # 2 * e_ONEHOT_DIM instead, the only key with a score of 2 * scale
+            k = torch.zeros_like(k)
+            k[torch.arange(n, device=device), :, pos % d] = 1.0
+            if stream < 1_000_000 and n - self.n_q >= 0:
+                j = n - self.n_q
+                k[j] = 0.0
+                k[j, :, ONEHOT_DIM] = 2.0
+        elif prof == "sink_outlier":
+            # position 0 of every sequence carries a key leaning along the
+            # direction, about SINK_NATS above the typical score
+            if pos0 == 0 and n > 0:
+                k[0] = k[0] + (SINK_NATS / math.sqrt(d)) * self._direction(device)
+        elif prof not in ("q_big", "q_small", "q_zero"):
+            raise ValueError(f"unknown profile {prof}")
         return k, v
 
     def _prefix_stream(self, grp: int) -> int:
@@ -114,7 +194,7 @@ class Workload:
             kp, vp = self._gen_rows(self._prefix_stream(int(self.group[b])), p, device)
             ks.append(kp)
             vs.append(vp)
-        ko, vo = self._gen_rows(b, ctx - p, device)
+        ko, vo = self._gen_rows(b, ctx - p, device, pos0=p)
         ks.append(ko)
         vs.append(vo)
         return torch.cat(ks, 0), torch.cat(vs, 0)
@@ -128,6 +208,21 @@ class Workload:
         if self.n_q > 1:
             shape = (self.B, self.n_q) + shape[1:]
         x = torch.randn(shape, generator=gen, device=device)
+        prof = self.profile
+        if prof in ("rising", "sink_outlier"):
+            # every query head leans along its kv head's direction (the
+            # noise halved so that <u, q> stays near d_h for every head)
+            u = self._direction(device).repeat_interleave(self.geom.g, dim=0)
+            x = 0.5 * x + u
+        elif prof == "q_big":
+            x = x * 1e3
+        elif prof == "q_small":
+            x = x * 1e-3
+        elif prof == "q_zero":
+            x = torch.zeros_like(x)
+        elif prof == "onehot":
+            x = torch.zeros_like(x)
+            x[..., ONEHOT_DIM] = 1.0
         return x.to(torch.bfloat16)
 
     # ------------------------------------------------------------------ slots
@@ -163,7 +258,7 @@ class Workload:
             ko = vo = None
             if ctx > 0:
                 assert max(ctx - self.n_q, 0) >= p, "new tokens must be private to their sequence"
-                ko, vo = self._gen_rows(b, ctx - p, device)
+                ko, vo = self._gen_rows(b, ctx - p, device, pos0=p)
             for pos in range(ctx - self.n_q, ctx):
                 ks.append(ko[pos - p] if pos >= 0 else z)
                 vs.append(vo[pos - p] if pos >= 0 else z)
@@ -190,7 +285,7 @@ class Workload:
                 yield from self._chunk(k, v, self.slot_of(b, np.arange(p)), max_rows)
             n_priv = ctx - self.n_q - p
             if n_priv > 0:
-                k, v = self._gen_rows(b, ctx - p, device)
+                k, v = self._gen_rows(b, ctx - p, device, pos0=p)
                 yield from self._chunk(k[:n_priv], v[:n_priv],
                                        self.slot_of(b, np.arange(p, ctx - self.n_q)), max_rows)
 
@@ -247,7 +342,7 @@ def make_workload(name: str, geom: Geometry, context_lens, seed: int,
                   pool_factor: float = 1.1, num_blocks: Optional[int] = None,
                   prefix_len=None, group=None, scale: Optional[float] = None,
                   extra_table_cols: int = 0, description: str = "",
-                  window: int = 0, n_q: int = 1) -> Workload:
+                  window: int = 0, n_q: int = 1, profile: str = "normal") -> Workload:
     """Build a workload from explicit context lengths.
 
     pool_factor: the physical pool holds ceil(pool_factor * blocks needed) blocks
@@ -279,9 +374,12 @@ def make_workload(name: str, geom: Geometry, context_lens, seed: int,
     tables = _deal_tables(perm, ctx, bs, pl, gr, max(max_blocks, 1))
     if scale is None:
         scale = 1.0 / math.sqrt(geom.d_h)
+    if profile not in PROFILES:
+        raise ValueError(f"unknown profile {profile}")
     return Workload(name=name, geom=geom, seed=seed, context_lens=ctx, block_tables=tables,
                     num_blocks=int(num_blocks), scale=float(scale), prefix_len=pl, group=gr,
-                    description=description, window=int(window), n_q=int(n_q))
+                    description=description, window=int(window), n_q=int(n_q),
+                    profile=profile)
 
 
 # ---------------------------------------------------------------------------
