@@ -1,64 +1,89 @@
-"""Plain Python block allocator with chained-hash prefix caching and
-copy-on-write (TEST INFRASTRUCTURE ONLY).
+"""Plain Python block manager with prefix caching and copy-on-write
+(TEST INFRASTRUCTURE ONLY).
 
-This is the oracle for the native allocator in the CUDA library and for the
-device block copy. Only the test suite and ``bench.py``'s CPU legs use it; it
-shares no code with the library.
+The oracle for the native block manager of the CUDA library and for the
+device block copy. Only the test suite and ``bench.py``'s CPU legs use it;
+it shares no code with the library.
 
-What it follows ("LLM 推理底层：KV Cache 显存几何、GQA/MLA 压缩与 PagedAttention 调度",
-section "Prefix Caching 与 Copy-on-Write" and its allocator reference):
-  * a full block k of a prompt is named by the chained hash
-        H_k = Hash(H_{k-1}, tokens of block k),   H_{-1} = 0,
-    with Hash = BLAKE2b, 8-byte digest, over the parent as 8 little-endian
-    bytes followed by each token id as 4 little-endian bytes;
-  * a block whose reference count drops to zero is not wiped: it joins an
-    LRU pool of evictable blocks and stays findable by its hash until it is
-    taken for new data (then its hash is dropped);
-  * a new prompt matches H_0, H_1, ... in order; every hit increments the
-    block's reference count and counts 16 tokens as cached; the first miss
-    ends matching for the rest of the prompt;
-  * appending a decoded token to a last block that is full takes a new block;
-    appending to a last block that is not full but shared (reference count
-    > 1) copies it to a new block first (copy-on-write) and leaves the shared
-    block to the other holders.
-Forking a table for beam search or parallel sampling increments the
-reference count of each of its blocks (same page, 考点 4: branches point at
-the same physical blocks and each holder counts once).
+It is written from the rules that "LLM 推理底层：KV Cache 显存几何、GQA/MLA
+压缩与 PagedAttention 调度" states in section "Prefix Caching 与
+Copy-on-Write" (and the vLLM interview page, 考点 4–5), one method per rule:
+
+  R1  identity of a full block: the chained hash
+          H_k = Hash(H_{k-1}, token ids of block k),   H_{-1} = 0
+      so a block's hash names its whole prefix (``chain_hashes``);
+  R2  reuse: a prompt's full blocks are looked up by H_0, H_1, ... in order;
+      the lookups stop at the first miss, every hit is shared (one more
+      reference) and its tokens count as cached (``_cached_prefix``);
+  R3  release without wiping: a block nobody references keeps its contents
+      and hash and waits in a least-recently-released order; a new block is
+      the one released longest ago, and only then does it lose its old hash
+      (``_release``, ``_claim``, ``_recycle``);
+  R4  sharing by reference: forking a sequence (beam search, parallel
+      sampling) adds one reference to each of its blocks (``fork``);
+  R5  copy-on-write: a token appended to a last block that is partly filled
+      and shared goes to a private copy of that block; the others keep the
+      original (``append_slot``); a full last block (or none) gets a new one.
 
 Readings where the pages leave a step open:
-  * every method either succeeds or raises MemoryError and leaves the
-    allocator exactly as it was. A prompt first counts its hits (matching
-    changes nothing) and the blocks it must take; if the pool, less the hit
-    blocks that sit in it, is too small, it fails before any change (a
-    half-done prompt cannot be released like a sequence: its new blocks
-    already carry hashes of KV data that will never be written).
-    ``append_slot`` takes the new block before it touches any reference
-    count;
-  * appending to an empty table takes a new block;
-  * ``append_slot`` returns the slot of the new token (block * 16 + offset)
-    and the (source, destination) pair that the caller must copy on the
-    device, or None;
-  * only prompt blocks get a hash (the reference hashes nothing on append).
+  * Hash = BLAKE2b with an 8-byte digest over ``hash_input`` (the parent as
+    8 little-endian bytes, then each token id as 4 little-endian bytes); the
+    digest read as a little-endian integer. Token ids are >= 0.
+  * Only prompt blocks get a hash; appended tokens never create one.
+  * A hash names at most one block: a block registered under a hash that an
+    older block still carries takes the hash over. (With blocks released in
+    table order and recycled oldest first, the older copies of a prefix are
+    recycled before the new blocks are registered, so this does not arise
+    through these calls; the rule keeps the map exact regardless.)
+  * Every method either succeeds or raises MemoryError and changes nothing.
+    A prompt is planned in full first (hits, then the number of blocks it
+    must recycle, counting that hit blocks waiting in the pool are no longer
+    free); a half-admitted prompt could not simply be freed, its new blocks
+    would carry hashes of K/V that is never written.
+  * Blocks start out free in id order (block 0 is recycled first).
+  * ``append_slot`` returns the new token's slot (block * 16 + offset) and
+    the (source, destination) pair the caller must copy on the device, or
+    None.
 """
 from __future__ import annotations
 
 import hashlib
-from collections import OrderedDict
-from typing import List, Optional, Tuple
+import heapq
+from typing import Dict, List, Optional, Tuple
 
 import numpy as np
 
 
-def block_hash(parent: int, tokens) -> int:
-    """H_k = BLAKE2b-64(parent as 8 LE bytes || each token as 4 LE bytes)."""
-    h = hashlib.blake2b(digest_size=8)
-    h.update(int(parent).to_bytes(8, "little", signed=False))
+# ------------------------------------------------------------------- R1
+def hash_input(parent: int, tokens) -> bytes:
+    """The bytes a block hash digests: parent (8 bytes LE), then each token
+    id (4 bytes LE)."""
+    out = bytearray(int(parent).to_bytes(8, "little"))
     for t in tokens:
-        h.update(int(t).to_bytes(4, "little", signed=False))
-    return int.from_bytes(h.digest(), "little", signed=False)
+        out += int(t).to_bytes(4, "little")
+    return bytes(out)
 
 
-class _Block:
+def block_hash(parent: int, tokens) -> int:
+    """H_k from H_{k-1} (`parent`) and the token ids of block k."""
+    return int.from_bytes(hashlib.blake2b(hash_input(parent, tokens), digest_size=8).digest(),
+                          "little")
+
+
+def chain_hashes(token_ids, block_size: int) -> List[int]:
+    """H_0, H_1, ... of every full block of a token sequence."""
+    hashes: List[int] = []
+    parent = 0
+    for k in range(len(token_ids) // block_size):
+        parent = block_hash(parent, token_ids[k * block_size:(k + 1) * block_size])
+        hashes.append(parent)
+    return hashes
+
+
+class BlockState:
+    """One physical block: holders, prefix hash (full prompt blocks only),
+    and the token ids written into its slots."""
+
     __slots__ = ("ref", "hash", "tokens")
 
     def __init__(self):
@@ -70,104 +95,124 @@ class _Block:
 class Allocator:
     def __init__(self, num_blocks: int, block_size: int = 16):
         self.block_size = block_size
-        self.blocks = [_Block() for _ in range(num_blocks)]
-        # ref == 0 blocks, least recently released first; initially in id order
-        self.pool: "OrderedDict[int, None]" = OrderedDict((i, None) for i in range(num_blocks))
-        self.by_hash: dict = {}
+        self.blocks = [BlockState() for _ in range(num_blocks)]
+        self.by_hash: Dict[int, int] = {}
+        # R3: free blocks ordered by release time. A min-heap of (stamp, id);
+        # a block's live stamp is _stamp[id] (None while held), entries with
+        # another stamp are stale and skipped.
+        self._stamp: List[Optional[int]] = list(range(num_blocks))
+        self._heap: List[Tuple[int, int]] = [(i, i) for i in range(num_blocks)]
+        self._clock = num_blocks
+        self._free = num_blocks
 
-    # ---- one physical block out of the pool (the LRU end)
-    def _take(self) -> int:
-        if not self.pool:
-            raise MemoryError("no free KV cache block")
-        bid, _ = self.pool.popitem(last=False)
+    # ---------------------------------------------------------------- R3
+    def _release(self, bid: int) -> None:
+        blk = self.blocks[bid]
+        if blk.ref <= 0:
+            raise ValueError(f"block {bid} is not held")
+        blk.ref -= 1
+        if blk.ref == 0:
+            self._stamp[bid] = self._clock
+            heapq.heappush(self._heap, (self._clock, bid))
+            self._clock += 1
+            self._free += 1
+
+    def _claim(self, bid: int) -> None:
+        """One more holder; a free block leaves the free order."""
+        if self._stamp[bid] is not None:
+            self._stamp[bid] = None
+            self._free -= 1
+        self.blocks[bid].ref += 1
+
+    def _recycle(self, tokens: List[int]) -> int:
+        """The block released longest ago, stripped of its old identity and
+        given `tokens`, with one holder."""
+        while True:
+            if not self._heap:
+                raise MemoryError("no free KV cache block")
+            stamp, bid = heapq.heappop(self._heap)
+            if self._stamp[bid] == stamp:
+                break
+        self._claim(bid)
         blk = self.blocks[bid]
         if blk.hash is not None:
             del self.by_hash[blk.hash]
             blk.hash = None
-        blk.tokens = []
-        blk.ref = 1
+        blk.tokens = list(tokens)
         return bid
 
+    # ---------------------------------------------------------------- R2
+    def _cached_prefix(self, hashes: List[int]) -> List[int]:
+        """Block ids of the leading hashes found in the cache (up to the
+        first miss)."""
+        hits: List[int] = []
+        for h in hashes:
+            bid = self.by_hash.get(h)
+            if bid is None:
+                break
+            hits.append(bid)
+        return hits
+
     def allocate_for_prompt(self, token_ids) -> Tuple[List[int], int]:
+        """Blocks for a whole prompt: the cached prefix shared, the rest
+        recycled (full ones registered under their hash). Returns (table,
+        number of cached tokens)."""
         bs = self.block_size
-        chunks = [[int(t) for t in token_ids[s:s + bs]] for s in range(0, len(token_ids), bs)]
-        # count the hits and the hit blocks that sit in the pool, changing nothing
-        n_hit, hits_in_pool, parent = 0, 0, 0
-        for chunk in chunks:
-            if len(chunk) < bs:
-                break
-            hit = self.by_hash.get(block_hash(parent, chunk))
-            if hit is None:
-                break
-            n_hit += 1
-            hits_in_pool += self.blocks[hit].ref == 0
-            parent = self.blocks[hit].hash
-        if len(chunks) - n_hit > len(self.pool) - hits_in_pool:
+        ids = [int(t) for t in token_ids]
+        hashes = chain_hashes(ids, bs)
+        hits = self._cached_prefix(hashes)
+        n_blocks = -(-len(ids) // bs)
+        waiting_hits = sum(1 for bid in hits if self.blocks[bid].ref == 0)
+        if n_blocks - len(hits) > self._free - waiting_hits:
             raise MemoryError("no free KV cache block")
-
-        table: List[int] = []
-        cached = 0
-        parent = 0
-        matching = True
-        for chunk in chunks:
-            full = len(chunk) == bs
-            if full and matching:
-                h = block_hash(parent, chunk)
-                hit = self.by_hash.get(h)
-                if hit is not None:
-                    if self.blocks[hit].ref == 0:
-                        del self.pool[hit]
-                    self.blocks[hit].ref += 1
-                    table.append(hit)
-                    cached += bs
-                    parent = h
-                    continue
-                matching = False
-            bid = self._take()
-            blk = self.blocks[bid]
-            blk.tokens = list(chunk)
-            if full:
-                h = block_hash(parent, chunk)
-                blk.hash = h
-                self.by_hash[h] = bid
-                parent = h
+        table = []
+        for bid in hits:
+            self._claim(bid)
             table.append(bid)
-        return table, cached
+        for k in range(len(hits), n_blocks):
+            bid = self._recycle(ids[k * bs:(k + 1) * bs])
+            if k < len(hashes):
+                older = self.by_hash.get(hashes[k])
+                if older is not None:           # one block per hash
+                    self.blocks[older].hash = None
+                self.blocks[bid].hash = hashes[k]
+                self.by_hash[hashes[k]] = bid
+            table.append(bid)
+        return table, len(hits) * bs
 
+    # ---------------------------------------------------------------- R5
     def append_slot(self, table: List[int], token: int) -> Tuple[int, Optional[Tuple[int, int]]]:
+        """Write one decoded token at the end of a sequence (its table is
+        updated in place). Returns (slot, copy pair or None)."""
         bs = self.block_size
-        if not table or len(self.blocks[table[-1]].tokens) == bs:
-            bid = self._take()
-            self.blocks[bid].tokens.append(int(token))
+        tail = self.blocks[table[-1]] if table else None
+        if tail is None or len(tail.tokens) == bs:          # no room: a new block
+            bid = self._recycle([int(token)])
             table.append(bid)
             return bid * bs, None
-        last = table[-1]
-        lb = self.blocks[last]
-        if lb.ref > 1:
-            bid = self._take()
-            lb.ref -= 1
-            nb = self.blocks[bid]
-            nb.tokens = list(lb.tokens) + [int(token)]
-            table[-1] = bid
-            return bid * bs + len(nb.tokens) - 1, (last, bid)
-        lb.tokens.append(int(token))
-        return last * bs + len(lb.tokens) - 1, None
+        if tail.ref == 1:                                   # private: write in place
+            tail.tokens.append(int(token))
+            return table[-1] * bs + len(tail.tokens) - 1, None
+        src = table[-1]                                     # shared: copy, then write
+        bid = self._recycle(tail.tokens + [int(token)])
+        self._release(src)
+        table[-1] = bid
+        return bid * bs + len(self.blocks[bid].tokens) - 1, (src, bid)
 
+    # ---------------------------------------------------------------- R4
     def fork(self, table: List[int]) -> List[int]:
         for bid in table:
-            self.blocks[bid].ref += 1
+            self._claim(bid)
         return list(table)
 
     def free_sequence(self, table: List[int]) -> None:
         for bid in table:
-            blk = self.blocks[bid]
-            if blk.ref <= 0:
+            if self.blocks[bid].ref <= 0:
                 raise ValueError(f"block {bid} is not held")
-            blk.ref -= 1
-            if blk.ref == 0:
-                self.pool[bid] = None
+        for bid in table:
+            self._release(bid)
 
-    # ---- introspection
+    # ------------------------------------------------------- introspection
     def ref_count(self, bid: int) -> int:
         return self.blocks[bid].ref
 
@@ -178,20 +223,20 @@ class Allocator:
         return len(self.blocks[bid].tokens)
 
     def free_order(self) -> List[int]:
-        return list(self.pool.keys())
+        """Free blocks, the next one to be recycled first."""
+        return [bid for _, bid in sorted((s, b) for b, s in enumerate(self._stamp)
+                                         if s is not None)]
 
     def num_free(self) -> int:
-        return len(self.pool)
+        return self._free
 
 
 def block_copy(k_cache: np.ndarray, v_cache: np.ndarray, pairs,
                k_scale: Optional[np.ndarray] = None, v_scale: Optional[np.ndarray] = None):
-    """Copy every (src, dst) block of the pool, all heads and all 16 slots, in
-    place: the device half of copy-on-write. Arrays are indexed by block
-    first. Destinations are distinct and no destination is a source."""
+    """The device half of copy-on-write: for every (src, dst) pair, block dst
+    of each array (indexed by block first) becomes a copy of block src, all
+    heads and all slots. Destinations are distinct and none is a source."""
+    arrays = [a for a in (k_cache, v_cache, k_scale, v_scale) if a is not None]
     for src, dst in pairs:
-        k_cache[dst] = k_cache[src]
-        v_cache[dst] = v_cache[src]
-        if k_scale is not None:
-            k_scale[dst] = k_scale[src]
-            v_scale[dst] = v_scale[src]
+        for a in arrays:
+            a[dst] = a[src]

@@ -1,15 +1,16 @@
 """Pure-Python brute force of paged decode attention (TEST INFRASTRUCTURE ONLY).
 
 A second, independent restatement of the computation in plain Python floats
-(IEEE double) and nested lists, for tiny inputs. It exists to pin the C oracle:
-the two must agree to rounding.
+(IEEE double) and lists, for tiny inputs. It exists to pin the C oracle: the
+two must agree to rounding.
 
-It follows the paged pseudocode of "【infra之路】10-PagedAttention 与 KV Cache
-管理" (qwbw.cn) §3.4: for each physical block named by the block table, take
-its K rows and score them against the query; softmax over the concatenated
-scores; walk the table again and accumulate V weighted by the probabilities.
-The score is q.k / sqrt(d) per "LLM 推理底层：KV Cache 显存几何、GQA/MLA 压缩与
-PagedAttention 调度" (blog.faulkner.fun), eq. for o_t, with the scale passed in.
+It works position by position: logical token j of a sequence is found in
+physical block BlockTable[j // bs] at offset j % bs ("LLM 推理底层：KV Cache
+显存几何、GQA/MLA 压缩与 PagedAttention 调度", section "逻辑块与物理块映射"), which
+gathers the sequence's K and V rows into plain lists; those rows then go
+through the attention definition o = softmax(q K^T * scale) V of the same
+page (section "自回归解码与 KV Cache 的物理来源", eq. for o_t), with the scale
+passed in. Query head h reads KV head h // g (GQA, contiguous groups).
 """
 from __future__ import annotations
 
@@ -21,77 +22,43 @@ def bf16_to_float(bits: int) -> float:
     return struct.unpack("<f", struct.pack("<I", (int(bits) & 0xFFFF) << 16))[0]
 
 
-def paged_decode_one(q_row, k_blocks, v_blocks, block_table, ctx, scale):
-    """One query head.
-
-    q_row: list of floats (d values).
-    k_blocks/v_blocks: callables blk -> list of block_size rows (lists of floats)
-    for the KV head this query head reads.
-    """
-    if ctx == 0:
+def attend_rows(q_row, k_rows, v_rows, scale):
+    """Softmax attention of one query over explicit K/V rows (lists of
+    floats); no rows give a zero vector."""
+    if not k_rows:
         return [0.0] * len(q_row)
-    bs = len(k_blocks(block_table[0]))
-    scores = []
-    n_blocks = (ctx + bs - 1) // bs
-    for i in range(n_blocks):
-        rows = k_blocks(block_table[i])
-        for o in range(bs):
-            if i * bs + o >= ctx:
-                break
-            scores.append(sum(a * b for a, b in zip(q_row, rows[o])) * scale)
-    m = max(scores)
-    e = [math.exp(s - m) for s in scores]
-    z = sum(e)
-    p = [x / z for x in e]
-    out = [0.0] * len(q_row)
-    j = 0
-    for i in range(n_blocks):
-        rows = v_blocks(block_table[i])
-        for o in range(bs):
-            if j >= ctx:
-                break
-            for d in range(len(out)):
-                out[d] += p[j] * rows[o][d]
-            j += 1
-    return out
+    logits = [scale * sum(a * b for a, b in zip(q_row, k)) for k in k_rows]
+    top = max(logits)
+    weights = [math.exp(x - top) for x in logits]
+    total = sum(weights)
+    return [sum(w * v[d] for w, v in zip(weights, v_rows)) / total for d in range(len(q_row))]
+
+
+def gather_rows(cache_bits, table, ctx, kv_head, block_size):
+    """Rows of logical positions 0..ctx-1 of one KV head, through the block
+    table, as lists of floats."""
+    rows = []
+    for j in range(ctx):
+        blk = table[j // block_size]
+        rows.append([bf16_to_float(x) for x in cache_bits[blk][kv_head][j % block_size]])
+    return rows
 
 
 def paged_decode(q_bits, k_cache_bits, v_cache_bits, block_tables, context_lens, n_h, n_kv,
                  scale):
     """q_bits [B][n_h][d] and caches [NB][n_kv][bs][d] of bf16 bit patterns (nested
     sequences or numpy arrays). Returns nested lists [B][n_h][d] of floats."""
-    B = len(context_lens)
     g = n_h // n_kv
+    bs = len(k_cache_bits[0][0])
     out = []
-    for b in range(B):
+    for b, ctx in enumerate(context_lens):
+        table = [int(x) for x in block_tables[b]]
         per_head = []
-        for h in range(n_h):
-            kv = h // g
-            q_row = [bf16_to_float(x) for x in q_bits[b][h]]
-
-            def kb(blk, kv=kv):
-                return [[bf16_to_float(x) for x in row] for row in k_cache_bits[blk][kv]]
-
-            def vb(blk, kv=kv):
-                return [[bf16_to_float(x) for x in row] for row in v_cache_bits[blk][kv]]
-
-            per_head.append(paged_decode_one(q_row, kb, vb, list(block_tables[b]),
-                                             int(context_lens[b]), scale))
+        for kv in range(n_kv):
+            k_rows = gather_rows(k_cache_bits, table, int(ctx), kv, bs)
+            v_rows = gather_rows(v_cache_bits, table, int(ctx), kv, bs)
+            for h in range(kv * g, (kv + 1) * g):
+                q_row = [bf16_to_float(x) for x in q_bits[b][h]]
+                per_head.append(attend_rows(q_row, k_rows, v_rows, scale))
         out.append(per_head)
-    return out
-
-
-def attend_rows(q_row, k_rows, v_rows, scale):
-    """Softmax attention of one query over an explicit list of K/V rows
-    (lists of floats): the plain definition, for the window and sink pins."""
-    if not k_rows:
-        return [0.0] * len(q_row)
-    scores = [sum(a * b for a, b in zip(q_row, k)) * scale for k in k_rows]
-    m = max(scores)
-    e = [math.exp(s - m) for s in scores]
-    z = sum(e)
-    out = [0.0] * len(q_row)
-    for w, v in zip(e, v_rows):
-        for d in range(len(out)):
-            out[d] += (w / z) * v[d]
     return out

@@ -253,9 +253,11 @@ static double cached_elem(const void *cache, const float *scales, int kv_kind, i
  * head; query head h reads KV head h / g (contiguous groups).
  * Token j of sequence b lives in physical block block_tables[b][j / bs] at
  * offset j % bs ([F] "逻辑块与物理块映射", block_idx / block_offset).
- * The two passes follow [Q] §3.4 `paged_attention`: one walk over the block
- * table for the scores, a softmax over all of them, a second walk for V.
- * The softmax subtracts the maximum score before exponentiating.
+ * The definition is written out directly: every cached token's score, the
+ * softmax of all of them (maximum subtracted before exponentiating), then
+ * the probability-weighted sum of the V rows; each row is located through
+ * the block table as it is needed ([Q] §3.4 describes the same paged
+ * computation).
  * ctx_b == 0 gives an all-zero output row.
  * out: double [B][n_h][d_h].
  * ---------------------------------------------------------------------- */

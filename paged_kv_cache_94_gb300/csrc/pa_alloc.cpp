@@ -317,6 +317,13 @@ pa_status pa_allocator_allocate_prompt(pa_allocator *a, const int32_t *token_ids
         x.ntok = len;
         if (len == bs) {
             parent = chain_hash(parent, chunk, bs);
+            // One block per hash: an older holder of this hash gives it up
+            // (blocks leave the pool oldest first, so the older copies of a
+            // prefix are recycled before this point; the check keeps the map
+            // exact regardless).
+            const int32_t old = a->find(parent);
+            if (old >= 0)
+                a->blk[old].has_hash = false;
             x.hash = parent;
             x.has_hash = true;
             a->by_hash[parent] = b;

@@ -11,7 +11,7 @@ import struct
 import numpy as np
 import pytest
 
-from oracle.allocator import Allocator, block_copy, block_hash
+from oracle.allocator import Allocator, block_copy, block_hash, hash_input
 
 BS = 16
 
@@ -43,11 +43,18 @@ def check_invariants(a: Allocator, tables):
 
 
 def test_hash_byte_layout():
-    # H_{-1} = 0; parent as 8 little-endian bytes, then each id as 4 little-endian bytes
-    import hashlib
-    toks = list(range(1000, 1016))
-    raw = struct.pack("<Q", 0) + struct.pack("<16I", *toks)
-    assert block_hash(0, toks) == int.from_bytes(hashlib.blake2b(raw, digest_size=8).digest(), "little")
+    # parent 7 as 8 little-endian bytes, then the ids 1 and 258 (0x102) as
+    # 4 little-endian bytes each, written out by hand
+    assert hash_input(7, [1, 258]).hex() == "0700000000000000" "01000000" "02010000"
+    assert hash_input(0, []).hex() == "0000000000000000"
+    assert hash_input(2**64 - 1, [2**31 - 1]).hex() == "ffffffffffffffff" "ffffff7f"
+    # the digest is an 8-byte BLAKE2b of exactly those bytes, read little-endian:
+    # it changes with every byte and never depends on anything else
+    base = block_hash(7, [1, 258])
+    assert 0 <= base < 2**64
+    assert block_hash(7, [1, 258]) == base
+    assert len({base, block_hash(7, [1, 259]), block_hash(6, [1, 258]),
+                block_hash(7, [258, 1]), block_hash(7, [1, 258, 0])}) == 5
 
 
 def test_hash_chain_identifies_prefixes():
@@ -217,3 +224,4 @@ def test_block_copy_oracle():
     block_copy(k, v, [(1, 4), (2, 5)])
     assert np.array_equal(k[4], k0[1]) and np.array_equal(v[5], v0[2])
     assert np.array_equal(k[:4], k0[:4]) and np.array_equal(v[:4], v0[:4])
+
