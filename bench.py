@@ -110,9 +110,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--num-ctas", type=int, default=0, help="force the decode split (tuning)")
-    ap.add_argument("--op", choices=["step", "block_copy", "allocator"], default="step",
+    ap.add_argument("--op", choices=["step", "block_copy", "allocator", "read_probe"],
+                    default="step",
                     help="step: the decode step (default); block_copy: pa_block_copy; "
-                         "allocator: the host block manager")
+                         "allocator: the host block manager; read_probe: plain reads of the "
+                         "decode's K/V blocks (the access pattern's ceiling)")
     ap.add_argument("--pairs", type=int, default=4096, help="block pairs per pa_block_copy")
     ap.add_argument("--no-share", action="store_true",
                     help="decode shared-prefix workloads without the shared-prefix passes")
@@ -592,6 +594,76 @@ def cpu_baseline(w, dev, seconds):
                            "seconds": round(secs, 2)}}
 
 
+# ---------------------------------------------------------------- read probe
+def probe_bytes(w) -> int:
+    """Bytes pa_kv_read_probe reads: every block of every sequence, K and V
+    (and their scales), and the block-table entries."""
+    g = w.geom
+    blocks = sum(w.num_seq_blocks(b) for b in range(w.B))
+    tile = 16 * g.d_h * kv_bits_per_elem(w) // 8
+    scales = 2 * 16 * 4 if g.kv_dtype != "bf16" else 0
+    return blocks * g.n_kv * (2 * tile + scales) + 4 * blocks
+
+
+def run_read_probe(args, rank, world, local_rank):
+    """pa_kv_read_probe over the workload's pool: the same scattered blocks as
+    its decode, read with plain 16-byte loads, one (block, head) tile at a
+    time and all heads of a block at once; L2 flushed between launches."""
+    import paged_kv_cache_94_gb300 as pa
+    from paged_kv_cache_94_gb300 import build as pa_build
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    pa_build.build()
+    w = named_workload(args.workload)
+    g = w.geom
+    kc, vc, ks, vs = pa.allocate_pool(w.num_blocks, g.n_kv, g.d_h, g.kv_dtype, dev)
+    for k, v, slots in w.history_chunks(device=dev):
+        pa.pa_cache_write(k, v, torch.from_numpy(slots).to(dev), kc, vc, ks, vs)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    cl = torch.from_numpy(w.context_lens).to(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    grid = args.num_ctas or 4 * sms
+    sink = torch.zeros(grid, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream(dev)
+    nbytes = probe_bytes(w)
+    out = {}
+    for hg in sorted({1, g.n_kv}):
+        def launch():
+            pa.pa_kv_read_probe(kc, vc, bt, cl, g.n_h, hg, grid, sink, k_scale=ks, v_scale=vs)
+        for _ in range(args.warmup):
+            flush()
+            launch()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush()
+            ev[i][0].record(stream)
+            launch()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        out[hg] = (ms, nbytes / (ms * 1e-3) / 1e9)
+    pk = peaks()
+    per_tile, per_block = out[1], out[g.n_kv]
+    return {
+        "metric": "K/V read probe: HBM GB/s of the decode's scattered reads",
+        "value": round(per_tile[1], 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_tile[0], 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": g.kv_dtype, "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.description}", "grid": grid,
+                   "l2": L2_NOTE, "reads": "16-byte loads, no arithmetic"},
+        "bytes_per_step": nbytes,
+        "per_head_tiles": {"ms": round(per_tile[0], 5), "gbs": round(per_tile[1], 1),
+                           "frac": round(per_tile[1] / pk["hbm_gbs"], 4)},
+        "all_heads_per_block": {"ms": round(per_block[0], 5), "gbs": round(per_block[1], 1),
+                                "frac": round(per_block[1] / pk["hbm_gbs"], 4)},
+        "peak": pk["hbm_gbs"], "gpu_launches": 2 * args.steps,
+    }
+
+
 # ---------------------------------------------------------------- block copy
 def block_copy_bytes(g, pairs: int) -> int:
     """Read + write of every copied block: K and V tiles (+ INT8/INT4 scales)."""
@@ -834,6 +906,8 @@ def main():
     try:
         if args.op == "block_copy":
             res = run_block_copy(args, rank, world, local_rank)
+        elif args.op == "read_probe":
+            res = run_read_probe(args, rank, world, local_rank)
         else:
             res = run_native(args, rank, world, local_rank)
         if rank == 0:

@@ -331,6 +331,29 @@ pa_status pa_sink_write(const void *k, const void *v, const int32_t *seq_rows,
                         int32_t n_sink, int32_t num_seqs, pa_geom geom, void *stream);
 
 /*
+ * pa_kv_read_probe -- read the K/V bytes a decode of this batch reads, and
+ * nothing more, to measure what the scattered access pattern allows.
+ * The pages have no counterpart: it is a measurement aid that times plain
+ * 16-byte loads of the same physical blocks, through the same block tables,
+ * as pa_decode would read (every block of ctx_b tokens of every sequence),
+ * without arithmetic.
+ *
+ *   heads_per_read  kv heads read together as one contiguous run of a block
+ *                   (1: the (block, head) tiles one by one; n_kv: all heads
+ *                   of a block); must divide n_kv
+ *   num_ctas        grid size (> 0)
+ *   sink            uint32 [num_ctas], written: an XOR of every word read
+ * Other arguments as pa_decode (INT8/INT4 pools also read their scales;
+ * bf16 pools take NULL scales). Blocks outside the pool and context lengths
+ * outside [0, max_blocks_per_seq * 16] are skipped.
+ */
+pa_status pa_kv_read_probe(const void *k_cache, const void *v_cache, const float *k_scale,
+                           const float *v_scale, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t heads_per_read, int32_t num_ctas,
+                           uint32_t *sink, pa_geom geom, void *stream);
+
+/*
  * pa_decode_noalloc -- pa_decode without a caller workspace, for callers that
  * cannot allocate device memory (for example a plugin whose host framework
  * owns all device memory and forbids allocating inside its execute callback).

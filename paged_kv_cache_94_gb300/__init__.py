@@ -46,6 +46,7 @@ EXPORTED = ["pa_cache_write", "pa_decode_workspace_size", "pa_decode_workspace_i
             "pa_plan_owner", "pa_block_copy", "pa_decode_opt", "pa_sink_write",
             "pa_decode_mq", "pa_decode_mq_ex", "pa_decode_mq_workspace_size", "pa_decode_opt_workspace_size",
             "pa_status_string", "pa_status_from_device", "pa_version", "pa_wait_selftest",
+            "pa_kv_read_probe",
             # host block manager (include/pa_alloc.h)
             "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate_prompt",
             "pa_allocator_append_slots", "pa_allocator_fork", "pa_allocator_free",
@@ -131,6 +132,8 @@ def _lib():
         lib.pa_decode_opt.argtypes = dec[:14] + [P] + dec[14:]
         lib.pa_sink_write.restype = ctypes.c_int
         lib.pa_sink_write.argtypes = [P, P, P, P, i64, P, P, i32, i32, pa_geom, P]
+        lib.pa_kv_read_probe.restype = ctypes.c_int
+        lib.pa_kv_read_probe.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, P, pa_geom, P]
         lib.pa_block_copy.restype = ctypes.c_int
         lib.pa_block_copy.argtypes = [P, P, P, P, P, i32, pa_geom, P, P]
         u64 = ctypes.c_uint64
@@ -469,6 +472,29 @@ def pa_sink_write(k: torch.Tensor, v: torch.Tensor, seq_rows: torch.Tensor,
     _check(_lib().pa_sink_write(_ptr(k), _ptr(v), _ptr(seq_rows), _ptr(positions), T,
                                 _ptr(sink_k), _ptr(sink_v), n_sink, B, g, _stream_ptr(stream)),
            "pa_sink_write")
+
+
+def pa_kv_read_probe(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                     context_lens: torch.Tensor, n_h: int, heads_per_read: int, num_ctas: int,
+                     sink: torch.Tensor, k_scale: Optional[torch.Tensor] = None,
+                     v_scale: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Read the K/V bytes a decode of this batch reads, with plain loads and
+    no arithmetic (a measurement aid); sink: uint8/int32 tensor of >= 4 *
+    num_ctas bytes, written."""
+    _need_cuda("k_cache", k_cache)
+    _need_cuda("v_cache", v_cache, k_cache.dtype)
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    _need_cuda("sink", sink)
+    if sink.numel() * sink.element_size() < 4 * num_ctas:
+        raise ValueError("sink must hold num_ctas uint32 words")
+    g = geometry(k_cache, n_h)
+    s = torch.cuda.current_stream(k_cache.device) if stream is None else stream
+    _check(_lib().pa_kv_read_probe(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                   _ptr(block_tables), block_tables.shape[1], _ptr(context_lens),
+                                   context_lens.shape[0], int(heads_per_read), int(num_ctas),
+                                   _ptr(sink), g, ctypes.c_void_p(s.cuda_stream)),
+           "pa_kv_read_probe")
 
 
 def pa_decode_default_ctas(k_cache: torch.Tensor, n_h: int, num_seqs: int) -> int:

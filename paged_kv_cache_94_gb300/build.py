@@ -40,6 +40,7 @@ SOURCES = [
     "pa_selftest.cu",
     "pa_decode_noalloc.cu",
     "pa_block_copy.cu",
+    "pa_probe.cu",
     "pa_alloc.cpp",
 ]
 

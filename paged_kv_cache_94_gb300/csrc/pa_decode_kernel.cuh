@@ -173,7 +173,7 @@ struct Bf16Policy {
 
         // ---- online softmax (columns = heads; rows = tokens gid, gid+8)
         const bool lo_ok = gid >= lo && gid < valid, hi_ok = gid + 8 >= lo && gid + 8 < valid;
-        uint32_t pb0[NT], pb1[NT];
+        uint32_t pb0[NT], pb1[NT], pl0[NT], pl1[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             float sc[4];
@@ -225,8 +225,19 @@ struct Bf16Policy {
 #pragma unroll
             for (int e = 0; e < 2; ++e)
                 st.l[nt][e] += sc[e] + sc[e + 2];
-            pb0[nt] = movmatrix_trans(pack_bf16x2(sc[0], sc[1]));
-            pb1[nt] = movmatrix_trans(pack_bf16x2(sc[2], sc[3]));
+            // The weights go to the tensor cores as two bf16 parts, P = hi + lo
+            // (hi = bf16(P), lo = bf16(P - hi)): 16 significant bits instead of
+            // 8, so the weighted sum stays accurate when V rows differ in
+            // magnitude by orders and their terms cancel.
+            const uint32_t h0 = pack_bf16x2(sc[0], sc[1]), h1 = pack_bf16x2(sc[2], sc[3]);
+            const uint32_t r0 = pack_bf16x2(sc[0] - __uint_as_float(h0 << 16),
+                                            sc[1] - __uint_as_float(h0 & 0xffff0000u));
+            const uint32_t r1 = pack_bf16x2(sc[2] - __uint_as_float(h1 << 16),
+                                            sc[3] - __uint_as_float(h1 & 0xffff0000u));
+            pb0[nt] = movmatrix_trans(h0);
+            pb1[nt] = movmatrix_trans(h1);
+            pl0[nt] = movmatrix_trans(r0);
+            pl1[nt] = movmatrix_trans(r1);
         }
 
         // ---- O^T += V^T P^T. Rows of V outside [lo, valid) may hold anything
@@ -237,8 +248,10 @@ struct Bf16Policy {
                 uint32_t a0, a1, a2, a3;
                 ldmatrix_x4_trans(v_addr(vt, mt, mi, rr), a0, a1, a2, a3);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt) {
                     mma_bf16_16816(st.acc[nt][mt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+                    mma_bf16_16816(st.acc[nt][mt], a0, a1, a2, a3, pl0[nt], pl1[nt]);
+                }
             }
         } else {
             const int t0 = 2 * t4;
@@ -254,8 +267,10 @@ struct Bf16Policy {
                 a2 &= mhi;
                 a3 &= mhi;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt) {
                     mma_bf16_16816(st.acc[nt][mt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+                    mma_bf16_16816(st.acc[nt][mt], a0, a1, a2, a3, pl0[nt], pl1[nt]);
+                }
             }
         }
     }

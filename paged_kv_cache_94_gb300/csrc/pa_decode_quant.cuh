@@ -7,12 +7,12 @@
 // Every code is exact in fp16. A code c becomes fp16 by writing its
 // offset-binary form (c + 128, or c + 8) into the mantissa of 1024
 // (exponent bits 0x64): that half is B + c with B = 1152 (INT8) or 1032
-// (INT4). The bias is not subtracted per element: sum_d (B + c_d) q_d =
-// sum_d c_d q_d + B * sum_d q_d, so one correction per score with the
-// per-head sum of the fp16 query values removes it, and likewise
-// B * sum_tok w_tok per head for the weighted V sum (every product of two
-// fp16 values is exact in the fp32 accumulators). Both contractions run as
-// mma.sync m16n8k16 with fp16 inputs and fp32 accumulation:
+// (INT4); one fp16x2 subtraction of B (a fused multiply-add for the INT4
+// codes that land as 1152 + 16 c) then leaves exactly c. The contractions
+// thus see the codes themselves: no bias term is carried through the fp32
+// accumulators, whose rounding stays relative to the result. Both
+// contractions run as mma.sync m16n8k16 with fp16 inputs and fp32
+// accumulation (every product of two fp16 values is exact):
 //   S^T[16 tok][8 heads] = Kcode[16 tok][D] . Q'^T[D][8 heads]
 //       (tokens on M; the k index is permuted so each thread's A fragments
 //        for all k-steps come from one 16-byte (or 8-byte) load of a row)
@@ -23,9 +23,8 @@
 //        from one load of each of its four token rows)
 // INT4 codes take one AND-XOR each (no shifts into place): the nibble at
 // bits 0-3 of a 16-bit half becomes 1024 + (c + 8) = 1032 + c, the nibble at
-// bits 4-7 becomes 1024 + 16 (c + 8) = 1152 + 16 c. The two kinds feed
-// separate accumulators (Q.K: even and odd k-steps; V: even and odd d rows),
-// each with its own bias, and the x16 ones are divided by 16 at the end.
+// bits 4-7 becomes 1024 + 16 (c + 8) = 1152 + 16 c; the first loses 1032,
+// the second is scaled by 1/16 and loses 72, in one fp16x2 operation each.
 // Q' = q * 2^-e with e >= 0 chosen per (sequence, kv head) so that
 // max|Q'| < 2^15: the bf16 -> fp16 conversion is then exact for every
 // normal value. W = p * v_scale[tok] / s_base, where s_base is a running
@@ -38,16 +37,6 @@
 #include "pa_decode.cuh"
 
 namespace pa {
-
-// Two int8 codes (bytes of `w` already XORed with 0x80, picked by SEL) ->
-// fp16x2 {1152 + code0, 1152 + code1}: the codes with a constant bias, which
-// the policy subtracts from the contraction's result instead of from every
-// element.
-template <uint32_t SEL>
-__device__ __forceinline__ uint32_t bytes_to_h2(uint32_t w)
-{
-    return __byte_perm(w, 0x64646464u, SEL);
-}
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 {
@@ -103,6 +92,39 @@ __device__ __forceinline__ uint32_t nib_hi(uint32_t w)
     return (w & 0x00F000F0u) ^ 0x64806480u;
 }
 
+// fp16x2 {B + c0, B + c1} -> {c0, c1}, exact (every value involved is an
+// fp16 integer below 2^11).
+__device__ __forceinline__ uint32_t h2_sub(uint32_t x, uint32_t b2)
+{
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(b2));
+    return r;
+}
+
+// fp16x2 {1152 + 16 c0, 1152 + 16 c1} -> {c0, c1}: x / 16 - 72, exact.
+__device__ __forceinline__ uint32_t h2_hi_code(uint32_t x)
+{
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0x2C002C00u), "r"(0xD480D480u));
+    return r;
+}
+
+constexpr uint32_t kH2_1152 = 0x64806480u; // fp16x2 {1152, 1152}
+constexpr uint32_t kH2_1032 = 0x64086408u; // fp16x2 {1032, 1032}
+
+// Exact fp16x2 codes: two INT8 codes (bytes of `w` XORed with 0x80, picked
+// by SEL, first land as {1152 + c0, 1152 + c1}); two low INT4 nibbles (bits
+// 0-3, 16-19); two high ones (4-7, 20-23).
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t code8_h2(uint32_t w)
+{
+    return h2_sub(__byte_perm(w, 0x64646464u, SEL), kH2_1152);
+}
+
+__device__ __forceinline__ uint32_t code4_lo_h2(uint32_t w) { return h2_sub(nib_lo(w), kH2_1032); }
+
+__device__ __forceinline__ uint32_t code4_hi_h2(uint32_t w) { return h2_hi_code(nib_hi(w)); }
+
 // fp32 values of the two halves of an fp16x2.
 __device__ __forceinline__ void h2_to_f2(uint32_t x, float &lo, float &hi)
 {
@@ -142,8 +164,6 @@ struct QuantMmaPolicy {
     static constexpr int QBYTES = 0;
     static constexpr uint32_t TX = STAGE + EXTRA;
     static constexpr float kScaleRatio = 64.f;     // V-scale base moves beyond this
-    static constexpr float kBias = BITS == 8 ? 1152.f : 1032.f; // fp16 value of code 0
-    static constexpr float kBiasHi = 1152.f;       // INT4, x16 nibbles: 1152 + 16 c
     using Layout = SmemLayout<D, GQ, NW, S, STAGE, EXTRA, QBYTES>;
 
     struct State {
@@ -153,10 +173,6 @@ struct QuantMmaPolicy {
         float acc[NT][KS][4];   // O^T accumulators: rows permuted d, cols heads
         float sbase;            // V-scale base of acc (0 until a nonzero scale is seen)
         float sinv;             // 1 / sbase (0 while sbase is 0)
-        float qsum[NT][2];      // sum_d of the fp16 Q' values of head 2t4 + e (INT4: even k-steps)
-        float qsum1[NT][2];     // INT4: the same over the odd k-steps
-        float wacc[NT][4];      // sum of the fp16 weights per head: the PV accumulator
-                                // of an all-ones V tile (every row holds the sum)
     };
 
     // Tiles of 1-2 KiB move faster as 16-byte cp.async copies spread over the
@@ -279,7 +295,6 @@ struct QuantMmaPolicy {
 
     __device__ static void finish_q(State &st)
     {
-        const int lane = threadIdx.x & 31, t4 = lane & 3;
         float qv[NT][KS][4]; // per k-step: register 0 (lo, hi), register 1 (lo, hi)
         float mx = 0.f;
 #pragma unroll
@@ -329,33 +344,12 @@ struct QuantMmaPolicy {
         st.qexp = __uint_as_float((uint32_t)(127 + e) << 23);
         const float down = __uint_as_float((uint32_t)(127 - e) << 23);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            // sums of this thread's fp16 values of head nt*8 + gid: even and
-            // odd k-steps (INT8 adds both)
-            float part[2] = {0.f, 0.f};
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
                 st.qf[nt][kk][0] = pack_f16x2(qv[nt][kk][0] * down, qv[nt][kk][1] * down);
                 st.qf[nt][kk][1] = pack_f16x2(qv[nt][kk][2] * down, qv[nt][kk][3] * down);
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    float lo, hi;
-                    h2_to_f2(st.qf[nt][kk][r], lo, hi);
-                    part[BITS == 4 ? (kk & 1) : 0] += lo + hi;
-                }
             }
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                part[i] += __shfl_xor_sync(0xffffffffu, part[i], 1);
-                part[i] += __shfl_xor_sync(0xffffffffu, part[i], 2);
-            }
-            // score columns are heads 2t4 + e: their sums sit in lanes 4 (2t4 + e)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                st.qsum[nt][e] = __shfl_sync(0xffffffffu, part[0], 4 * (2 * t4 + e));
-                st.qsum1[nt][e] = __shfl_sync(0xffffffffu, part[1], 4 * (2 * t4 + e));
-            }
-        }
     }
 
     __device__ static void reset(State &st)
@@ -376,11 +370,6 @@ struct QuantMmaPolicy {
                     st.acc[nt][mt][e] = 0.f;
         st.sbase = 0.f;
         st.sinv = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                st.wacc[nt][e] = 0.f;
     }
 
     // One item of BPI 16-token blocks: block j's K codes at kt + j*TILE, its V
@@ -393,7 +382,7 @@ struct QuantMmaPolicy {
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
 
-        // ---- S^T = Kcode . Q'^T per block (INT4: even and odd k-steps apart)
+        // ---- S^T = Kcode . Q'^T per block (INT4: even and odd k-steps in two chains)
         float s0[BPI][NT][4], s1[BPI][NT][4];
 #pragma unroll
         for (int j = 0; j < BPI; ++j)
@@ -405,7 +394,7 @@ struct QuantMmaPolicy {
         auto kstep = [&](int j, int kk, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                if (BITS == 4 && (kk & 1)) // INT4: the x16 k-steps; INT8: one chain per block
+                if (BITS == 4 && (kk & 1)) // INT4: two chains per block; INT8: one
                     mma_f16_16816(s1[j][nt], a0, a1, a2, a3, st.qf[nt][kk][0], st.qf[nt][kk][1]);
                 else
                     mma_f16_16816(s0[j][nt], a0, a1, a2, a3, st.qf[nt][kk][0], st.qf[nt][kk][1]);
@@ -426,8 +415,8 @@ struct QuantMmaPolicy {
                                             kb.z ^ 0x80808080u, kb.w ^ 0x80808080u};
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        kstep(j, 4 * g4 + i, bytes_to_h2<0x4140>(wa[i]), bytes_to_h2<0x4140>(wb[i]),
-                              bytes_to_h2<0x4342>(wa[i]), bytes_to_h2<0x4342>(wb[i]));
+                        kstep(j, 4 * g4 + i, code8_h2<0x4140>(wa[i]), code8_h2<0x4140>(wb[i]),
+                              code8_h2<0x4342>(wa[i]), code8_h2<0x4342>(wb[i]));
                 }
         } else {
             // rows gid, gid+8: the thread's D/8 contiguous bytes (D/4 codes), unswizzled
@@ -448,10 +437,12 @@ struct QuantMmaPolicy {
                 }
 #pragma unroll
                 for (int wi = 0; wi < KS / 2; ++wi) {
-                    // nibbles 0, 4 and (after >> 8) 2, 6: even k-step; 1, 5 and 3, 7 (x16): odd
+                    // nibbles 0, 4 and (after >> 8) 2, 6: even k-step; 1, 5 and 3, 7: odd
                     const uint32_t xa = wa[wi], xb = wb[wi], ya = xa >> 8, yb = xb >> 8;
-                    kstep(j, 2 * wi, nib_lo(xa), nib_lo(xb), nib_lo(ya), nib_lo(yb));
-                    kstep(j, 2 * wi + 1, nib_hi(xa), nib_hi(xb), nib_hi(ya), nib_hi(yb));
+                    kstep(j, 2 * wi, code4_lo_h2(xa), code4_lo_h2(xb), code4_lo_h2(ya),
+                          code4_lo_h2(yb));
+                    kstep(j, 2 * wi + 1, code4_hi_h2(xa), code4_hi_h2(xb), code4_hi_h2(ya),
+                          code4_hi_h2(yb));
                 }
             }
         }
@@ -474,12 +465,7 @@ struct QuantMmaPolicy {
                 // S^T element c: token row gid (c < 2) or gid+8, head column 2t4 + (c & 1)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    float sb;
-                    if constexpr (BITS == 8)
-                        sb = fmaf(-kBias, st.qsum[nt][c & 1], s0[j][nt][c]);
-                    else
-                        sb = fmaf(fmaf(-kBiasHi, st.qsum1[nt][c & 1], s1[j][nt][c]), 0.0625f,
-                                  fmaf(-kBias, st.qsum[nt][c & 1], s0[j][nt][c]));
+                    const float sb = BITS == 8 ? s0[j][nt][c] : s0[j][nt][c] + s1[j][nt][c];
                     const float sc = sb * ((c & 2) ? f_hi : f_lo);
                     pr[j][nt][c] = ((c & 2) ? hi_ok[j] : lo_ok[j]) ? sc : -INFINITY;
                 }
@@ -508,8 +494,6 @@ struct QuantMmaPolicy {
                         const float alpha = fast_exp2(st.m[nt][e] - mx);
                         st.m[nt][e] = mx;
                         st.l[nt][e] *= alpha;
-                        st.wacc[nt][e] *= alpha;
-                        st.wacc[nt][e + 2] *= alpha;
 #pragma unroll
                         for (int mt = 0; mt < KS; ++mt) {
                             st.acc[nt][mt][e] *= alpha;
@@ -550,9 +534,6 @@ struct QuantMmaPolicy {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    st.wacc[nt][e] *= f;
-#pragma unroll
                 for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
@@ -587,11 +568,6 @@ struct QuantMmaPolicy {
                 for (int nt = 0; nt < NT; ++nt)
                     mma_f16_16816(st.acc[nt][mt], a0, a1, a2, a3, pb0[j][nt], pb1[j][nt]);
             };
-            // the weights' sums (for the codes' bias): an all-ones V tile
-            constexpr uint32_t kOnes = 0x3C003C00u; // fp16x2 {1, 1}
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                mma_f16_16816(st.wacc[nt], kOnes, kOnes, kOnes, kOnes, pb0[j][nt], pb1[j][nt]);
             if constexpr (BITS == 8) {
                 constexpr int WPR = D / 32; // 32-bit words per thread per row
                 uint32_t ra[WPR], rb[WPR], rc[WPR], rd[WPR];
@@ -624,10 +600,10 @@ struct QuantMmaPolicy {
                     const uint32_t ab_hi = __byte_perm(A, B, 0x7362);
                     const uint32_t ce_lo = __byte_perm(C, E, 0x5140);
                     const uint32_t ce_hi = __byte_perm(C, E, 0x7362);
-                    pv(2 * i, bytes_to_h2<0x4140>(ab_lo), bytes_to_h2<0x4342>(ab_lo),
-                       bytes_to_h2<0x4140>(ce_lo), bytes_to_h2<0x4342>(ce_lo));
-                    pv(2 * i + 1, bytes_to_h2<0x4140>(ab_hi), bytes_to_h2<0x4342>(ab_hi),
-                       bytes_to_h2<0x4140>(ce_hi), bytes_to_h2<0x4342>(ce_hi));
+                    pv(2 * i, code8_h2<0x4140>(ab_lo), code8_h2<0x4342>(ab_lo),
+                       code8_h2<0x4140>(ce_lo), code8_h2<0x4342>(ce_lo));
+                    pv(2 * i + 1, code8_h2<0x4140>(ab_hi), code8_h2<0x4342>(ab_hi),
+                       code8_h2<0x4140>(ce_hi), code8_h2<0x4342>(ce_hi));
                 }
             } else {
                 // CW/2 bytes per row; byte k of word i holds d values 8i+2k (low
@@ -655,10 +631,11 @@ struct QuantMmaPolicy {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         // bytes {A_k, A_k, B_k, B_k}: nibble pairs (row 2t, row 2t+1) of
-                        // d (low nibbles) and d + 1 (high nibbles, x16: A rows gid + 8)
+                        // d (low nibbles) and d + 1 (high nibbles: A rows gid + 8)
                         const uint32_t sel = k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12);
                         const uint32_t Y = __byte_perm(A, B, sel), Z = __byte_perm(C, E, sel);
-                        pv(4 * i + k, nib_lo(Y), nib_hi(Y), nib_lo(Z), nib_hi(Z));
+                        pv(4 * i + k, code4_lo_h2(Y), code4_hi_h2(Y), code4_lo_h2(Z),
+                           code4_hi_h2(Z));
                     }
                 }
             }
@@ -686,24 +663,18 @@ struct QuantMmaPolicy {
                 }
             }
         // acc[nt][mt][e]: row gid (e < 2) or gid+8 (e >= 2) of row tile mt is
-        // d = CW*gid + 2*mt + (e >> 1); column 2t4 + (e & 1) is the head. The
-        // codes' bias contributed kBias * (sum of the head's weights) to every d
-        // (INT4: kBiasHi to the odd d, whose codes entered x16).
+        // d = CW*gid + 2*mt + (e >> 1); column 2t4 + (e & 1) is the head.
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
-                const float ws = st.wacc[nt][c]; // the head's whole weight sum
-                const float bias = kBias * ws;
-                const float bias1 = (BITS == 8 ? kBias : kBiasHi) * ws;
-                const float sb1 = BITS == 8 ? st.sbase : st.sbase * 0.0625f;
                 const int h = nt * 8 + 2 * t4 + c;
                 if (h < GQ) {
                     float *mb = merge + (warp * GQ + h) * (D + 2) + 2 + CW * gid;
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
-                        mb[2 * mt] = (st.acc[nt][mt][c] - bias) * st.sbase;
-                        mb[2 * mt + 1] = (st.acc[nt][mt][c + 2] - bias1) * sb1;
+                        mb[2 * mt] = st.acc[nt][mt][c] * st.sbase;
+                        mb[2 * mt + 1] = st.acc[nt][mt][c + 2] * st.sbase;
                     }
                 }
             }

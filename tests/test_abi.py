@@ -189,3 +189,16 @@ def test_mq_workspace_size_per_pool_type(lib, kv_dtype):
         g = _geom(n_h=n_h, n_kv=8, kv_dtype=kv_dtype)
         size = lib.pa_decode_mq_workspace_size(g, 4, n_q, 304)
         assert (size > 0) == ok, (n_h, n_q, kv_dtype)
+
+
+def test_read_probe_argument_checks(lib):
+    fake = ctypes.c_void_p(256)
+    g = _geom()
+    args = lambda **o: [fake, fake, None, None, fake, 16, fake, o.get("B", 4),
+                        o.get("hg", 1), o.get("grid", 8), fake, o.get("g", g), None]
+    assert lib.pa_kv_read_probe(*args(B=0)) == 0          # nothing to read
+    assert lib.pa_kv_read_probe(*args(hg=3)) == -2        # must divide n_kv
+    assert lib.pa_kv_read_probe(*args(hg=0)) == -2
+    assert lib.pa_kv_read_probe(*args(grid=0)) == -2
+    assert lib.pa_kv_read_probe(*args(g=_geom(kv_dtype=1))) == -2   # INT8 pools read scales
+    assert lib.pa_kv_read_probe(*args(g=_geom(d_h=96))) == -2
