@@ -31,8 +31,6 @@ SOURCES = [
     "pa_decode_int8_d64.cu",
     "pa_decode_int4_d128.cu",
     "pa_decode_int4_d64.cu",
-    "pa_decode_hg_int8.cu",
-    "pa_decode_hg_int4.cu",
     "pa_decode_bf16_mq.cu",
     "pa_decode_int8_mq_d128.cu",
     "pa_decode_int8_mq_d64.cu",

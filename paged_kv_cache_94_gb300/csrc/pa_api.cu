@@ -107,41 +107,34 @@ struct AttrEntry {
 AttrEntry g_attr[kOccCache];
 int g_attr_n = 0;
 
-pa_status ctas_per_sm_fn(const void *fn, int threads, size_t smem, int &n);
-
 pa_status ctas_per_sm(const DecodeKernel *kd, size_t smem, int &n)
-{
-    return ctas_per_sm_fn(kd->fn, kd->threads, smem, n);
-}
-
-pa_status ctas_per_sm_fn(const void *fn, int threads, size_t smem, int &n)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return PA_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
     for (int i = 0; i < g_occ_n; ++i)
-        if (g_occ[i].fn == fn && g_occ[i].dev == dev && g_occ[i].smem == smem) {
+        if (g_occ[i].fn == kd->fn && g_occ[i].dev == dev && g_occ[i].smem == smem) {
             n = g_occ[i].per_sm;
             return n > 0 ? PA_OK : PA_ERR_UNSUPPORTED;
         }
     bool attr_set = false;
     for (int i = 0; i < g_attr_n; ++i)
-        attr_set |= (g_attr[i].fn == fn && g_attr[i].dev == dev);
+        attr_set |= (g_attr[i].fn == kd->fn && g_attr[i].dev == dev);
     if (!attr_set) {
         int max_optin = 0;
         if (cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
                 cudaSuccess ||
-            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin) !=
+            cudaFuncSetAttribute(kd->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin) !=
                 cudaSuccess)
             return PA_ERR_CUDA;
         if (g_attr_n < kOccCache)
-            g_attr[g_attr_n++] = {fn, dev};
+            g_attr[g_attr_n++] = {kd->fn, dev};
     }
     n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kd->fn, kd->threads, smem) != cudaSuccess)
         return PA_ERR_CUDA;
-    g_occ[g_occ_n < kOccCache ? g_occ_n++ : (int)(smem % kOccCache)] = {fn, dev, smem, n};
+    g_occ[g_occ_n < kOccCache ? g_occ_n++ : (int)(smem % kOccCache)] = {kd->fn, dev, smem, n};
     if (n <= 0)
         return PA_ERR_UNSUPPORTED; // does not fit on an SM
     return PA_OK;
@@ -165,12 +158,10 @@ pa_status default_ctas(const pa_geom &g, int num_seqs, int &grid, int nq = 1)
 
 size_t counters_bytes(int64_t units) { return (size_t)((units * 4 + 255) / 256 * 256); }
 
-// Decode workspace: a counter per unit, then (grid + units) partial records
-// of hg * g * nq query rows; a unit is (sequence, group of hg kv heads).
-size_t workspace_bytes_for(const pa_geom &g, int num_seqs, int grid, int nq = 1, int hg = 1)
+size_t workspace_bytes_for(const pa_geom &g, int num_seqs, int grid, int nq = 1)
 {
-    const int64_t units = (int64_t)num_seqs * (g.n_kv / hg);
-    const int64_t rec = (int64_t)hg * group_of(g) * nq * (g.d_h + 2) * 4;
+    const int64_t units = (int64_t)num_seqs * g.n_kv;
+    const int64_t rec = (int64_t)group_of(g) * nq * (g.d_h + 2) * 4;
     return counters_bytes(units) + (size_t)((grid + units) * rec);
 }
 
@@ -201,137 +192,18 @@ pa_status share_fits(const DecodeKernel *kp, int num_seqs, size_t &smem, int &pe
     return ctas_per_sm(kp, smem, per);
 }
 
-ShareLayout share_layout(const pa_geom &g, int num_seqs, int grid, int hg = 1)
+ShareLayout share_layout(const pa_geom &g, int num_seqs, int grid)
 {
     ShareLayout L;
-    const size_t units2 = 2 * (size_t)num_seqs * (g.n_kv / hg);
+    const size_t units2 = 2 * (size_t)num_seqs * g.n_kv;
     L.zero_end = round256(4 * units2);
     L.records = L.zero_end;
-    const size_t rec =
-        (size_t)hg * group_of(g) * pa::kShareMembers(group_of(g)) * (g.d_h + 2) * 4;
+    const size_t rec = (size_t)group_of(g) * pa::kShareMembers(group_of(g)) * (g.d_h + 2) * 4;
     L.skip = round256(L.records + (grid + units2) * rec);
     L.groups = L.skip + round256(4 * (size_t)num_seqs);
     L.pre = L.groups + round256(12 * (size_t)num_seqs);
     L.end = L.pre + (size_t)num_seqs * g.n_h * (g.d_h + 2) * 4;
     return L;
-}
-
-// ------------------------------------------------------------ launch plan
-// Which kernel a decode runs, its grid, shared memory and workspace. INT8
-// and INT4 pools run the head-group kernel (one item = a block of HG kv
-// heads, HG the largest power of two <= 8 dividing n_kv) for single-token
-// decodes, plain or shared-prefix, when its ring of at least two stages fits;
-// everything else runs decode_kernel.
-struct Plan {
-    bool share = false;
-    const DecodeKernel *kd = nullptr; // decode_kernel (plain, multi-query or shared-prefix)
-    const pa::HgKernel *hk = nullptr; // the head-group kernel
-    int grid = 0;
-    size_t smem = 0;
-    int hg = 1, stages = 0, stage_bytes = 0;
-    size_t ws_bytes = 0;
-    ShareLayout SL{};
-};
-
-int max_smem_optin()
-{
-    int dev = -1, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-        return 0;
-    return v;
-}
-
-pa_status make_plan(const pa_geom &g, int num_seqs, int nq, bool want_share, int num_ctas, Plan &pl)
-{
-    pl = Plan{};
-    int dev, sms;
-    pa_status st = current_device(dev, sms);
-    if (st != PA_OK)
-        return st;
-    const int gq = group_of(g);
-    bool share = want_share && nq == 1 && gq <= 8;
-    const bool quant = g.kv_dtype != PA_KV_BF16;
-    if (quant && nq == 1) {
-        const int optin = max_smem_optin();
-        if (optin <= 0)
-            return PA_ERR_CUDA;
-        // the shared-prefix launch if asked for and its arrays fit, else plain
-        for (int attempt = share ? 0 : 1; attempt < 2; ++attempt) {
-            const bool sh = attempt == 0;
-            const pa::HgKernel *hk = pa::find_hg_kernel(g.kv_dtype, g.d_h, gq, sh);
-            if (!hk)
-                continue;
-            // head group: the largest power of two <= 8 dividing both n_kv
-            // and the consumer warp count
-            int hg = g.n_kv & -g.n_kv;
-            hg = hg < (hk->consumers & -hk->consumers) ? hg : (hk->consumers & -hk->consumers);
-            hg = hg < 8 ? hg : 8;
-            const int stage = pa::hg_stage_bytes(hk->tile, hg);
-            const int seqs = sh ? 2 * num_seqs : num_seqs;
-            // the ring's stages are a multiple of the consumer warp sets
-            // (consumers / hg), so each stage is only ever read by one set
-            const int sets = hk->consumers / hg;
-            int stages = sets > 8 ? sets : 8;
-            while (stages >= 2 && (stages % sets != 0 ||
-                                   hk->smem_bytes(stages, stage, hg, seqs) > (size_t)optin))
-                --stages;
-            if (stages < 2)
-                continue;
-            const size_t smem = hk->smem_bytes(stages, stage, hg, seqs);
-            int per = 0;
-            if ((st = ctas_per_sm_fn(hk->fn, hk->threads, smem, per)) != PA_OK) {
-                if (st != PA_ERR_UNSUPPORTED)
-                    return st;
-                continue;
-            }
-            pl.share = sh;
-            pl.hk = hk;
-            pl.hg = hg;
-            pl.stages = stages;
-            pl.stage_bytes = stage;
-            pl.smem = smem;
-            pl.grid = num_ctas > 0 ? num_ctas : sms * per;
-            if (sh) {
-                pl.SL = share_layout(g, num_seqs, pl.grid, hg);
-                pl.ws_bytes = pl.SL.end;
-            } else {
-                pl.ws_bytes = workspace_bytes_for(g, num_seqs, pl.grid, 1, hg);
-            }
-            return PA_OK;
-        }
-    }
-    const DecodeKernel *kd = kernel_for(g, nq);
-    if (!kd)
-        return PA_ERR_UNSUPPORTED;
-    int per = 0;
-    pl.smem = kd->smem_bytes(num_seqs);
-    if ((st = ctas_per_sm(kd, pl.smem, per)) != PA_OK)
-        return st;
-    pl.kd = kd;
-    pl.grid = num_ctas > 0 ? num_ctas : sms * per;
-    if (share) {
-        const DecodeKernel *kp = pa::find_prefix_kernel(g.kv_dtype, g.d_h, gq);
-        if (!kp)
-            return PA_ERR_UNSUPPORTED;
-        size_t smem_sh = 0;
-        int per_sh = 0;
-        st = share_fits(kp, num_seqs, smem_sh, per_sh);
-        if (st == PA_OK) {
-            pl.share = true;
-            pl.kd = kp;
-            pl.smem = smem_sh;
-            pl.grid = num_ctas > 0 ? num_ctas : sms * per_sh;
-            pl.SL = share_layout(g, num_seqs, pl.grid);
-            pl.ws_bytes = pl.SL.end;
-            return PA_OK;
-        }
-        if (st != PA_ERR_UNSUPPORTED)
-            return st;
-        // the batch's prefix arrays do not fit: decode without sharing
-    }
-    pl.ws_bytes = workspace_bytes_for(g, num_seqs, pl.grid, nq);
-    return PA_OK;
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -359,7 +231,7 @@ EncodeTiledFn encode_fn()
 // tile of at most 128 bytes per row. bf16 and INT8 tiles are swizzled so that
 // ldmatrix/ld.shared of 8 consecutive rows hit distinct banks; INT4 rows (64
 // or 32 bytes) are read as whole contiguous runs and stay unswizzled.
-pa_status encode_pool_uncached(CUtensorMap &m, const void *base, const pa_geom &g, int rows)
+pa_status encode_pool_uncached(CUtensorMap &m, const void *base, const pa_geom &g)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -370,7 +242,7 @@ pa_status encode_pool_uncached(CUtensorMap &m, const void *base, const pa_geom &
     const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)(g.num_blocks * g.n_kv * 16)};
     const cuuint64_t strides[1] = {(cuuint64_t)row_elems * esz};
     const cuuint32_t box_x = (cuuint32_t)((row_elems * esz > 128) ? 128 / esz : row_elems);
-    const cuuint32_t box[2] = {box_x, (cuuint32_t)rows};
+    const cuuint32_t box[2] = {box_x, 16};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapSwizzle sw = i4                     ? CU_TENSOR_MAP_SWIZZLE_NONE
                                   : (box_x * esz == 128) ? CU_TENSOR_MAP_SWIZZLE_128B
@@ -388,33 +260,32 @@ pa_status encode_pool_uncached(CUtensorMap &m, const void *base, const pa_geom &
 struct MapEntry {
     const void *base;
     int64_t num_blocks;
-    int32_t n_kv, d_h, kv_dtype, rows;
+    int32_t n_kv, d_h, kv_dtype;
     CUtensorMap map;
 };
 constexpr int kMapCache = 64;
 MapEntry g_maps[kMapCache];
 int g_maps_n = 0, g_maps_next = 0;
 
-// rows: box height (16: one (block, head) tile; 16 * hg: hg adjacent heads).
-pa_status encode_pool(CUtensorMap &m, const void *base, const pa_geom &g, int rows = 16)
+pa_status encode_pool(CUtensorMap &m, const void *base, const pa_geom &g)
 {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         for (int i = 0; i < g_maps_n; ++i) {
             const MapEntry &e = g_maps[i];
             if (e.base == base && e.num_blocks == g.num_blocks && e.n_kv == g.n_kv &&
-                e.d_h == g.d_h && e.kv_dtype == g.kv_dtype && e.rows == rows) {
+                e.d_h == g.d_h && e.kv_dtype == g.kv_dtype) {
                 m = e.map;
                 return PA_OK;
             }
         }
     }
-    const pa_status st = encode_pool_uncached(m, base, g, rows);
+    const pa_status st = encode_pool_uncached(m, base, g);
     if (st != PA_OK)
         return st;
     std::lock_guard<std::mutex> lk(g_mu);
     MapEntry &e = g_maps[g_maps_next];
-    e = {base, g.num_blocks, g.n_kv, g.d_h, g.kv_dtype, rows, m};
+    e = {base, g.num_blocks, g.n_kv, g.d_h, g.kv_dtype, m};
     g_maps_next = (g_maps_next + 1) % kMapCache;
     if (g_maps_n < kMapCache)
         ++g_maps_n;
@@ -464,18 +335,34 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
         !aligned(workspace, 256) || (i8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16))))
         return PA_ERR_ALIGNMENT;
 
-    Plan pl;
-    if ((st = make_plan(g, num_seqs, nq, share, num_ctas, pl)) != PA_OK)
+    const DecodeKernel *kd = kernel_for(g, nq);
+    if (!kd)
+        return PA_ERR_UNSUPPORTED;
+    int dev, sms, per;
+    if ((st = current_device(dev, sms)) != PA_OK)
         return st;
-    share = pl.share;
-    const int grid = pl.grid;
-    const ShareLayout &SL = pl.SL;
-    if (workspace_bytes < pl.ws_bytes)
+    const size_t smem = kd->smem_bytes(num_seqs);
+    if ((st = ctas_per_sm(kd, smem, per)) != PA_OK)
+        return st;
+    int grid = num_ctas > 0 ? num_ctas : sms * per;
+    const DecodeKernel *kp = share ? pa::find_prefix_kernel(g.kv_dtype, g.d_h, group_of(g)) : nullptr;
+    if (share && !kp)
+        return PA_ERR_UNSUPPORTED;
+    size_t smem_sh = 0;
+    int per_sh = 0;
+    if (share && (st = share_fits(kp, num_seqs, smem_sh, per_sh)) != PA_OK) {
+        if (st != PA_ERR_UNSUPPORTED)
+            return st;
+        share = false; // the batch's prefix arrays do not fit: decode without sharing
+    }
+    if (share) // default: one wave of resident CTAs
+        grid = num_ctas > 0 ? num_ctas : sms * per_sh;
+    const ShareLayout SL = share ? share_layout(g, num_seqs, grid) : ShareLayout{};
+    if (workspace_bytes < (share ? SL.end : workspace_bytes_for(g, num_seqs, grid, nq)))
         return PA_ERR_WORKSPACE;
 
     CUtensorMap tk, tv;
-    if ((st = encode_pool(tk, k_cache, g, 16 * pl.hg)) != PA_OK ||
-        (st = encode_pool(tv, v_cache, g, 16 * pl.hg)) != PA_OK)
+    if ((st = encode_pool(tk, k_cache, g)) != PA_OK || (st = encode_pool(tv, v_cache, g)) != PA_OK)
         return st;
 
     DecodeParams p;
@@ -487,7 +374,7 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.out = static_cast<__nv_bfloat16 *>(out);
-    const int64_t units = (int64_t)num_seqs * (g.n_kv / pl.hg);
+    const int64_t units = (int64_t)num_seqs * g.n_kv;
     p.counters = static_cast<int32_t *>(workspace);
     p.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + counters_bytes(units));
     p.dev_status = dev_status;
@@ -510,10 +397,6 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     p.groups = nullptr;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     p.num_real = num_seqs;
-    p.ups = g.n_kv / pl.hg;
-    p.hg = pl.hg;
-    p.stages = pl.stages;
-    p.stage_bytes = pl.stage_bytes;
     if (share) {
         // 1) groups of adjacent sequences sharing leading blocks; 2) one
         //    launch over the group units, then every sequence's remaining
@@ -537,9 +420,9 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
         p.groups = groups;
         p.pre = reinterpret_cast<float *>(ws + SL.pre);
         p.num_ctas = grid;
+        return kp->launch(tk, tv, p, grid, smem_sh, cs) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     }
-    const cudaError_t e = pl.hk ? pl.hk->launch(tk, tv, p, grid, pl.smem, cs)
-                                : pl.kd->launch(tk, tv, p, grid, pl.smem, cs);
+    const cudaError_t e = kd->launch(tk, tv, p, grid, smem, cs);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -600,16 +483,6 @@ const DecodeKernel *find_decode_kernel_int4_mq(int d_h, int group, int nq)
 {
     return d_h == 128 ? find_decode_kernel_int4_mq_d128(group, nq)
                       : d_h == 64 ? find_decode_kernel_int4_mq_d64(group, nq) : nullptr;
-}
-
-const HgKernel *find_hg_kernel_int8(int d_h, int group, bool share);
-const HgKernel *find_hg_kernel_int4(int d_h, int group, bool share);
-
-const HgKernel *find_hg_kernel(int kind, int d_h, int group, bool share)
-{
-    return kind == PA_KV_INT8   ? find_hg_kernel_int8(d_h, group, share)
-           : kind == PA_KV_INT4 ? find_hg_kernel_int4(d_h, group, share)
-                                : nullptr;
 }
 
 const DecodeKernel *find_decode_kernel_int8(int d_h, int group)
@@ -685,10 +558,10 @@ size_t pa_decode_workspace_size(pa_geom geom, int32_t num_seqs, int32_t num_ctas
 {
     if (check_geom(geom) != PA_OK || num_seqs < 0 || num_seqs > kMaxSeqs || num_ctas < 0)
         return 0;
-    Plan pl;
-    if (make_plan(geom, num_seqs, 1, false, num_ctas, pl) != PA_OK)
+    int grid = num_ctas;
+    if (grid == 0 && default_ctas(geom, num_seqs, grid) != PA_OK)
         return 0;
-    return pl.ws_bytes;
+    return workspace_bytes_for(geom, num_seqs, grid);
 }
 
 pa_status pa_decode_workspace_init(void *workspace, size_t workspace_bytes, void *stream)
@@ -734,13 +607,22 @@ size_t pa_decode_opt_workspace_size(pa_geom geom, int32_t num_seqs, const pa_dec
     const int num_ctas = opts ? opts->num_ctas : 0;
     if (num_ctas < 0)
         return 0;
-    const bool share = opts && opts->share_prefix == 1;
-    if (share && group_of(geom) > 8)
+    int grid = num_ctas;
+    if (grid == 0 && default_ctas(geom, num_seqs, grid) != PA_OK)
         return 0;
-    Plan pl;
-    if (make_plan(geom, num_seqs, 1, share, num_ctas, pl) != PA_OK)
+    if (!opts || opts->share_prefix == 0)
+        return workspace_bytes_for(geom, num_seqs, grid);
+    const DecodeKernel *kp = pa::find_prefix_kernel(geom.kv_dtype, geom.d_h, group_of(geom));
+    int dev, sms, per;
+    size_t smem;
+    if (!kp || current_device(dev, sms) != PA_OK)
         return 0;
-    return pl.ws_bytes;
+    const pa_status st = share_fits(kp, num_seqs, smem, per);
+    if (st == PA_ERR_UNSUPPORTED) // decoded without sharing
+        return workspace_bytes_for(geom, num_seqs, grid);
+    if (st != PA_OK)
+        return 0;
+    return share_layout(geom, num_seqs, num_ctas > 0 ? num_ctas : sms * per).end;
 }
 
 pa_status pa_decode_opt(const void *q, const void *k_cache, const void *v_cache,
@@ -829,9 +711,9 @@ int32_t pa_decode_default_ctas(pa_geom geom, int32_t num_seqs)
         return st;
     if (num_seqs < 0 || num_seqs > kMaxSeqs)
         return PA_ERR_SHAPE;
-    Plan pl;
-    st = make_plan(geom, num_seqs, 1, false, 0, pl);
-    return st != PA_OK ? st : pl.grid;
+    int grid = 0;
+    st = default_ctas(geom, num_seqs, grid);
+    return st != PA_OK ? st : grid;
 }
 
 int32_t pa_plan_owner(int64_t item, int64_t total_items, int32_t num_ctas)

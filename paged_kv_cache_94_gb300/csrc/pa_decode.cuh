@@ -84,14 +84,6 @@ struct DecodeParams {
     float *pre;
     const int32_t *groups;
     int32_t num_real;
-    // The work line's units per sequence: n_kv when an item is one kv head's
-    // blocks, n_kv / hg when an item holds a block of hg consecutive kv heads
-    // (the head-group kernel, pa_decode_hg.cuh; stages and stage_bytes are
-    // its ring, sized on the host).
-    int32_t ups;
-    int32_t hg;
-    int32_t stages;
-    int32_t stage_bytes;
 };
 
 // Pass 0: decode of each sequence; pass 2: shared-prefix groups, then each
@@ -166,18 +158,7 @@ struct SmemLayout {
 // context length outside [0, max_blocks*16] counts as 0 blocks (and is
 // reported).
 // ---------------------------------------------------------------------------
-// Barrier over the threads running prefix_blocks: the whole CTA (BAR 0),
-// or the first NT threads only, on named barrier BAR.
-template <int NT, int BAR>
-__device__ __forceinline__ void prefix_sync()
-{
-    if constexpr (BAR != 0)
-        asm volatile("bar.sync %0, %1;" ::"n"(BAR), "r"(NT) : "memory");
-    else
-        __syncthreads();
-}
-
-template <int NT, int PASS, int BPI, int BAR = 0>
+template <int NT, int PASS, int BPI>
 __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P, int32_t *wsum)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -231,7 +212,7 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
             wsum[warp] = x;
             wsum[8 + warp] = z;
         }
-        prefix_sync<NT, BAR>();
+        __syncthreads();
         if (warp == 0) {
             int32_t t = lane < NWARP ? wsum[lane] : 0;
             int32_t tz = lane < NWARP ? wsum[8 + lane] : 0;
@@ -249,7 +230,7 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
                 wsum[8 + lane] = tz;
             }
         }
-        prefix_sync<NT, BAR>();
+        __syncthreads();
         const int32_t before = warp ? wsum[warp - 1] : 0;
         const int32_t zbefore = warp ? wsum[8 + warp - 1] : 0;
         if (b < p.num_seqs) {
@@ -258,7 +239,7 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
         }
         carry += wsum[NWARP - 1];
         zcarry += wsum[8 + NWARP - 1];
-        prefix_sync<NT, BAR>();
+        __syncthreads();
     }
 }
 
@@ -270,8 +251,7 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
 // order. CTA c of G owns virtual [plan_lo(c, Wv, G), plan_lo(c+1, Wv, G)),
 // i.e. the contiguous real items whose virtual positions fall there, so a CTA
 // covering many short units gets fewer blocks. Every sequence with blocks
-// carries ups * kSegCost (ups = units per sequence: n_kv), so the virtual
-// prefix is ups * (P[b] + kSegCost * Z[b]).
+// carries n_kv * kSegCost, so the virtual prefix is P[b] + kSegCost * Z[b].
 // ---------------------------------------------------------------------------
 #ifndef PA_SEG_COST
 #define PA_SEG_COST 8
@@ -291,7 +271,7 @@ __device__ __forceinline__ int64_t virt_start(const DecodeParams &p, const int32
 {
     const uint16_t *Z = reinterpret_cast<const uint16_t *>(P + p.num_seqs + 1);
     const int64_t zl = Z[b < p.lead_units ? b : p.lead_units];
-    return (int64_t)p.ups * (P[b] + (int64_t)p.seg_cost * Z[b] +
+    return (int64_t)p.n_kv * (P[b] + (int64_t)p.seg_cost * Z[b] +
                               ((int64_t)p.seg_cost_lead - p.seg_cost) * zl);
 }
 
@@ -313,7 +293,7 @@ __device__ __forceinline__ int64_t real_at_virtual(const DecodeParams &p, const 
                                                    int64_t y)
 {
     if (y >= virt_total(p, P))
-        return (int64_t)p.ups * P[p.num_seqs];
+        return (int64_t)p.n_kv * P[p.num_seqs];
     int lo = 0, hi = p.num_seqs;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -329,7 +309,7 @@ __device__ __forceinline__ int64_t real_at_virtual(const DecodeParams &p, const 
     const int64_t nb = P[b + 1] - P[b], v = nb + C;
     const int64_t r = y - virt_start(p, P, b);
     const int64_t kvh = r / v, off = r - kvh * v;
-    const int64_t base = (int64_t)p.ups * P[b] + kvh * nb;
+    const int64_t base = (int64_t)p.n_kv * P[b] + kvh * nb;
     return off < C ? base : base + (off - C);
 }
 

@@ -372,24 +372,13 @@ struct QuantMmaPolicy {
         st.sinv = 0.f;
     }
 
-    // One item of BPI 16-token blocks laid out as a ring stage: block j's K
-    // codes at kt + j*TILE, its V codes at kt + (BPI+j)*TILE, its scales at
-    // extra + 64*j (K) and extra + 64*(BPI+j) (V).
+    // One item of BPI 16-token blocks: block j's K codes at kt + j*TILE, its V
+    // codes at kt + (BPI+j)*TILE, its scales at extra + 64*j (K) and
+    // extra + 64*(BPI+j) (V). Tokens [lo, valid) of the item are attended,
+    // those of block j only if bit j of mask is set (the block was loaded);
+    // rem = ctx - (the item's first position), for the causal mask (NQ > 1).
     __device__ static void compute(State &st, uint32_t kt, uint32_t extra, int lo, int valid,
                                    int rem, float scale_log2, uint32_t mask)
-    {
-        compute4(st, kt, kt + BPI * TILE, extra, extra + 64 * BPI, lo, valid, rem, scale_log2,
-                 mask);
-    }
-
-    // The same with every operand's address given: block j's K codes at
-    // kt + j*TILE, V codes at vt0 + j*TILE, K scales at ksc + 64*j, V scales
-    // at vsc + 64*j. Tokens [lo, valid) of the item are attended, those of
-    // block j only if bit j of mask is set (the block was loaded); rem = ctx -
-    // (the item's first position), for the causal mask (NQ > 1).
-    __device__ static void compute4(State &st, uint32_t kt, uint32_t vt0, uint32_t ksc,
-                                    uint32_t vsc, int lo, int valid, int rem, float scale_log2,
-                                    uint32_t mask)
     {
         const int lane = threadIdx.x & 31, gid = lane >> 2, t4 = lane & 3;
 
@@ -469,8 +458,8 @@ struct QuantMmaPolicy {
             const bool in = (mask >> j) & 1u;
             lo_ok[j] = in && tl >= lo && tl < valid;
             hi_ok[j] = in && th >= lo && th < valid;
-            const float f_lo = st.qexp * lds_f32(ksc + 64 * j + 4 * gid) * scale_log2;
-            const float f_hi = st.qexp * lds_f32(ksc + 64 * j + 4 * (gid + 8)) * scale_log2;
+            const float f_lo = st.qexp * lds_f32(extra + 64 * j + 4 * gid) * scale_log2;
+            const float f_hi = st.qexp * lds_f32(extra + 64 * j + 4 * (gid + 8)) * scale_log2;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 // S^T element c: token row gid (c < 2) or gid+8, head column 2t4 + (c & 1)
@@ -531,8 +520,8 @@ struct QuantMmaPolicy {
         float sv_lo[BPI], sv_hi[BPI], svm = 0.f;
 #pragma unroll
         for (int j = 0; j < BPI; ++j) {
-            sv_lo[j] = lo_ok[j] ? lds_f32(vsc + 64 * j + 4 * gid) : 0.f;
-            sv_hi[j] = hi_ok[j] ? lds_f32(vsc + 64 * j + 4 * (gid + 8)) : 0.f;
+            sv_lo[j] = lo_ok[j] ? lds_f32(extra + 64 * (BPI + j) + 4 * gid) : 0.f;
+            sv_hi[j] = hi_ok[j] ? lds_f32(extra + 64 * (BPI + j) + 4 * (gid + 8)) : 0.f;
             svm = fmaxf(svm, fmaxf(sv_lo[j], sv_hi[j]));
         }
         if (__any_sync(0xffffffffu, svm > st.sbase * kScaleRatio)) {
@@ -573,7 +562,7 @@ struct QuantMmaPolicy {
         // gid+8): CW contiguous codes of each token row.
 #pragma unroll
         for (int j = 0; j < BPI; ++j) {
-            const uint32_t vt = vt0 + j * TILE;
+            const uint32_t vt = kt + (BPI + j) * TILE;
             auto pv = [&](int mt, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)

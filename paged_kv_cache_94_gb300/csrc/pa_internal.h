@@ -24,29 +24,6 @@ struct DecodeKernel {
                           int grid, size_t smem, cudaStream_t stream);
 };
 
-// A compiled head-group decode kernel (pa_decode_hg.cuh): one item is a
-// block of hg consecutive kv heads, streamed by a producer warp into a ring
-// of `stages` stages of `stage_bytes` each (both chosen on the host).
-struct HgKernel {
-    const void *fn;
-    int threads;
-    int consumers;                 // consumer warps (the head group divides it)
-    int tile;                      // bytes of one (block, kv head) code tile
-    size_t (*smem_bytes)(int stages, int stage_bytes, int hg, int num_seqs);
-    cudaError_t (*launch)(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
-                          int grid, size_t smem, cudaStream_t stream);
-};
-// Bytes of one ring stage of the head-group kernel: K codes, V codes, K
-// scales, V scales of hg heads, rounded to 1024 so that every stage, and
-// every (block, head) tile in it, stays aligned for the TMA swizzle.
-constexpr int hg_stage_bytes(int tile, int hg)
-{
-    return (2 * hg * tile + 2 * hg * 64 + 1023) / 1024 * 1024;
-}
-// kind 1: INT8, 2: INT4; share: the shared-prefix launch (group <= 8). NULL
-// when the combination is not compiled.
-const HgKernel *find_hg_kernel(int kind, int d_h, int group, bool share);
-
 // NULL when the combination is not compiled.
 const DecodeKernel *find_decode_kernel_bf16(int d_h, int group);
 const DecodeKernel *find_decode_kernel_int8(int d_h, int group);
