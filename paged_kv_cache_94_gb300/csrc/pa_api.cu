@@ -397,6 +397,7 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     p.groups = nullptr;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     p.num_real = num_seqs;
+    p.grid_fixed = num_ctas > 0 ? 1 : 0;
     if (share) {
         // 1) groups of adjacent sequences sharing leading blocks; 2) one
         //    launch over the group units, then every sequence's remaining

@@ -378,11 +378,20 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
     // kv head) are exactly the owners of its first through last block, which
     // the split merge counts on.
     const int64_t Wv = virt_total(p, P);
-    const int64_t G = plan_ctas(p.num_ctas, Wv);
-    if ((int64_t)blockIdx.x >= G)
-        return;
-    const int64_t lo = real_at_virtual(p, P, plan_lo(blockIdx.x, Wv, G));
-    const int64_t hi = real_at_virtual(p, P, plan_lo(blockIdx.x + 1, Wv, G));
+    int64_t G = plan_ctas(p.num_ctas, Wv);
+    int64_t lo, hi;
+    const int64_t U = PASS == 0 ? whole_unit_grid<NW * 32>(p, P, G, misc + 8) : 0;
+    if (U > 0) { // one CTA per unit: every segment is a whole unit
+        if ((int64_t)blockIdx.x >= U)
+            return;
+        unit_items(p, P, blockIdx.x, lo, hi);
+        G = U;
+    } else {
+        if ((int64_t)blockIdx.x >= G)
+            return;
+        lo = real_at_virtual(p, P, plan_lo(blockIdx.x, Wv, G));
+        hi = real_at_virtual(p, P, plan_lo(blockIdx.x + 1, Wv, G));
+    }
 
     if (lane == 0)
         for (int s = 0; s < S; ++s)
