@@ -92,21 +92,32 @@ __device__ __forceinline__ uint32_t nib_hi(uint32_t w)
     return (w & 0x00F000F0u) ^ 0x64806480u;
 }
 
+__device__ __forceinline__ __half2 as_h2(uint32_t x)
+{
+    __half2 h;
+    memcpy(&h, &x, sizeof h);
+    return h;
+}
+
+__device__ __forceinline__ uint32_t as_u32(__half2 h)
+{
+    uint32_t x;
+    memcpy(&x, &h, sizeof x);
+    return x;
+}
+
 // fp16x2 {B + c0, B + c1} -> {c0, c1}, exact (every value involved is an
-// fp16 integer below 2^11).
+// fp16 integer below 2^11). Written with the half2 intrinsics (not inline
+// assembly) so that a constant B can be encoded in the instruction.
 __device__ __forceinline__ uint32_t h2_sub(uint32_t x, uint32_t b2)
 {
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(b2));
-    return r;
+    return as_u32(__hsub2(as_h2(x), as_h2(b2)));
 }
 
 // fp16x2 {1152 + 16 c0, 1152 + 16 c1} -> {c0, c1}: x / 16 - 72, exact.
 __device__ __forceinline__ uint32_t h2_hi_code(uint32_t x)
 {
-    uint32_t r;
-    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0x2C002C00u), "r"(0xD480D480u));
-    return r;
+    return as_u32(__hfma2(as_h2(x), as_h2(0x2C002C00u), as_h2(0xD480D480u)));
 }
 
 constexpr uint32_t kH2_1152 = 0x64806480u; // fp16x2 {1152, 1152}
