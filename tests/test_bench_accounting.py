@@ -44,3 +44,21 @@ def test_window_counts_only_the_window():
     # sequence 0 attends [60, 100): blocks 3..6; sequence 1 attends [0, 20): blocks 0..1
     d = bench.decode_bytes(w)
     assert d["bytes"] == (40 + 20) * 512 + 4 * (4 + 2) + 8 + 2048
+
+
+def test_oracle_on_all_cores_runs_the_sample():
+    # the CPU baseline's all-cores leg: (sequence, kv head) units of the
+    # sample dealt to spawned processes, timed by wall clock
+    w = bench.named_workload("tiny")
+    pool = bench.OracleCores(w, [0, 1])
+    try:
+        assert 1 <= pool.cores <= 2 * w.geom.n_kv
+        assert pool.run() > 0 and pool.run() > 0
+    finally:
+        pool.close()
+
+
+def test_probe_bytes_count_every_block():
+    w = make_workload("probe", Geometry(n_h=4, n_kv=2, d_h=64, kv_dtype="int8"), [5, 37], seed=1)
+    blocks = 1 + 3
+    assert bench.probe_bytes(w) == blocks * 2 * (2 * 16 * 64 + 2 * 16 * 4) + 4 * blocks
