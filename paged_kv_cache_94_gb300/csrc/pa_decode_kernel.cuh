@@ -493,6 +493,8 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         locate_item(seg_lo, P, p.num_seqs, p.n_kv, b, kvh, i0, nb);
         Pol::prefetch_q(st, p, rows(b, kvh));
     }
+    // the next segment's context length, loaded with its q (pass 0)
+    int32_t ctx_next = (PASS == 0 && seg_lo < hi) ? __ldg(p.context_lens + b) : 0;
     while (seg_lo < hi) {
         const int i0_cur = i0;
         const int64_t unit_start = seg_lo - i0;
@@ -514,7 +516,7 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
                 fb = __ldg(p.skip + (b - p.num_real));
             }
         } else {
-            ctx = __ldg(p.context_lens + b);
+            ctx = ctx_next;
             ws = window_start(p, ctx);
             pool_from = ws > p.n_sink ? ws : p.n_sink;
             fb = seq_first_block(p, ctx);
@@ -561,6 +563,8 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
         if (seg_hi < hi) {
             locate_item(seg_hi, P, p.num_seqs, p.n_kv, b, kvh, i0, nb);
             Pol::prefetch_q(st, p, rows(b, kvh));
+            if constexpr (PASS == 0)
+                ctx_next = __ldg(p.context_lens + b);
         }
         Pol::to_merge(st, merge);
         __syncthreads();

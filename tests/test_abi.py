@@ -130,6 +130,15 @@ def test_plan_owner_matches_brute_force(lib):
         sizes = [lo[c + 1] - lo[c] for c in range(G)]
         assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
     assert lib.pa_plan_owner(5, 5, 3) == -1
+    # lines whose W * G passes 2^32 take 64-bit arithmetic, the others 32-bit:
+    # the owner of x is the c with floor(c W / G) <= x < floor((c+1) W / G)
+    import random
+    rng = random.Random(5)
+    for W, grid in [(2**32 // 456, 456), (2**32 // 456 + 1, 456), (10**9, 1000), (3 * 10**9, 8000)]:
+        G = min(grid, W)
+        for x in [0, 1, W - 2, W - 1] + [rng.randrange(W) for _ in range(200)]:
+            c = lib.pa_plan_owner(x, W, grid)
+            assert c * W // G <= x < (c + 1) * W // G, (W, grid, x, c)
 
 
 def test_binding_refuses_cpu_tensors():
