@@ -259,6 +259,15 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
 #endif
 constexpr int kSegCost = PA_SEG_COST;
 
+// a / b for 0 <= a, 0 < b: in 32-bit arithmetic when a fits (the usual
+// case; a 64-bit division is several times longer on the device).
+__device__ __forceinline__ int64_t div_small(int64_t a, int64_t b)
+{
+    if (a <= (int64_t)0xFFFFFFFF && b <= (int64_t)0xFFFFFFFF)
+        return (int64_t)((uint32_t)a / (uint32_t)b);
+    return a / b;
+}
+
 // Virtual position of the first block of unit (b, kvh) (nb = blocks of b).
 // Z = P + num_seqs + 1 counts the sequences with blocks: an empty sequence
 // has no segment and costs nothing. A unit of one of the first lead_units
@@ -309,7 +318,7 @@ __device__ __forceinline__ int64_t real_at_virtual(const DecodeParams &p, const 
     const int64_t C = unit_cost(p, b);
     const int64_t nb = P[b + 1] - P[b], v = nb + C;
     const int64_t r = y - virt_start(p, P, b);
-    const int64_t kvh = r / v, off = r - kvh * v;
+    const int64_t kvh = div_small(r, v), off = r - kvh * v;
     const int64_t base = (int64_t)p.n_kv * P[b] + kvh * nb;
     return off < C ? base : base + (off - C);
 }
@@ -385,7 +394,7 @@ __device__ __forceinline__ void locate_item(int64_t x, const int32_t *P, int num
     b = lo;
     nb = P[b + 1] - P[b];
     const int64_t r = x - (int64_t)n_kv * P[b];
-    kvh = (int)(r / nb);
+    kvh = (int)div_small(r, nb);
     i = (int)(r - (int64_t)kvh * nb);
 }
 
