@@ -140,7 +140,7 @@ struct SmemLayout {
     static constexpr int kMeta = NW * S * 4;
     static constexpr int kMerge = NW * GQ * (D + 2) * 4;                // per-warp (m, l, acc)
     static constexpr int kSinkSc = GQ * 16 * 4;                         // sink-row scores
-    static constexpr int kMisc = 128; // 32 int32 of per-CTA scratch (flags, scan sums)
+    static constexpr int kMisc = 256; // 64 int32 of per-CTA scratch (flags, scan sums)
     static constexpr int kOffExtra = kRing;
     static constexpr int kOffQ = kOffExtra + kExtra;
     static constexpr int kOffBars = (kOffQ + kQ + 15) / 16 * 16;
@@ -159,9 +159,12 @@ struct SmemLayout {
 // context length outside [0, max_blocks*16] counts as 0 blocks (and is
 // reported).
 // ---------------------------------------------------------------------------
+// wsum: 32 int32 of scratch (per-warp sums at [w], nonempty counts at
+// [16 + w]; up to 16 warps).
 template <int NT, int PASS, int BPI>
 __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P, int32_t *wsum)
 {
+    static_assert(NT <= 16 * 32, "the scan's scratch holds 16 warp sums");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NWARP = NT / 32;
     int32_t carry = 0, zcarry = 0;
@@ -211,12 +214,12 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
         }
         if (lane == 31) {
             wsum[warp] = x;
-            wsum[8 + warp] = z;
+            wsum[16 + warp] = z;
         }
         __syncthreads();
         if (warp == 0) {
             int32_t t = lane < NWARP ? wsum[lane] : 0;
-            int32_t tz = lane < NWARP ? wsum[8 + lane] : 0;
+            int32_t tz = lane < NWARP ? wsum[16 + lane] : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int32_t y = __shfl_up_sync(0xffffffffu, t, o);
@@ -228,18 +231,18 @@ __device__ __forceinline__ void prefix_blocks(const DecodeParams &p, int32_t *P,
             }
             if (lane < NWARP) {
                 wsum[lane] = t; // inclusive
-                wsum[8 + lane] = tz;
+                wsum[16 + lane] = tz;
             }
         }
         __syncthreads();
         const int32_t before = warp ? wsum[warp - 1] : 0;
-        const int32_t zbefore = warp ? wsum[8 + warp - 1] : 0;
+        const int32_t zbefore = warp ? wsum[16 + warp - 1] : 0;
         if (b < p.num_seqs) {
             P[b + 1] = carry + before + x;
             Z[b + 1] = (uint16_t)(zcarry + zbefore + z);
         }
         carry += wsum[NWARP - 1];
-        zcarry += wsum[8 + NWARP - 1];
+        zcarry += wsum[16 + NWARP - 1];
         __syncthreads();
     }
 }

@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(Pol::NW * 32, Pol::kMinBlocks)
 {
     constexpr int NW = Pol::NW, S = Pol::S, D = Pol::D, GQ = Pol::GQ;
     using L = typename Pol::Layout;
-    static_assert(NW <= 8, "misc scratch holds 8 warp sums");
+    static_assert(NW <= 16, "misc scratch holds 16 warp sums");
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
