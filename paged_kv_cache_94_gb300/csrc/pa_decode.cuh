@@ -510,6 +510,16 @@ __device__ __forceinline__ void emit(const DecodeParams &p, int b, int kvh, int 
     p.out[row * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
 }
 
+// Final output of d and d + 1 (d even) of query row h: one bf16x2 store.
+template <int D, int GQ, int NQ>
+__device__ __forceinline__ void emit2(const DecodeParams &p, int b, int kvh, int h, int d, float L,
+                                      float O0, float O1)
+{
+    const size_t row = qo_row<GQ, NQ>(p, b, kvh, h);
+    *reinterpret_cast<__nv_bfloat162 *>(p.out + row * D + d) =
+        __floats2bfloat162_rn(L > 0.f ? O0 / L : 0.f, L > 0.f ? O1 / L : 0.f);
+}
+
 template <int D, int GQ, int NW, int NQ>
 __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int32_t *P,
                                                const float *merge, int32_t *misc, float *sink_sc,
@@ -580,43 +590,63 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
     __syncthreads();
     if (!misc[0])
         return;
-    // Last arrival: merge the nseg records, loads issued four at a time.
+    // Last arrival: merge the nseg records. A thread takes two adjacent d of
+    // one head per step and two steps at a time; the records' (m, l, o[d],
+    // o[d+1]) are read four records at a time and folded in with a running
+    // maximum, so one round of loads serves four records of two steps.
     const float *base = p.partials + ((size_t)c_first + u) * (GQ * REC);
+    constexpr int PAIRS = GQ * D / 2;
 #pragma unroll 1
-    for (int idx = threadIdx.x; idx < GQ * D; idx += NT) {
-        const int h = idx / D, d = idx - h * D;
-        float M = -INFINITY;
+    for (int p0 = threadIdx.x; p0 < PAIRS; p0 += 2 * NT) {
+        float M[2], L[2], O0[2], O1[2];
+        int hq[2], dq[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int pq = min(p0 + q * NT, PAIRS - 1); // past the end: read, not written
+            hq[q] = 2 * pq / D;
+            dq[q] = 2 * pq - hq[q] * D;
+            M[q] = -INFINITY;
+            L[q] = O0[q] = O1[q] = 0.f;
+        }
 #pragma unroll 1
         for (int s0 = 0; s0 < nseg; s0 += 4) {
-            float m4[4];
+            float m4[2][4], l4[2][4];
+            float2 o4[2][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                m4[j] = (s0 + j < nseg) ? __ldcg(base + (size_t)(s0 + j) * GQ * REC + h * REC)
-                                        : -INFINITY;
-            M = fmaxf(M, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
-        }
-        float O = 0.f, L = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll 1
-            for (int s0 = 0; s0 < nseg; s0 += 4) {
-                float m4[4], l4[4], o4[4];
+            for (int q = 0; q < 2; ++q)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const bool in = s0 + j < nseg;
-                    const float *r = base + (size_t)(in ? s0 + j : s0) * GQ * REC + h * REC;
-                    m4[j] = in ? __ldcg(r) : -INFINITY;
-                    l4[j] = in ? __ldcg(r + 1) : 0.f;
-                    o4[j] = in ? __ldcg(r + 2 + d) : 0.f;
+                    const float *r = base + (size_t)(in ? s0 + j : s0) * GQ * REC + hq[q] * REC;
+                    m4[q][j] = in ? __ldcg(r) : -INFINITY;
+                    l4[q][j] = in ? __ldcg(r + 1) : 0.f;
+                    o4[q][j] = in ? __ldcg(reinterpret_cast<const float2 *>(r + 2 + dq[q]))
+                                  : make_float2(0.f, 0.f);
                 }
 #pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const float mx = fmaxf(fmaxf(M[q], fmaxf(m4[q][0], m4[q][1])),
+                                       fmaxf(m4[q][2], m4[q][3]));
+                if (mx == -INFINITY)
+                    continue;
+                const float a = (M[q] == -INFINITY) ? 0.f : fast_exp2(M[q] - mx);
+                L[q] *= a;
+                O0[q] *= a;
+                O1[q] *= a;
+#pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float sc = (m4[j] == -INFINITY) ? 0.f : fast_exp2(m4[j] - M);
-                    L = fmaf(sc, l4[j], L);
-                    O = fmaf(sc, o4[j], O);
+                    const float sc = (m4[q][j] == -INFINITY) ? 0.f : fast_exp2(m4[q][j] - mx);
+                    L[q] = fmaf(sc, l4[q][j], L[q]);
+                    O0[q] = fmaf(sc, o4[q][j].x, O0[q]);
+                    O1[q] = fmaf(sc, o4[q][j].y, O1[q]);
                 }
+                M[q] = mx;
             }
         }
-        emit<D, GQ, NQ>(p, b, kvh, h, d, M, L, O);
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            if (p0 + q * NT < PAIRS)
+                emit2<D, GQ, NQ>(p, b, kvh, hq[q], dq[q], L[q], O0[q], O1[q]);
     }
 }
 
