@@ -500,16 +500,6 @@ __device__ __forceinline__ int64_t unit_row(const DecodeParams &p, int s, int kv
     }
 }
 
-// Final (M, L, O) of query row h, column d of (sequence b, kv head kvh):
-// the bf16 output.
-template <int D, int GQ, int NQ>
-__device__ __forceinline__ void emit(const DecodeParams &p, int b, int kvh, int h, int d, float M,
-                                     float L, float O)
-{
-    const size_t row = qo_row<GQ, NQ>(p, b, kvh, h);
-    p.out[row * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
-}
-
 // Final output of d and d + 1 (d even) of query row h: one bf16x2 store.
 template <int D, int GQ, int NQ>
 __device__ __forceinline__ void emit2(const DecodeParams &p, int b, int kvh, int h, int d, float L,
@@ -528,6 +518,11 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
 {
     constexpr int NT = NW * 32;
     constexpr int REC = D + 2;
+    // A thread combines a run of RUN adjacent d of one head, so the head's
+    // weights are worked out once per thread (GQ, D and NT are powers of two).
+    constexpr int RUN = GQ * D / NT > 2 ? GQ * D / NT : 2;
+    constexpr int RUNS = GQ * D / RUN;
+    static_assert(RUNS <= NT && D % RUN == 0, "one run per thread");
     const int u = b * p.n_kv + kvh;
     float *rec = p.partials + ((size_t)blockIdx.x + u) * (GQ * REC);
     // Sink rows [s_lo, s_hi) join this segment's merge as one more partial
@@ -537,9 +532,10 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
         sink_scores<D, GQ, NW, NQ>(p, b, kvh, s_lo, s_hi, sink_sc);
     const __nv_bfloat16 *sv = p.sink_v + ((size_t)b * p.n_kv + kvh) * p.n_sink * D;
 
-#pragma unroll 1
-    for (int idx = threadIdx.x; idx < GQ * D; idx += NT) {
-        const int h = idx / D, d = idx - h * D;
+    const bool act = threadIdx.x < RUNS;
+    const int h = act ? (int)threadIdx.x * RUN / D : 0;
+    const int d0 = act ? (int)threadIdx.x * RUN - h * D : 0;
+    if (act) {
         float mw[NW];
         float M = -INFINITY;
 #pragma unroll
@@ -549,28 +545,43 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
         }
         for (int j = 0; j < ns; ++j)
             M = fmaxf(M, sink_sc[h * 16 + j]);
-        float O = 0.f, L = 0.f;
+        float O[RUN], L = 0.f;
+#pragma unroll
+        for (int e = 0; e < RUN; ++e)
+            O[e] = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
+                const float *mrow = merge + (w * GQ + h) * REC;
                 const float sc = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
-                L = fmaf(sc, merge[(w * GQ + h) * REC + 1], L);
-                O = fmaf(sc, merge[(w * GQ + h) * REC + 2 + d], O);
+                L = fmaf(sc, mrow[1], L);
+#pragma unroll
+                for (int e = 0; e < RUN; e += 2) {
+                    const float2 a = *reinterpret_cast<const float2 *>(mrow + 2 + d0 + e);
+                    O[e] = fmaf(sc, a.x, O[e]);
+                    O[e + 1] = fmaf(sc, a.y, O[e + 1]);
+                }
             }
             for (int j = 0; j < ns; ++j) {
-                const float e = fast_exp2(sink_sc[h * 16 + j] - M);
-                L += e;
-                O = fmaf(e, __bfloat162float(sv[(s_lo + j) * D + d]), O);
+                const float ej = fast_exp2(sink_sc[h * 16 + j] - M);
+                L += ej;
+#pragma unroll
+                for (int e = 0; e < RUN; ++e)
+                    O[e] = fmaf(ej, __bfloat162float(sv[(s_lo + j) * D + d0 + e]), O[e]);
             }
         }
         if (whole) {
-            emit<D, GQ, NQ>(p, b, kvh, h, d, M, L, O);
+#pragma unroll
+            for (int e = 0; e < RUN; e += 2)
+                emit2<D, GQ, NQ>(p, b, kvh, h, d0 + e, L, O[e], O[e + 1]);
         } else {
-            if (d == 0) {
+            if (d0 == 0) {
                 rec[h * REC] = M;
                 rec[h * REC + 1] = L;
             }
-            rec[h * REC + 2 + d] = O;
+#pragma unroll
+            for (int e = 0; e < RUN; e += 2)
+                *reinterpret_cast<float2 *>(rec + h * REC + 2 + d0 + e) = make_float2(O[e], O[e + 1]);
         }
     }
     __syncthreads(); // also: every record store of this CTA is done (CTA scope)
@@ -588,66 +599,57 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
         misc[0] = last;
     }
     __syncthreads();
-    if (!misc[0])
+    if (!misc[0] || !act)
         return;
-    // Last arrival: merge the nseg records. A thread takes two adjacent d of
-    // one head per step and two steps at a time; the records' (m, l, o[d],
-    // o[d+1]) are read four records at a time and folded in with a running
-    // maximum, so one round of loads serves four records of two steps.
-    const float *base = p.partials + ((size_t)c_first + u) * (GQ * REC);
-    constexpr int PAIRS = GQ * D / 2;
-#pragma unroll 1
-    for (int p0 = threadIdx.x; p0 < PAIRS; p0 += 2 * NT) {
-        float M[2], L[2], O0[2], O1[2];
-        int hq[2], dq[2];
+    // Last arrival: merge the nseg records, RB of them per round of loads
+    // (each thread's run of d), folded in with a running maximum.
+    constexpr int RB = RUN >= 16 ? 2 : 4;
+    const float *base = p.partials + ((size_t)c_first + u) * (GQ * REC) + h * REC;
+    float M = -INFINITY, L = 0.f, O[RUN];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int pq = min(p0 + q * NT, PAIRS - 1); // past the end: read, not written
-            hq[q] = 2 * pq / D;
-            dq[q] = 2 * pq - hq[q] * D;
-            M[q] = -INFINITY;
-            L[q] = O0[q] = O1[q] = 0.f;
+    for (int e = 0; e < RUN; ++e)
+        O[e] = 0.f;
+#pragma unroll 1
+    for (int s0 = 0; s0 < nseg; s0 += RB) {
+        float mr[RB], lr[RB];
+        float2 orr[RB][RUN / 2];
+#pragma unroll
+        for (int j = 0; j < RB; ++j) {
+            const bool in = s0 + j < nseg;
+            const float *r = base + (size_t)(in ? s0 + j : s0) * GQ * REC;
+            mr[j] = in ? __ldcg(r) : -INFINITY;
+            lr[j] = in ? __ldcg(r + 1) : 0.f;
+#pragma unroll
+            for (int e = 0; e < RUN / 2; ++e)
+                orr[j][e] = in ? __ldcg(reinterpret_cast<const float2 *>(r + 2 + d0) + e)
+                               : make_float2(0.f, 0.f);
         }
-#pragma unroll 1
-        for (int s0 = 0; s0 < nseg; s0 += 4) {
-            float m4[2][4], l4[2][4];
-            float2 o4[2][4];
+        float mx = M;
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
+        for (int j = 0; j < RB; ++j)
+            mx = fmaxf(mx, mr[j]);
+        if (mx == -INFINITY)
+            continue;
+        const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mx);
+        L *= a;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const bool in = s0 + j < nseg;
-                    const float *r = base + (size_t)(in ? s0 + j : s0) * GQ * REC + hq[q] * REC;
-                    m4[q][j] = in ? __ldcg(r) : -INFINITY;
-                    l4[q][j] = in ? __ldcg(r + 1) : 0.f;
-                    o4[q][j] = in ? __ldcg(reinterpret_cast<const float2 *>(r + 2 + dq[q]))
-                                  : make_float2(0.f, 0.f);
-                }
+        for (int e = 0; e < RUN; ++e)
+            O[e] *= a;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const float mx = fmaxf(fmaxf(M[q], fmaxf(m4[q][0], m4[q][1])),
-                                       fmaxf(m4[q][2], m4[q][3]));
-                if (mx == -INFINITY)
-                    continue;
-                const float a = (M[q] == -INFINITY) ? 0.f : fast_exp2(M[q] - mx);
-                L[q] *= a;
-                O0[q] *= a;
-                O1[q] *= a;
+        for (int j = 0; j < RB; ++j) {
+            const float sc = (mr[j] == -INFINITY) ? 0.f : fast_exp2(mr[j] - mx);
+            L = fmaf(sc, lr[j], L);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float sc = (m4[q][j] == -INFINITY) ? 0.f : fast_exp2(m4[q][j] - mx);
-                    L[q] = fmaf(sc, l4[q][j], L[q]);
-                    O0[q] = fmaf(sc, o4[q][j].x, O0[q]);
-                    O1[q] = fmaf(sc, o4[q][j].y, O1[q]);
-                }
-                M[q] = mx;
+            for (int e = 0; e < RUN / 2; ++e) {
+                O[2 * e] = fmaf(sc, orr[j][e].x, O[2 * e]);
+                O[2 * e + 1] = fmaf(sc, orr[j][e].y, O[2 * e + 1]);
             }
         }
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-            if (p0 + q * NT < PAIRS)
-                emit2<D, GQ, NQ>(p, b, kvh, hq[q], dq[q], L[q], O0[q], O1[q]);
+        M = mx;
     }
+#pragma unroll
+    for (int e = 0; e < RUN; e += 2)
+        emit2<D, GQ, NQ>(p, b, kvh, h, d0 + e, L, O[e], O[e + 1]);
 }
 
 // ---------------------------------------------------------------------------
