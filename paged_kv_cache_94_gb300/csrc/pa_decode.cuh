@@ -510,6 +510,78 @@ __device__ __forceinline__ void emit2(const DecodeParams &p, int b, int kvh, int
         __floats2bfloat162_rn(L > 0.f ? O0 / L : 0.f, L > 0.f ? O1 / L : 0.f);
 }
 
+// Log-sum-exp state of a run of RUN adjacent d of one row, merged from
+// partial states (m, l, o[d]) with a running maximum:
+//   M = max m,  L = sum 2^(m - M) l,  O[e] = sum 2^(m - M) o[d0 + e].
+template <int RUN>
+struct RunState {
+    float M, L, O[RUN];
+    __device__ __forceinline__ void clear()
+    {
+        M = -INFINITY;
+        L = 0.f;
+#pragma unroll
+        for (int e = 0; e < RUN; ++e)
+            O[e] = 0.f;
+    }
+};
+
+// Fold the states of nrec rows (row r at base + r * stride, laid out m, l,
+// o[D]) for d in [d0, d0 + RUN) into st, RB rows per round of loads.
+template <int RUN, int RB>
+__device__ __forceinline__ void fold_rows(RunState<RUN> &st, const float *base, size_t stride,
+                                          int nrec, int d0)
+{
+#pragma unroll 1
+    for (int s0 = 0; s0 < nrec; s0 += RB) {
+        float mr[RB], lr[RB];
+        float2 orr[RB][RUN / 2];
+#pragma unroll
+        for (int j = 0; j < RB; ++j) {
+            const bool in = s0 + j < nrec;
+            const float *r = base + (size_t)(in ? s0 + j : s0) * stride;
+            mr[j] = in ? __ldcg(r) : -INFINITY;
+            lr[j] = in ? __ldcg(r + 1) : 0.f;
+#pragma unroll
+            for (int e = 0; e < RUN / 2; ++e)
+                orr[j][e] = in ? __ldcg(reinterpret_cast<const float2 *>(r + 2 + d0) + e)
+                               : make_float2(0.f, 0.f);
+        }
+        float mx = st.M;
+#pragma unroll
+        for (int j = 0; j < RB; ++j)
+            mx = fmaxf(mx, mr[j]);
+        if (mx == -INFINITY)
+            continue;
+        const float a = (st.M == -INFINITY) ? 0.f : fast_exp2(st.M - mx);
+        st.L *= a;
+#pragma unroll
+        for (int e = 0; e < RUN; ++e)
+            st.O[e] *= a;
+#pragma unroll
+        for (int j = 0; j < RB; ++j) {
+            const float sc = (mr[j] == -INFINITY) ? 0.f : fast_exp2(mr[j] - mx);
+            st.L = fmaf(sc, lr[j], st.L);
+#pragma unroll
+            for (int e = 0; e < RUN / 2; ++e) {
+                st.O[2 * e] = fmaf(sc, orr[j][e].x, st.O[2 * e]);
+                st.O[2 * e + 1] = fmaf(sc, orr[j][e].y, st.O[2 * e + 1]);
+            }
+        }
+        st.M = mx;
+    }
+}
+
+// Run length of the merges: each thread takes RUN adjacent d of one row
+// (GQ, D and the CTA's NT threads are powers of two), four rows per round
+// of loads (two for the longest runs).
+template <int D, int GQ, int NT>
+struct MergeRun {
+    static constexpr int RUN = GQ * D / NT > 2 ? GQ * D / NT : 2;
+    static constexpr int RB = RUN >= 16 ? 2 : 4;
+    static_assert(GQ * D / RUN <= NT && D % RUN == 0, "one run per thread");
+};
+
 template <int D, int GQ, int NW, int NQ>
 __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int32_t *P,
                                                const float *merge, int32_t *misc, float *sink_sc,
@@ -519,10 +591,9 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
     constexpr int NT = NW * 32;
     constexpr int REC = D + 2;
     // A thread combines a run of RUN adjacent d of one head, so the head's
-    // weights are worked out once per thread (GQ, D and NT are powers of two).
-    constexpr int RUN = GQ * D / NT > 2 ? GQ * D / NT : 2;
+    // weights are worked out once per thread.
+    constexpr int RUN = MergeRun<D, GQ, NT>::RUN;
     constexpr int RUNS = GQ * D / RUN;
-    static_assert(RUNS <= NT && D % RUN == 0, "one run per thread");
     const int u = b * p.n_kv + kvh;
     float *rec = p.partials + ((size_t)blockIdx.x + u) * (GQ * REC);
     // Sink rows [s_lo, s_hi) join this segment's merge as one more partial
@@ -601,55 +672,14 @@ __device__ __forceinline__ void finish_segment(const DecodeParams &p, const int3
     __syncthreads();
     if (!misc[0] || !act)
         return;
-    // Last arrival: merge the nseg records, RB of them per round of loads
-    // (each thread's run of d), folded in with a running maximum.
-    constexpr int RB = RUN >= 16 ? 2 : 4;
-    const float *base = p.partials + ((size_t)c_first + u) * (GQ * REC) + h * REC;
-    float M = -INFINITY, L = 0.f, O[RUN];
-#pragma unroll
-    for (int e = 0; e < RUN; ++e)
-        O[e] = 0.f;
-#pragma unroll 1
-    for (int s0 = 0; s0 < nseg; s0 += RB) {
-        float mr[RB], lr[RB];
-        float2 orr[RB][RUN / 2];
-#pragma unroll
-        for (int j = 0; j < RB; ++j) {
-            const bool in = s0 + j < nseg;
-            const float *r = base + (size_t)(in ? s0 + j : s0) * GQ * REC;
-            mr[j] = in ? __ldcg(r) : -INFINITY;
-            lr[j] = in ? __ldcg(r + 1) : 0.f;
-#pragma unroll
-            for (int e = 0; e < RUN / 2; ++e)
-                orr[j][e] = in ? __ldcg(reinterpret_cast<const float2 *>(r + 2 + d0) + e)
-                               : make_float2(0.f, 0.f);
-        }
-        float mx = M;
-#pragma unroll
-        for (int j = 0; j < RB; ++j)
-            mx = fmaxf(mx, mr[j]);
-        if (mx == -INFINITY)
-            continue;
-        const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mx);
-        L *= a;
-#pragma unroll
-        for (int e = 0; e < RUN; ++e)
-            O[e] *= a;
-#pragma unroll
-        for (int j = 0; j < RB; ++j) {
-            const float sc = (mr[j] == -INFINITY) ? 0.f : fast_exp2(mr[j] - mx);
-            L = fmaf(sc, lr[j], L);
-#pragma unroll
-            for (int e = 0; e < RUN / 2; ++e) {
-                O[2 * e] = fmaf(sc, orr[j][e].x, O[2 * e]);
-                O[2 * e + 1] = fmaf(sc, orr[j][e].y, O[2 * e + 1]);
-            }
-        }
-        M = mx;
-    }
+    // Last arrival: merge the nseg records (each thread's run of d).
+    RunState<RUN> st;
+    st.clear();
+    fold_rows<RUN, MergeRun<D, GQ, NT>::RB>(
+        st, p.partials + ((size_t)c_first + u) * (GQ * REC) + h * REC, (size_t)GQ * REC, nseg, d0);
 #pragma unroll
     for (int e = 0; e < RUN; e += 2)
-        emit2<D, GQ, NQ>(p, b, kvh, h, d0 + e, L, O[e], O[e + 1]);
+        emit2<D, GQ, NQ>(p, b, kvh, h, d0 + e, st.L, st.O[e], st.O[e + 1]);
 }
 
 // ---------------------------------------------------------------------------
@@ -672,42 +702,26 @@ __device__ __forceinline__ void unit_owners(const DecodeParams &p, const int32_t
     nseg = (int)(plan_owner(v0 + nb - 1, Wv, G) - c_first + 1);
 }
 
-// Output element (h, d) of sequence b, kv head kvh: its records, written
-// by CTAs c_first .. c_first + nseg - 1, and its group's prefix state.
-template <int D, int GQ>
-__device__ __forceinline__ void merge_element(const DecodeParams &p, int b, int kvh,
-                                              int64_t c_first, int nseg, int h, int d)
+// Output run [d0, d0 + RUN) of head h of sequence b, kv head kvh: its
+// records, written by CTAs c_first .. c_first + nseg - 1, and its group's
+// prefix state (a pre row has a record's layout).
+template <int D, int GQ, int RUN, int RB>
+__device__ __forceinline__ void merge_run(const DecodeParams &p, int b, int kvh, int64_t c_first,
+                                          int nseg, int h, int d0)
 {
     constexpr int REC = D + 2;
     const int u = (p.num_real + b) * p.n_kv + kvh;
-    const float *base = p.partials + ((size_t)c_first + u) * (GQ * REC) + h * REC;
     const int64_t row = ((int64_t)b * p.n_kv + kvh) * p.g + h;
-    float M = -INFINITY, pm = -INFINITY, pl = 0.f, po = 0.f;
-    if (__ldg(p.skip + b) > 0) {
-        const float *pr = p.pre + row * REC;
-        pm = __ldcg(pr);
-        pl = __ldcg(pr + 1);
-        po = __ldcg(pr + 2 + d);
-        M = pm;
-    }
-    for (int j = 0; j < nseg; ++j)
-        M = fmaxf(M, __ldcg(base + (size_t)j * GQ * REC));
-    float O = 0.f, L = 0.f;
-    if (M != -INFINITY) {
-        if (pm != -INFINITY) {
-            const float sc = fast_exp2(pm - M);
-            L = sc * pl;
-            O = sc * po;
-        }
-        for (int j = 0; j < nseg; ++j) {
-            const float *r = base + (size_t)j * GQ * REC;
-            const float m = __ldcg(r);
-            const float sc = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
-            L = fmaf(sc, __ldcg(r + 1), L);
-            O = fmaf(sc, __ldcg(r + 2 + d), O);
-        }
-    }
-    p.out[row * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    RunState<RUN> st;
+    st.clear();
+    if (__ldg(p.skip + b) > 0)
+        fold_rows<RUN, 1>(st, p.pre + row * REC, 0, 1, d0);
+    fold_rows<RUN, RB>(st, p.partials + ((size_t)c_first + u) * (GQ * REC) + h * REC,
+                       (size_t)GQ * REC, nseg, d0);
+#pragma unroll
+    for (int e = 0; e < RUN; e += 2)
+        *reinterpret_cast<__nv_bfloat162 *>(p.out + row * D + d0 + e) = __floats2bfloat162_rn(
+            st.L > 0.f ? st.O[e] / st.L : 0.f, st.L > 0.f ? st.O[e + 1] / st.L : 0.f);
 }
 
 // One arrival on sequence b's counter, which expects nseg arrivals (+1 for
@@ -747,12 +761,13 @@ __device__ __forceinline__ void arrive_sequences(const DecodeParams &p, const in
         ns[threadIdx.x] = nseg;
     }
     __syncthreads();
-    const int per = p.g * D;
+    using MR = MergeRun<D, GQ, NT>;
+    const int per = p.g * D / MR::RUN; // runs per sequence
 #pragma unroll 1
     for (int idx = threadIdx.x; idx < n * per; idx += NT) {
-        const int j = idx / per, r = idx - j * per;
+        const int j = idx / per, k = (idx - j * per) * MR::RUN;
         if (last[j])
-            merge_element<D, GQ>(p, b0 + j, kvh, cf[j], ns[j], r / D, r % D);
+            merge_run<D, GQ, MR::RUN, MR::RB>(p, b0 + j, kvh, cf[j], ns[j], k / D, k % D);
     }
     __syncthreads(); // misc is reused by the next segment
 }
@@ -771,10 +786,13 @@ __device__ __forceinline__ void finish_fused(const DecodeParams &p, const int32_
     const bool direct = whole && !group && !member; // a plain sequence in one piece
     // live rows: a group's members' heads, else the sequence's g heads
     const int rows = group ? __ldg(p.groups + 3 * s + 1) * p.g : p.g;
-    // warps' states -> this CTA's state of the unit: output or record
+    // warps' states -> this CTA's state of the unit: output or record, a run
+    // of RUN adjacent d of one row per thread
+    using MR = MergeRun<D, GQ, NT>;
+    constexpr int RUN = MR::RUN;
 #pragma unroll 1
-    for (int idx = threadIdx.x; idx < rows * D; idx += NT) {
-        const int h = idx / D, d = idx - h * D;
+    for (int idx = threadIdx.x; idx < rows * (D / RUN); idx += NT) {
+        const int h = idx * RUN / D, d0 = idx * RUN - h * D;
         float mw[NW];
         float M = -INFINITY;
 #pragma unroll
@@ -782,24 +800,38 @@ __device__ __forceinline__ void finish_fused(const DecodeParams &p, const int32_
             mw[w] = merge[(w * GQ + h) * REC];
             M = fmaxf(M, mw[w]);
         }
-        float O = 0.f, L = 0.f;
+        float O[RUN], L = 0.f;
+#pragma unroll
+        for (int e = 0; e < RUN; ++e)
+            O[e] = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
+                const float *mrow = merge + (w * GQ + h) * REC;
                 const float sc = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
-                L = fmaf(sc, merge[(w * GQ + h) * REC + 1], L);
-                O = fmaf(sc, merge[(w * GQ + h) * REC + 2 + d], O);
+                L = fmaf(sc, mrow[1], L);
+#pragma unroll
+                for (int e = 0; e < RUN; e += 2) {
+                    const float2 a = *reinterpret_cast<const float2 *>(mrow + 2 + d0 + e);
+                    O[e] = fmaf(sc, a.x, O[e]);
+                    O[e + 1] = fmaf(sc, a.y, O[e + 1]);
+                }
             }
         }
         if (direct) {
-            p.out[(((int64_t)b * p.n_kv + kvh) * p.g + h) * D + d] =
-                __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+            __nv_bfloat16 *o = p.out + (((int64_t)b * p.n_kv + kvh) * p.g + h) * D + d0;
+#pragma unroll
+            for (int e = 0; e < RUN; e += 2)
+                *reinterpret_cast<__nv_bfloat162 *>(o + e) = __floats2bfloat162_rn(
+                    L > 0.f ? O[e] / L : 0.f, L > 0.f ? O[e + 1] / L : 0.f);
         } else {
-            if (d == 0) {
+            if (d0 == 0) {
                 rec[h * REC] = M;
                 rec[h * REC + 1] = L;
             }
-            rec[h * REC + 2 + d] = O;
+#pragma unroll
+            for (int e = 0; e < RUN; e += 2)
+                *reinterpret_cast<float2 *>(rec + h * REC + 2 + d0 + e) = make_float2(O[e], O[e + 1]);
         }
     }
     __syncthreads();
@@ -833,28 +865,20 @@ __device__ __forceinline__ void finish_fused(const DecodeParams &p, const int32_
     const int b0 = __ldg(p.groups + 3 * s), n = __ldg(p.groups + 3 * s + 1);
     const float *base = p.partials + ((size_t)c_first + u) * (GQ * REC);
 #pragma unroll 1
-    for (int idx = threadIdx.x; idx < n * p.g * D; idx += NT) {
-        const int h = idx / D, d = idx - h * D;
+    for (int idx = threadIdx.x; idx < n * p.g * (D / RUN); idx += NT) {
+        const int h = idx * RUN / D, d0 = idx * RUN - h * D;
         const int j = h / p.g;
-        float M = -INFINITY;
-        for (int k = 0; k < nseg; ++k)
-            M = fmaxf(M, __ldcg(base + (size_t)k * GQ * REC + h * REC));
-        float O = 0.f, L = 0.f;
-        if (M != -INFINITY) {
-            for (int k = 0; k < nseg; ++k) {
-                const float *r = base + (size_t)k * GQ * REC + h * REC;
-                const float m = __ldcg(r);
-                const float sc = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
-                L = fmaf(sc, __ldcg(r + 1), L);
-                O = fmaf(sc, __ldcg(r + 2 + d), O);
-            }
-        }
+        RunState<RUN> st;
+        st.clear();
+        fold_rows<RUN, MR::RB>(st, base + h * REC, (size_t)GQ * REC, nseg, d0);
         float *pr = p.pre + (((int64_t)(b0 + j) * p.n_kv + kvh) * p.g + (h - j * p.g)) * REC;
-        if (d == 0) {
-            pr[0] = M;
-            pr[1] = L;
+        if (d0 == 0) {
+            pr[0] = st.M;
+            pr[1] = st.L;
         }
-        pr[2 + d] = O;
+#pragma unroll
+        for (int e = 0; e < RUN; e += 2)
+            *reinterpret_cast<float2 *>(pr + 2 + d0 + e) = make_float2(st.O[e], st.O[e + 1]);
     }
     __syncthreads(); // the pre rows are written (released by the arrivals below)
     arrive_sequences<D, GQ, NW>(p, P, misc, b0, n, kvh, Wv, G);
