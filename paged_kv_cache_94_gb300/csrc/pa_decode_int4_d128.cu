@@ -19,7 +19,7 @@
 #define PA_INT4_D128_BPI 2 // blocks per ring item
 #endif
 #ifndef PA_INT4_D128_STAGES
-#define PA_INT4_D128_STAGES 3
+#define PA_INT4_D128_STAGES 2
 #endif
 
 // The shared-prefix kernel keeps a GQ = g * members merge area per warp, so

@@ -22,10 +22,11 @@
 #define PA_INT8_D128_STAGES 2
 #endif
 
-// The shared-prefix kernel keeps a GQ = g * members merge area per warp, so
-// its ring uses one-block items to leave room for the same CTAs per SM.
+// The shared-prefix kernel keeps a GQ = g * members merge area per warp;
+// with two-block items and two stages (~86 KB per CTA) two CTAs fit per SM,
+// which measured faster than one-block items at three stages and three CTAs.
 #ifndef PA_INT8_D128_SHARE_BPI
-#define PA_INT8_D128_SHARE_BPI 1
+#define PA_INT8_D128_SHARE_BPI 2
 #endif
 #ifndef PA_INT8_D128_SHARE_NW
 #define PA_INT8_D128_SHARE_NW PA_INT8_D128_NW
@@ -34,7 +35,7 @@
 #define PA_INT8_D128_SHARE_MINB PA_INT8_D128_MINB
 #endif
 #ifndef PA_INT8_D128_SHARE_STAGES
-#define PA_INT8_D128_SHARE_STAGES 3
+#define PA_INT8_D128_SHARE_STAGES 2
 #endif
 
 namespace pa {
