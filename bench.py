@@ -116,6 +116,9 @@ def parse_args():
                          "allocator: the host block manager; read_probe: plain reads of the "
                          "decode's K/V blocks (the access pattern's ceiling)")
     ap.add_argument("--pairs", type=int, default=4096, help="block pairs per pa_block_copy")
+    ap.add_argument("--shuffle", action="store_true",
+                    help="decode the batch's sequences in a seeded random order (sharers of a "
+                         "prefix are then spread over the batch)")
     ap.add_argument("--no-share", action="store_true",
                     help="decode shared-prefix workloads without the shared-prefix passes")
     return ap.parse_args()
@@ -414,10 +417,14 @@ def run_native(args, rank, world, local_rank):
     slots_new = torch.from_numpy(w.new_token_slots()).to(dev)
     bt = torch.from_numpy(w.block_tables).to(dev)
     cl = torch.from_numpy(w.context_lens).to(dev)
+    if args.shuffle:  # the decode's rows in another order (the cache append is order-free)
+        perm = torch.from_numpy(np.random.default_rng(7).permutation(w.B)).to(dev)
+        q, bt, cl = q[perm].contiguous(), bt[perm].contiguous(), cl[perm].contiguous()
     out = torch.empty_like(q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     # sequences sharing prefix blocks (prefix caching): attend those blocks once per group
     share = bool((w.group >= 0).any()) and not args.no_share
+    share_mode = (2 if args.shuffle else 1) if share else 0  # 2: sharers anywhere in the batch
     ws = pa.decode_workspace(pa.geometry(kc, g.n_h), w.B, dev, args.num_ctas, n_q=w.n_q,
                              share_prefix=share)
     flush = L2Flush(dev)
@@ -430,7 +437,7 @@ def run_native(args, rank, world, local_rank):
                                    dev_status=status, k_scale=ks, v_scale=vs, prepare=prepare)
         return pa.pa_decode(q_, kc, vc, bt_, cl_, w.scale, out=o, k_scale=ks, v_scale=vs,
                             workspace=ws, dev_status=status, num_ctas=args.num_ctas,
-                            window=w.window, share_prefix=share, prepare=prepare)
+                            window=w.window, share_prefix=share_mode, prepare=prepare)
 
     def step():
         pa.pa_cache_write(kn, vn, slots_new, kc, vc, ks, vs, dev_status=status)
@@ -487,7 +494,7 @@ def run_native(args, rank, world, local_rank):
                    "context_tokens": int(w.context_lens.sum()),
                    "l2": L2_NOTE + f"; KV working set {db['bytes'] / 1e6:.0f} MB > 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "shared_prefix_passes": share},
+                   "shared_prefix_passes": share, "shuffled": bool(args.shuffle)},
         "seqs_per_s": round(world * w.B / (ms_per_step * 1e-3), 1),
         "decode_ms": round(dec_avg, 5), "cache_write_ms": round(statistics.mean(write_ms), 5),
         "bytes_per_step": step_bytes, "logical_kv_bytes": db["logical_bytes"],

@@ -233,20 +233,24 @@ pa_status pa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
  *             2-byte aligned), required when n_sink > 0, else NULL.
  *             pa_sink_write fills them.
  *   num_ctas  > 0: the CTA count as in pa_decode_ex; 0: the default.
- *   share_prefix  1: sequences whose block tables start with the same
+ *   share_prefix  1 or 2: sequences whose block tables start with the same
  *             physical blocks (prefix caching, [F] "Prefix Caching 与
  *             Copy-on-Write") have those blocks attended once per group: a
- *             first kernel finds runs of adjacent sequences sharing >= 8
- *             leading full blocks (groups of at most 8 sequences for g <= 2,
- *             16/g otherwise); a second kernel attends each group's shared
+ *             first kernel cuts runs of neighbouring sequences sharing >= 8
+ *             leading full blocks into groups (of at most 8 sequences for
+ *             g <= 2, 16/g otherwise), neighbours in the batch's order (1:
+ *             sharers must be adjacent) or, with 2, in an order by a hash
+ *             of each sequence's first 8 table entries (sharers anywhere in
+ *             the batch; the sort costs a few microseconds more); a second
+ *             kernel attends each group's shared
  *             blocks once with all the group's query rows and, in the same
  *             launch, each sequence's remaining blocks, and the last piece of
  *             a sequence to finish merges the softmax states (log-sum-exp).
  *             The result equals pa_decode's up to rounding. A batch whose
  *             2 * num_seqs units' tables do not fit the kernel's shared
  *             memory (thousands of sequences at d_h 128) is decoded without
- *             sharing, with the same result. Sharers must be adjacent in the batch. Not with a
- *             window or sink rows; g <= 8. The workspace is
+ *             sharing, with the same result. Not with a window or sink rows;
+ *             g <= 8. The workspace is
  *             pa_decode_opt_workspace_size(geom, num_seqs, opts).
  */
 typedef struct pa_decode_opts {
@@ -255,12 +259,37 @@ typedef struct pa_decode_opts {
     const void *sink_k;
     const void *sink_v;
     int32_t num_ctas;
-    int32_t share_prefix; /* 1: attend shared prefixes once per group (below) */
+    int32_t share_prefix; /* 1, 2: attend shared prefixes once per group (below) */
     int32_t reserved;     /* must be 0 */
 } pa_decode_opts;
 
 /* Workspace bytes pa_decode_opt needs for these options (0 if invalid). */
 size_t pa_decode_opt_workspace_size(pa_geom geom, int32_t num_seqs, const pa_decode_opts *opts);
+
+/*
+ * The shared-prefix groups of a batch, as pa_decode_opt with share_prefix
+ * finds them (its first kernel), written to the caller's device buffers:
+ *   skip    int32 [num_seqs]: leading blocks sequence b's group shares, 0 if
+ *           b is in no group;
+ *   groups  int32 [3 * num_seqs]: for groups s = 0 .. NG-1 (first, members,
+ *           shared blocks), then zeros;
+ *   order   int32 [num_seqs]: the order the groups are cut in (mode 1: the
+ *           batch's own; mode 2: by a hash of each sequence's first 8 table
+ *           entries, ties by index); member j of group s is sequence
+ *           order[first + j].
+ * g is the query heads per kv head (1, 2, 4 or 8): groups hold at most 8
+ * sequences for g <= 2, 16/g otherwise. block_tables and context_lens are as
+ * for pa_decode; mode is pa_decode_opts.share_prefix (1 or 2).
+ * Asynchronous on `stream`; num_seqs == 0 does nothing.
+ * Errors: PA_ERR_SHAPE (num_seqs outside 0..8192, max_blocks_per_seq <= 0,
+ * another mode),
+ * PA_ERR_UNSUPPORTED (other g), PA_ERR_NULL, PA_ERR_CUDA. The pages have no
+ * counterpart: it exposes the grouping the shared-prefix decode uses.
+ */
+pa_status pa_share_groups(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *context_lens, int32_t num_seqs, int32_t g,
+                          int32_t mode, int32_t *skip, int32_t *groups, int32_t *order,
+                          void *stream);
 
 /* pa_decode with options (opts may be NULL: plain pa_decode). Extra
  * errors: PA_ERR_SHAPE for window < 0, n_sink outside 0..16, n_sink > 0 on

@@ -46,7 +46,7 @@ EXPORTED = ["pa_cache_write", "pa_decode_workspace_size", "pa_decode_workspace_i
             "pa_plan_owner", "pa_block_copy", "pa_decode_opt", "pa_sink_write",
             "pa_decode_mq", "pa_decode_mq_ex", "pa_decode_mq_workspace_size", "pa_decode_opt_workspace_size",
             "pa_status_string", "pa_status_from_device", "pa_version", "pa_wait_selftest",
-            "pa_kv_read_probe",
+            "pa_kv_read_probe", "pa_share_groups",
             # host block manager (include/pa_alloc.h)
             "pa_allocator_create", "pa_allocator_destroy", "pa_allocator_allocate_prompt",
             "pa_allocator_append_slots", "pa_allocator_fork", "pa_allocator_free",
@@ -134,6 +134,8 @@ def _lib():
         lib.pa_sink_write.argtypes = [P, P, P, P, i64, P, P, i32, i32, pa_geom, P]
         lib.pa_kv_read_probe.restype = ctypes.c_int
         lib.pa_kv_read_probe.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, P, pa_geom, P]
+        lib.pa_share_groups.restype = ctypes.c_int
+        lib.pa_share_groups.argtypes = [P, i32, P, i32, i32, i32, P, P, P, P]
         lib.pa_block_copy.restype = ctypes.c_int
         lib.pa_block_copy.argtypes = [P, P, P, P, P, i32, pa_geom, P, P]
         u64 = ctypes.c_uint64
@@ -330,7 +332,7 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
               v_scale: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
               dev_status: Optional[torch.Tensor] = None, stream=None, num_ctas: int = 0,
               window: int = 0, sink_k: Optional[torch.Tensor] = None,
-              sink_v: Optional[torch.Tensor] = None, share_prefix: bool = False,
+              sink_v: Optional[torch.Tensor] = None, share_prefix: int = 0,
               prepare: bool = False):
     """Decode attention: q [B, n_h, d_h] bf16 over the paged pool -> out [B, n_h, d_h] bf16.
 
@@ -338,8 +340,9 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     num_ctas > 0 forces the number of CTAs the work is split over (pa_decode_ex).
     window > 0 attends the last `window` tokens of each sequence; sink_k/sink_v
     (bf16 [B, n_kv, n_sink, d_h], INT8 pools) hold the unquantised rows of the
-    first n_sink positions (pa_decode_opt). share_prefix attends blocks that
-    adjacent sequences share once per group (pa_decode_opt, share_prefix).
+    first n_sink positions (pa_decode_opt). share_prefix (True or 1: sharers
+    adjacent in the batch; 2: anywhere) attends blocks that sequences share
+    once per group (pa_decode_opt, share_prefix).
     prepare=True validates and returns a Prepared call instead of running it.
     """
     _need_cuda("q", q, torch.bfloat16)
@@ -387,7 +390,7 @@ def pa_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                 raise ValueError("sink_k, sink_v must be [num_seqs, n_kv, n_sink, d_h]")
         opts = pa_decode_opts(window=int(window), n_sink=n_sink, sink_k=_ptr(sink_k),
                               sink_v=_ptr(sink_v), num_ctas=int(num_ctas),
-                              share_prefix=1 if share_prefix else 0, reserved=0)
+                              share_prefix=int(share_prefix), reserved=0)
         call = Prepared(lib.pa_decode_opt, args[:14] + [ctypes.byref(opts)] + args[14:], 16,
                         "pa_decode", out, stream)
     elif num_ctas > 0:
@@ -495,6 +498,26 @@ def pa_kv_read_probe(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables:
                                    context_lens.shape[0], int(heads_per_read), int(num_ctas),
                                    _ptr(sink), g, ctypes.c_void_p(s.cuda_stream)),
            "pa_kv_read_probe")
+
+
+def pa_share_groups(block_tables: torch.Tensor, context_lens: torch.Tensor, g: int,
+                    mode: int = 1, stream=None):
+    """The shared-prefix groups of a batch, as pa_decode's share_prefix=mode
+    finds them: (skip [B], groups [B, 3] = (first, members, shared blocks) per
+    group then zeros, order [B]); member j of group s is
+    order[groups[s, 0] + j]. int32 device tensors."""
+    _need_cuda("block_tables", block_tables, torch.int32)
+    _need_cuda("context_lens", context_lens, torch.int32)
+    B = context_lens.shape[0]
+    dev = block_tables.device
+    skip = torch.zeros(B, dtype=torch.int32, device=dev)
+    groups = torch.zeros(B, 3, dtype=torch.int32, device=dev)
+    order = torch.zeros(B, dtype=torch.int32, device=dev)
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    _check(_lib().pa_share_groups(_ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B,
+                                  int(g), int(mode), _ptr(skip), _ptr(groups), _ptr(order),
+                                  ctypes.c_void_p(s.cuda_stream)), "pa_share_groups")
+    return skip, groups, order
 
 
 def pa_decode_default_ctas(k_cache: torch.Tensor, n_h: int, num_seqs: int) -> int:

@@ -169,9 +169,9 @@ size_t workspace_bytes_for(const pa_geom &g, int num_seqs, int grid, int nq = 1)
 // B sequences' remaining blocks). Workspace:
 //   counters  [2B * n_kv] int32 (zero on entry and on exit)
 //   records   (grid + 2B * n_kv) x (g * members) x (d_h + 2) fp32
-//   skip[B], groups[3B] int32, pre[B][n_h][d_h + 2] fp32
+//   skip[B], groups[3B], order[B] int32, pre[B][n_h][d_h + 2] fp32
 struct ShareLayout {
-    size_t zero_end, records, skip, groups, pre, end;
+    size_t zero_end, records, skip, groups, order, pre, end;
 };
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
@@ -201,7 +201,8 @@ ShareLayout share_layout(const pa_geom &g, int num_seqs, int grid)
     const size_t rec = (size_t)group_of(g) * pa::kShareMembers(group_of(g)) * (g.d_h + 2) * 4;
     L.skip = round256(L.records + (grid + units2) * rec);
     L.groups = L.skip + round256(4 * (size_t)num_seqs);
-    L.pre = L.groups + round256(12 * (size_t)num_seqs);
+    L.order = L.groups + round256(12 * (size_t)num_seqs);
+    L.pre = L.order + round256(4 * (size_t)num_seqs);
     L.end = L.pre + (size_t)num_seqs * g.n_h * (g.d_h + 2) * 4;
     return L;
 }
@@ -305,9 +306,9 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     const pa_decode_opts none = {0, 0, nullptr, nullptr, 0, 0, 0};
     const pa_decode_opts &o = opts ? *opts : none;
     if (o.window < 0 || o.n_sink < 0 || o.n_sink > 16 || o.reserved != 0 ||
-        (o.share_prefix != 0 && o.share_prefix != 1))
+        (o.share_prefix < 0 || o.share_prefix > 2))
         return PA_ERR_SHAPE;
-    bool share = o.share_prefix == 1;
+    bool share = o.share_prefix != 0;
     if (share && (nq != 1 || o.window != 0 || o.n_sink != 0 || group_of(g) > 8))
         return PA_ERR_UNSUPPORTED;
     if (o.n_sink > 0) {
@@ -395,20 +396,22 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     p.skip = nullptr;
     p.pre = nullptr;
     p.groups = nullptr;
+    p.members = nullptr;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     p.num_real = num_seqs;
     p.grid_fixed = num_ctas > 0 ? 1 : 0;
     if (share) {
-        // 1) groups of adjacent sequences sharing leading blocks; 2) one
+        // 1) groups of sequences sharing leading blocks; 2) one
         //    launch over the group units, then every sequence's remaining
         //    blocks; the last arrival on each sequence merges its records and
         //    its group's prefix state
         uint8_t *ws = static_cast<uint8_t *>(workspace);
         int32_t *skip = reinterpret_cast<int32_t *>(ws + SL.skip);
         int32_t *groups = reinterpret_cast<int32_t *>(ws + SL.groups);
+        int32_t *order = reinterpret_cast<int32_t *>(ws + SL.order);
         cudaError_t e = pa::launch_share_detect(block_tables, max_blocks, context_lens, num_seqs,
                                                 pa::kShareMembers(p.g), pa::kShareMinBlocks, skip,
-                                                groups, cs);
+                                                groups, order, o.share_prefix == 2, cs);
         if (e != cudaSuccess)
             return PA_ERR_CUDA;
         p.num_seqs = 2 * num_seqs;
@@ -419,6 +422,7 @@ pa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
         p.partials = reinterpret_cast<float *>(ws + SL.records);
         p.skip = skip;
         p.groups = groups;
+        p.members = order;
         p.pre = reinterpret_cast<float *>(ws + SL.pre);
         p.num_ctas = grid;
         return kp->launch(tk, tv, p, grid, smem_sh, cs) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -703,6 +707,27 @@ pa_status pa_sink_write(const void *k, const void *v, const int32_t *seq_rows,
         k, v, seq_rows, positions, num_tokens, geom.n_kv, geom.d_h, n_sink, num_seqs, sink_k,
         sink_v, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_share_groups(const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *context_lens, int32_t num_seqs, int32_t g,
+                          int32_t mode, int32_t *skip, int32_t *groups, int32_t *order,
+                          void *stream)
+{
+    if (num_seqs < 0 || num_seqs > kMaxSeqs || max_blocks_per_seq <= 0 || mode < 1 || mode > 2)
+        return PA_ERR_SHAPE;
+    if (g != 1 && g != 2 && g != 4 && g != 8)
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!block_tables || !context_lens || !skip || !groups || !order)
+        return PA_ERR_NULL;
+    return pa::launch_share_detect(block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                   pa::kShareMembers(g), pa::kShareMinBlocks, skip, groups,
+                                   order, mode == 2, static_cast<cudaStream_t>(stream)) ==
+                       cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 int32_t pa_decode_default_ctas(pa_geom geom, int32_t num_seqs)

@@ -76,13 +76,16 @@ struct DecodeParams {
     int32_t seg_cost_lead;       // ... per unit of the first lead_units "sequences"
     int32_t lead_units;          //     (the group units of the shared-prefix launch)
     // Shared prefixes (PASS 2, see pa_share.cu): the line holds num_real
-    // group units first, group s = groups[3s..3s+2] = (first member, members,
-    // shared blocks), whose query rows are the g heads of each member; then
-    // the num_real sequences' blocks after their first skip[b]. A group's
-    // softmax state of each member's head h goes to pre[b][h] = (m, l, acc[D]).
+    // group units first, group s = groups[3s..3s+2] = (position of its first
+    // member in members, members, shared blocks), member j being sequence
+    // members[groups[3s] + j], whose query rows are the g heads of each
+    // member; then the num_real sequences' blocks after their first skip[b].
+    // A group's softmax state of each member's head h goes to pre[b][h] =
+    // (m, l, acc[D]).
     const int32_t *skip;
     float *pre;
     const int32_t *groups;
+    const int32_t *members;
     int32_t num_real;
     int32_t grid_fixed;          // 1: the caller chose num_ctas (no whole-unit grid)
 };
@@ -93,7 +96,7 @@ template <int PASS>
 __device__ __forceinline__ int32_t seq_table_row(const DecodeParams &p, int s)
 {
     if constexpr (PASS == 2)
-        return s < p.num_real ? __ldg(p.groups + 3 * s) : s - p.num_real;
+        return s < p.num_real ? __ldg(p.members + __ldg(p.groups + 3 * s)) : s - p.num_real;
     else
         return s;
 }
@@ -493,7 +496,7 @@ __device__ __forceinline__ int64_t unit_row(const DecodeParams &p, int s, int kv
         const int j = v / p.g, h = v - j * p.g;
         if (j >= __ldg(p.groups + 3 * s + 1))
             return -1;
-        const int b = __ldg(p.groups + 3 * s) + j;
+        const int b = __ldg(p.members + __ldg(p.groups + 3 * s) + j);
         return ((int64_t)b * p.n_kv + kvh) * p.g + h;
     } else {
         return (int64_t)qo_row<GQ, NQ>(p, s, kvh, v);
@@ -741,24 +744,26 @@ __device__ __forceinline__ bool arrive_one(const DecodeParams &p, const int32_t 
     return last;
 }
 
-// Arrivals of sequences b0 .. b0 + n - 1 (n <= 8), one thread each, then the
-// merges of those that arrived last, all threads together. Called by all
-// threads; the records and pre rows this CTA wrote are published by the
-// barrier before the release of each arrival.
+// Arrivals of sequences map[b0 .. b0 + n - 1] (n <= 8; map NULL: b0 .. b0 +
+// n - 1), one thread each, then the merges of those that arrived last, all
+// threads together. Called by all threads; the records and pre rows this
+// CTA wrote are published by the barrier before the release of each arrival.
 template <int D, int GQ, int NW>
 __device__ __forceinline__ void arrive_sequences(const DecodeParams &p, const int32_t *P,
-                                                 int32_t *misc, int b0, int n, int kvh,
-                                                 int64_t Wv, int64_t G)
+                                                 int32_t *misc, const int32_t *map, int b0, int n,
+                                                 int kvh, int64_t Wv, int64_t G)
 {
     constexpr int NT = NW * 32;
-    int32_t *last = misc, *cf = misc + 8, *ns = misc + 16;
+    int32_t *last = misc, *cf = misc + 8, *ns = misc + 16, *seq = misc + 24;
     if (threadIdx.x < n) {
         int64_t c_first;
         int nseg;
-        const bool l = arrive_one(p, P, b0 + threadIdx.x, kvh, Wv, G, c_first, nseg);
+        const int b = map ? __ldg(map + b0 + threadIdx.x) : b0 + (int)threadIdx.x;
+        const bool l = arrive_one(p, P, b, kvh, Wv, G, c_first, nseg);
         last[threadIdx.x] = l;
         cf[threadIdx.x] = (int32_t)c_first;
         ns[threadIdx.x] = nseg;
+        seq[threadIdx.x] = b;
     }
     __syncthreads();
     using MR = MergeRun<D, GQ, NT>;
@@ -767,7 +772,7 @@ __device__ __forceinline__ void arrive_sequences(const DecodeParams &p, const in
     for (int idx = threadIdx.x; idx < n * per; idx += NT) {
         const int j = idx / per, k = (idx - j * per) * MR::RUN;
         if (last[j])
-            merge_run<D, GQ, MR::RUN, MR::RB>(p, b0 + j, kvh, cf[j], ns[j], k / D, k % D);
+            merge_run<D, GQ, MR::RUN, MR::RB>(p, seq[j], kvh, cf[j], ns[j], k / D, k % D);
     }
     __syncthreads(); // misc is reused by the next segment
 }
@@ -838,7 +843,7 @@ __device__ __forceinline__ void finish_fused(const DecodeParams &p, const int32_
     if (direct)
         return;
     if (!group) { // a piece of sequence b: one arrival
-        arrive_sequences<D, GQ, NW>(p, P, misc, b, 1, kvh, Wv, G);
+        arrive_sequences<D, GQ, NW>(p, P, misc, nullptr, b, 1, kvh, Wv, G);
         return;
     }
     // a piece of group s: the last one merges the group's state into pre and
@@ -871,7 +876,8 @@ __device__ __forceinline__ void finish_fused(const DecodeParams &p, const int32_
         RunState<RUN> st;
         st.clear();
         fold_rows<RUN, MR::RB>(st, base + h * REC, (size_t)GQ * REC, nseg, d0);
-        float *pr = p.pre + (((int64_t)(b0 + j) * p.n_kv + kvh) * p.g + (h - j * p.g)) * REC;
+        const int bj = __ldg(p.members + b0 + j);
+        float *pr = p.pre + (((int64_t)bj * p.n_kv + kvh) * p.g + (h - j * p.g)) * REC;
         if (d0 == 0) {
             pr[0] = st.M;
             pr[1] = st.L;
@@ -881,7 +887,7 @@ __device__ __forceinline__ void finish_fused(const DecodeParams &p, const int32_
             *reinterpret_cast<float2 *>(pr + 2 + d0 + e) = make_float2(st.O[e], st.O[e + 1]);
     }
     __syncthreads(); // the pre rows are written (released by the arrivals below)
-    arrive_sequences<D, GQ, NW>(p, P, misc, b0, n, kvh, Wv, G);
+    arrive_sequences<D, GQ, NW>(p, P, misc, p.members, b0, n, kvh, Wv, G);
 }
 
 // Byte offset of 16-byte chunk `c` of row `r` in a TMA-swizzled tile whose

@@ -48,7 +48,8 @@ const DecodeKernel *find_prefix_kernel(int kv_dtype, int d_h, int group);
 cudaError_t launch_wait_selftest(int32_t *dev_status, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_share_detect(const int32_t *block_tables, int max_blocks,
                                 const int32_t *context_lens, int B, int gm, int min_blocks,
-                                int32_t *skip, int32_t *groups, cudaStream_t stream);
+                                int32_t *skip, int32_t *groups, int32_t *order, bool sort,
+                                cudaStream_t stream);
 
 // Multi-query (nq new tokens per sequence) bf16 kernels; NULL when not compiled.
 const DecodeKernel *find_decode_kernel_bf16_mq(int d_h, int group, int nq);

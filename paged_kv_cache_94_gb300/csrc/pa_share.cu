@@ -7,24 +7,37 @@
 // reader attending it (softmax states merge exactly by log-sum-exp), with the
 // readers' query rows filling the tensor cores' N side.
 //
-// This kernel finds the sharing from the block tables alone. For each
-// sequence b > 0, lcp[b] = the number of leading block-table entries equal to
-// those of sequence b - 1, among blocks both sequences fill completely and
-// excluding each sequence's last block (so every sequence keeps at least one
-// block for the decode pass). Runs of consecutive sequences with lcp >=
-// min_blocks are cut into groups of at most gm members; a group shares
-// S = the minimum lcp over its members after the first. Output:
+// This kernel finds the sharing from the block tables alone. With `sort`,
+// the sequences are first ordered by a hash of their first min_blocks table
+// entries (a sequence with fewer full blocks sorts last), ties by index, so
+// that sequences sharing a prefix become neighbours wherever they sit in the
+// batch; without it the order is the batch's own (sharers must then be
+// adjacent). order[i] is the i-th sequence of that order. For each position
+// i > 0, lcp[i] = the number of leading block-table entries of order[i]
+// equal to those of order[i - 1], among blocks both sequences fill
+// completely and excluding each sequence's last block (so every sequence
+// keeps at least one block for the decode pass). Runs of neighbours with
+// lcp >= min_blocks are cut into groups of at most gm members; a group
+// shares S = the minimum lcp over its members after the first. Output:
 //   skip[b]        S of b's group (0 if b is in no group of >= 2 members)
-//   groups[3 s..]  (first member, members, S) for groups s = 0 .. NG-1, then
-//                  (0, 0, 0) up to s = B-1
+//   groups[3 s..]  (position of the first member in order, members, S) for
+//                  groups s = 0 .. NG-1, then (0, 0, 0) up to s = B-1
+//   order[i]       the sequences in that order: member j of group s is
+//                  order[groups[3 s] + j]
 // One CTA of 1024 threads; B <= 8192.
+#include <atomic>
+
 #include "pa_internal.h"
 
 namespace pa {
 namespace {
 
+constexpr int kMaxDevices = 64;
 constexpr int kThreads = 1024;
 constexpr int kMaxPer = 8; // sequences per thread at most (B <= 8192)
+constexpr int kMaxSeqs = kThreads * kMaxPer;
+// dynamic shared memory: the sort keys (one 64-bit key per power-of-two slot)
+constexpr size_t kSortBytes = (size_t)kMaxSeqs * 8;
 
 __device__ __forceinline__ int32_t blocks_of(int32_t ctx, int32_t max_blocks)
 {
@@ -76,30 +89,92 @@ __device__ __forceinline__ void block_scan(int32_t (&v)[kPer], int32_t *wsum)
 }
 
 // kPer sequences per thread: 1 up to 1024 sequences, else 8.
+// Hash of the first N table entries of a row (FNV-1a over the entries; the
+// N loads are issued together).
+template <int N>
+__device__ __forceinline__ uint32_t prefix_hash(const int32_t *row)
+{
+    int32_t e[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        e[i] = __ldg(row + i);
+    uint32_t h = 2166136261u;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        h ^= (uint32_t)e[i];
+        h *= 16777619u;
+    }
+    return h;
+}
+
 template <int kPer>
 __global__ void __launch_bounds__(kThreads)
     share_detect_kernel(const int32_t *__restrict__ block_tables, int max_blocks,
                         const int32_t *__restrict__ context_lens, int B, int gm, int min_blocks,
-                        int32_t *skip, int32_t *groups)
+                        int32_t *skip, int32_t *groups, int32_t *order_out, bool sort)
 {
-    __shared__ int32_t lcp[kThreads * kPer];
+    extern __shared__ uint64_t key[]; // [N]: (hash << 32 | index), then lcp
+    __shared__ int32_t ord[kThreads * kPer];
     __shared__ int32_t wsum[32];
+    int32_t *lcp = reinterpret_cast<int32_t *>(key); // reuses the keys once sorted
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // the decode launch that reads these results may be scheduled now; it
     // waits for this grid to complete before its first read
     asm volatile("griddepcontrol.launch_dependents;");
 
-    // ---- lcp with the previous sequence: one warp per sequence; each round
-    // compares 256 entries with all loads in flight at once
+    // ---- order: bitonic sort of N = 2^k >= B keys (padding sorts last), or
+    // the batch's order
+    int N = 1;
+    while (N < B)
+        N <<= 1;
+    if (!sort)
+        N = 0;
+    for (int i = tid; i < N; i += kThreads) {
+        uint64_t k = ~0ull;
+        if (i < B) {
+            const int32_t nb = blocks_of(__ldg(context_lens + i), max_blocks);
+            const uint32_t h = nb > min_blocks
+                                   ? prefix_hash<kShareMinBlocks>(block_tables +
+                                                                  (size_t)i * max_blocks)
+                                   : 0xFFFFFFFFu;
+            k = ((uint64_t)h << 32) | (uint32_t)i;
+        }
+        key[i] = k;
+    }
+    __syncthreads();
+    for (int size = 2; size <= N; size <<= 1)
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = tid; t < N / 2; t += kThreads) {
+                const int i = 2 * t - (t & (stride - 1)); // lower index of the pair
+                const int j = i + stride;
+                const bool up = (i & size) == 0;
+                const uint64_t a = key[i], c = key[j];
+                if ((a > c) == up) {
+                    key[i] = c;
+                    key[j] = a;
+                }
+            }
+            __syncthreads();
+        }
+    for (int i = tid; i < B; i += kThreads) {
+        const int32_t b = sort ? (int32_t)(uint32_t)key[i] : i;
+        ord[i] = b;
+        order_out[i] = b;
+    }
+    __syncthreads();
+
+    // ---- lcp with the previous sequence in that order: one warp per
+    // position; each round compares 256 entries with all loads in flight
     constexpr int kRound = 8; // entries per lane per round
     for (int b = warp; b < B; b += kThreads / 32) {
         int32_t l = 0;
         if (b > 0) {
-            const int32_t nb0 = blocks_of(__ldg(context_lens + b - 1), max_blocks);
-            const int32_t nb1 = blocks_of(__ldg(context_lens + b), max_blocks);
+            const int32_t s0 = ord[b - 1], s1 = ord[b];
+            const int32_t nb0 = blocks_of(__ldg(context_lens + s0), max_blocks);
+            const int32_t nb1 = blocks_of(__ldg(context_lens + s1), max_blocks);
             const int32_t lim = max(0, min(nb0, nb1) - 1);
-            const int32_t *r0 = block_tables + (size_t)(b - 1) * max_blocks;
-            const int32_t *r1 = block_tables + (size_t)b * max_blocks;
+            const int32_t *r0 = block_tables + (size_t)s0 * max_blocks;
+            const int32_t *r1 = block_tables + (size_t)s1 * max_blocks;
             for (int i0 = 0; i0 < lim; i0 += 32 * kRound) {
                 int32_t a[kRound], c[kRound];
 #pragma unroll
@@ -153,7 +228,7 @@ __global__ void __launch_bounds__(kThreads)
             lead[i] = n >= 2 ? S : 0;
             cnt[i] = n;
             for (int j = 0; j < n; ++j)
-                skip[b + j] = n >= 2 ? S : 0;
+                skip[ord[b + j]] = n >= 2 ? S : 0;
         }
     }
     // ---- compact the groups of >= 2 members
@@ -186,16 +261,37 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_share_detect(const int32_t *block_tables, int max_blocks,
                                 const int32_t *context_lens, int B, int gm, int min_blocks,
-                                int32_t *skip, int32_t *groups, cudaStream_t stream)
+                                int32_t *skip, int32_t *groups, int32_t *order, bool sort,
+                                cudaStream_t stream)
 {
-    if (B < 1 || B > kThreads * kMaxPer || gm < 2)
+    if (B < 1 || B > kMaxSeqs || gm < 2 || min_blocks != kShareMinBlocks) // the hash's width
         return cudaErrorInvalidValue;
+    size_t N = 1;
+    while (N < (size_t)B)
+        N <<= 1;
+    const size_t smem = sort ? N * 8 : (size_t)B * 4; // keys, then lcp
+    // the opt-in above 48 KiB of shared memory, once per device
+    static std::atomic<bool> raised[kMaxDevices];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    if (!raised[dev].load()) {
+        if (cudaFuncSetAttribute(share_detect_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSortBytes) != cudaSuccess ||
+            cudaFuncSetAttribute(share_detect_kernel<kMaxPer>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSortBytes) != cudaSuccess)
+            return cudaErrorInvalidValue;
+        raised[dev].store(true);
+    }
     if (B <= kThreads)
-        share_detect_kernel<1><<<1, kThreads, 0, stream>>>(block_tables, max_blocks, context_lens,
-                                                           B, gm, min_blocks, skip, groups);
+        share_detect_kernel<1><<<1, kThreads, smem, stream>>>(
+            block_tables, max_blocks, context_lens, B, gm, min_blocks, skip, groups, order,
+            sort);
     else
-        share_detect_kernel<kMaxPer><<<1, kThreads, 0, stream>>>(
-            block_tables, max_blocks, context_lens, B, gm, min_blocks, skip, groups);
+        share_detect_kernel<kMaxPer><<<1, kThreads, smem, stream>>>(
+            block_tables, max_blocks, context_lens, B, gm, min_blocks, skip, groups, order,
+            sort);
     return cudaGetLastError();
 }
 

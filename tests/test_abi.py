@@ -184,7 +184,8 @@ def test_decode_opt_argument_checks(lib):
     assert call(gi, n_sink=17, sink_k=256, sink_v=256) == -2
     assert call(gi, n_sink=4, sink_k=None, sink_v=256) == -1
     assert call(gi, n_sink=4, sink_k=257, sink_v=256) == -11
-    assert call(g, share_prefix=2) == -2
+    assert call(g, share_prefix=3) == -2 and call(g, share_prefix=-1) == -2
+    assert call(g, share_prefix=2) != -2                            # sharers anywhere: valid
     assert call(g, share_prefix=1, window=64) == -4                 # not with a window
     assert call(_geom(n_h=128, n_kv=8), share_prefix=1) == -4      # g = 16
 
@@ -211,3 +212,14 @@ def test_read_probe_argument_checks(lib):
     assert lib.pa_kv_read_probe(*args(grid=0)) == -2
     assert lib.pa_kv_read_probe(*args(g=_geom(kv_dtype=1))) == -2   # INT8 pools read scales
     assert lib.pa_kv_read_probe(*args(g=_geom(d_h=96))) == -2
+
+
+def test_share_groups_argument_checks(lib):
+    fake = ctypes.c_void_p(256)
+    call = lambda B=4, mb=16, g=1, mode=1, bt=fake, cl=fake, out=fake: lib.pa_share_groups(
+        bt, mb, cl, B, g, mode, out, out, out, None)
+    assert call(B=0) == 0                      # nothing to do
+    assert call(B=-1) == -2 and call(B=8193) == -2 and call(mb=0) == -2
+    assert call(mode=0) == -2 and call(mode=3) == -2
+    assert call(g=3) == -4 and call(g=16) == -4
+    assert call(bt=None) == -1 and call(out=None) == -1

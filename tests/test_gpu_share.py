@@ -113,3 +113,93 @@ def test_shared_prefix_too_large_for_the_kernel_decodes_without_sharing():
     for s in (0, 4097, B - 1):
         ref, _ = oracle_one_sequence(w, s)
         assert_close(b[s], ref, f"seq {s}")
+
+
+def detected_groups(w, g, mode=2):
+    """(members, shared blocks) of every group pa_share_groups finds."""
+    skip, grp, order = pa.pa_share_groups(torch.from_numpy(w.block_tables).to(DEV),
+                                          torch.from_numpy(w.context_lens).to(DEV), g, mode)
+    torch.cuda.synchronize()
+    skip, grp, order = skip.cpu().numpy(), grp.cpu().numpy(), order.cpu().numpy()
+    assert sorted(order.tolist()) == list(range(w.B))
+    out = []
+    for first, n, shared in grp:
+        if n == 0:
+            break
+        members = tuple(int(b) for b in order[first:first + n])
+        assert all(skip[b] == shared for b in members)
+        out.append((members, int(shared)))
+    grouped_seqs = {b for m, _ in out for b in m}
+    assert all(skip[b] == 0 for b in range(w.B) if b not in grouped_seqs)
+    return out
+
+
+NON_ADJACENT = [
+    # (dtype, d_h, g, groups, prefix tokens, suffix tokens): members of a group
+    # are spread over the batch, interleaved with other groups and loners
+    ("bf16", 128, 4, [0, 1, 0, -1, 1, 0, 2, 1, 2], [256, 160, 256, 0, 160, 256, 512, 160, 512],
+     [5, 40, 300, 17, 1, 90, 16, 33, 7]),
+    ("int8", 128, 1, [0, 1] * 6, [400, 256] * 6, [3, 17, 50, 9, 100, 1, 64, 31, 7, 260, 44, 2]),
+    ("int4", 64, 2, [1, -1, 0, 1, 0, 1], [256, 0, 320, 256, 320, 256], [48, 1, 200, 16, 15, 100]),
+]
+
+
+@pytest.mark.parametrize("kv_dtype,d_h,g,groups,prefix,suffix", NON_ADJACENT)
+def test_shared_prefix_non_adjacent_members(kv_dtype, d_h, g, groups, prefix, suffix):
+    # share_prefix=2 finds sharers wherever they sit in the batch; the result
+    # equals the oracle's, and so does share_prefix=1's (which groups
+    # adjacent sharers only)
+    w = grouped(kv_dtype, d_h, g, groups, prefix, suffix, seed=83 + g + d_h)
+    pool = gpu_pool(w, DEV, fill_nan=True)
+    ref, _ = oracle_full(w)
+    plain, st0 = run(w, pool, share=False)
+    assert st0 == 0
+    out1, st1 = run(w, pool, share=1)
+    assert st1 == 0
+    assert_close(out1, ref, f"{kv_dtype} d{d_h} g{g} adjacent-only mode")
+    for num_ctas in (0, 1, 7, 200):
+        out, st = run(w, pool, share=2, num_ctas=num_ctas)
+        assert st == 0
+        assert_close(out, ref, f"{kv_dtype} d{d_h} g{g} ctas {num_ctas} (non-adjacent)")
+    assert np.abs(out - plain).max() < 2e-2
+    # the groups found are the workload's: members (by index) and shared blocks
+    found = detected_groups(w, g)
+    want = {}
+    for b, grp in enumerate(groups):
+        if grp >= 0:
+            want.setdefault(grp, []).append(b)
+    assert sorted(found) == sorted((tuple(m), prefix[m[0]] // 16) for m in want.values())
+
+
+def test_shared_prefix_full_size_int8_workload_shuffled():
+    # the LLaMA-2-7B INT8 workload with its 32 sequences in a seeded random
+    # order: the 4 groups of 8 are interleaved across the batch
+    w = named_workload("llama2_7b_int8_prefix")
+    pool = gpu_pool(w, DEV, gen_device=DEV)
+    perm = np.random.default_rng(5).permutation(w.B)
+    q = w.q(DEV)[torch.from_numpy(perm).to(DEV)]
+    bt = torch.from_numpy(np.ascontiguousarray(w.block_tables[perm])).to(DEV)
+    cl = torch.from_numpy(np.ascontiguousarray(w.context_lens[perm])).to(DEV)
+    kc, vc, ks, vs = pool
+    outs = []
+    for share in (True, False):
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        o = pa.pa_decode(q, kc, vc, bt, cl, w.scale, k_scale=ks, v_scale=vs, dev_status=status,
+                         share_prefix=2 if share else 0)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        outs.append(o.float().cpu().numpy())
+    out, plain = outs
+    assert np.isfinite(out).all()
+    assert np.abs(out - plain).max() < 2e-2
+    # the 4 groups of 8 are found in the shuffled batch, each sharing its 128
+    # prefix blocks
+    skip, grp, order = pa.pa_share_groups(bt, cl, 1, mode=2)
+    torch.cuda.synchronize()
+    grp, order = grp.cpu().numpy(), order.cpu().numpy()
+    found = sorted(sorted(int(perm[i]) for i in order[f:f + n]) for f, n, s_ in grp if n > 0)
+    want = sorted(sorted(np.nonzero(w.group == k)[0].tolist()) for k in range(4))
+    assert found == want and all(s_ == 128 for f, n, s_ in grp if n > 0)
+    for i in (0, 9, 22, w.B - 1):
+        ref, _ = oracle_one_sequence(w, int(perm[i]), gen_device=DEV)
+        assert_close(out[i], ref, f"int8 prefix shuffled position {i} (seq {perm[i]})")
