@@ -714,6 +714,7 @@ pa_status pa_share_groups(const int32_t *block_tables, int32_t max_blocks_per_se
                           int32_t mode, int32_t *skip, int32_t *groups, int32_t *order,
                           void *stream)
 {
+    const NvtxRange range("pa_share_groups");
     if (num_seqs < 0 || num_seqs > kMaxSeqs || max_blocks_per_seq <= 0 || mode < 1 || mode > 2)
         return PA_ERR_SHAPE;
     if (g != 1 && g != 2 && g != 4 && g != 8)
