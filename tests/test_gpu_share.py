@@ -203,3 +203,26 @@ def test_shared_prefix_full_size_int8_workload_shuffled():
     for i in (0, 9, 22, w.B - 1):
         ref, _ = oracle_one_sequence(w, int(perm[i]), gen_device=DEV)
         assert_close(out[i], ref, f"int8 prefix shuffled position {i} (seq {perm[i]})")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "int8"])
+def test_shared_prefix_maximum_batch_interleaved(kv_dtype):
+    # 8192 sequences, 1024 groups of 8 spread over the batch (member j of
+    # group k at position j * 1024 + k), share_prefix=2: the detection sorts
+    # 8192 keys; every group is found and the output equals the oracle's
+    rng = np.random.default_rng(9)
+    B = 8192
+    groups = np.tile(np.arange(B // 8), 8)
+    prefix = np.full(B, 128)
+    suffix = rng.integers(1, 50, B)
+    w = make_workload("share_maxb_il", Geometry(n_h=4, n_kv=2, d_h=64, kv_dtype=kv_dtype),
+                      (prefix + suffix).tolist(), 19, prefix_len=prefix.tolist(),
+                      group=groups.tolist())
+    pool = gpu_pool(w, DEV)
+    ref, _ = oracle_full(w)
+    out, st = run(w, pool, share=2)
+    assert st == 0
+    assert_close(out, ref, f"{kv_dtype} B=8192 interleaved shared")
+    found = detected_groups(w, 2)
+    assert len(found) == B // 8
+    assert all(len(m) == 8 and s == 8 and len({groups[b] for b in m}) == 1 for m, s in found)
