@@ -226,3 +226,75 @@ def test_shared_prefix_maximum_batch_interleaved(kv_dtype):
     found = detected_groups(w, 2)
     assert len(found) == B // 8
     assert all(len(m) == 8 and s == 8 and len({groups[b] for b in m}) == 1 for m, s in found)
+
+
+def reference_groups(bt, cl, g, mode, min_blocks=8):
+    """The grouping rules of pa_share_groups restated in plain Python (lists
+    of ints): order, lcp with the previous sequence in that order, runs of
+    lcp >= min_blocks cut into chunks of at most gm members."""
+    B, max_blocks = bt.shape
+    gm = 8 if g <= 2 else 16 // g
+    nb = [(int(c) + 15) // 16 if 0 < int(c) <= max_blocks * 16 else 0 for c in cl]
+
+    def fnv(entries):
+        h = 2166136261
+        for e in entries:
+            h = ((h ^ (int(e) & 0xFFFFFFFF)) * 16777619) & 0xFFFFFFFF
+        return h
+
+    if mode == 2:
+        order = [i for _, i in sorted(
+            ((fnv(bt[i, :min_blocks]) if nb[i] > min_blocks else 0xFFFFFFFF), i) for i in range(B))]
+    else:
+        order = list(range(B))
+    lcp = [0] * B
+    for p in range(1, B):
+        s0, s1 = order[p - 1], order[p]
+        lim = max(0, min(nb[s0], nb[s1]) - 1)
+        l = 0
+        while l < lim and bt[s0, l] == bt[s1, l]:
+            l += 1
+        lcp[p] = l
+    skip, groups = [0] * B, []
+    start = 0
+    for p in range(B):
+        if p == 0 or lcp[p] < min_blocks:
+            start = p
+        if (p - start) % gm:
+            continue
+        n, S = 1, None
+        while n < gm and p + n < B and lcp[p + n] >= min_blocks:
+            S = lcp[p + n] if S is None else min(S, lcp[p + n])
+            n += 1
+        if n >= 2:
+            groups.append((p, n, S))
+            for j in range(n):
+                skip[order[p + j]] = S
+    return skip, groups, order
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("seed", range(6))
+def test_share_groups_match_the_rules(mode, seed):
+    # random tables: sequences copy a random partner's leading blocks (3 to
+    # 40 of them, so some share fewer than 8), contexts ragged, a few empty
+    rng = np.random.default_rng(400 + seed)
+    B, max_blocks = int(rng.integers(2, 300)), 64
+    g = int(rng.choice([1, 2, 4, 8]))
+    bt = rng.permutation(B * max_blocks).reshape(B, max_blocks).astype(np.int32)
+    cl = rng.integers(0, max_blocks * 16 + 1, B).astype(np.int32)
+    cl[rng.random(B) < 0.05] = 0
+    for b in range(1, B):
+        if rng.random() < 0.6:
+            src = int(rng.integers(0, b))
+            k = int(rng.integers(3, 41))
+            bt[b, :k] = bt[src, :k]
+    skip, grp, order = pa.pa_share_groups(torch.from_numpy(bt).to(DEV), torch.from_numpy(cl).to(DEV),
+                                          g, mode)
+    torch.cuda.synchronize()
+    rskip, rgroups, rorder = reference_groups(bt, cl, g, mode)
+    assert order.cpu().numpy().tolist() == rorder
+    assert skip.cpu().numpy().tolist() == rskip
+    grp = grp.cpu().numpy()
+    assert [tuple(int(x) for x in r) for r in grp[:len(rgroups)]] == rgroups
+    assert not grp[len(rgroups):].any()
