@@ -774,7 +774,8 @@ __device__ __forceinline__ void arrive_sequences(const DecodeParams &p, const in
         if (last[j])
             merge_run<D, GQ, MR::RUN, MR::RB>(p, seq[j], kvh, cf[j], ns[j], k / D, k % D);
     }
-    __syncthreads(); // misc is reused by the next segment
+    // (misc is next written after the two CTA barriers that open the next
+    // segment's merge, so no barrier is needed here)
 }
 
 template <int D, int GQ, int NW>
@@ -861,10 +862,8 @@ __device__ __forceinline__ void finish_fused(const DecodeParams &p, const int32_
         misc[3] = nseg;
     }
     __syncthreads();
-    if (!misc[0]) {
-        __syncthreads(); // misc is reused by the next segment
-        return;
-    }
+    if (!misc[0])
+        return; // (misc is next written after the next segment's barriers)
     const int64_t c_first = misc[1];
     const int nseg = misc[3];
     const int b0 = __ldg(p.groups + 3 * s), n = __ldg(p.groups + 3 * s + 1);
